@@ -1,0 +1,180 @@
+/*
+ * kq.h -- C ABI of libkq: fused dequantise-and-multiply of K-quant weights
+ * against 1..16 bf16 activation rows on one NVIDIA B300 (sm_103a).
+ *
+ * What the operation is.  The daily.dev summary "Fast on-device agentic AI
+ * with Muse Glimmer on ExecuTorch" (answer "How does ExecuTorch export Muse
+ * Glimmer GGUF checkpoints for CUDA and Apple Silicon?") says the CUDA backend
+ * runs GGUF Q4_K/Q5_K/Q6_K weights directly as packed integer GEMV kernels and
+ * that adjacent sub-blocks with the same scale/min are merged, when lossless,
+ * into groups of up to 128.  The SGLang day-0 post on Muse Glimmer (paragraph
+ * on the GGUF checkpoints) names the "Q4KM format with a group size of 128".
+ * The Core AI model card for Muse-Glimmer-30B (first table and the sentence
+ * under it) shows decode streaming every weight once per token (23.7 tok/s x
+ * 17.9 GB = 424 GB/s), i.e. the product y = W x is weight-bandwidth bound.
+ *
+ * Every function computes, for t < n_tok and n < N_out,
+ *     y[t][n] = sum_k  w^[n][k] * x[t][k]
+ * where w^ is the dequantised weight defined by the record layouts below.
+ *
+ * Record layouts (all little-endian; a row of K weights is K/256
+ * consecutive super-blocks; rows are stored one after another):
+ *
+ *  KQ_Q4_K (144 B / 256 weights)
+ *     [0,2) d (fp16)  [2,4) dmin (fp16)  [4,16) scales[12]  [16,144) qs[128]
+ *     sub-block j (0..7) has a 6-bit scale sc_j and 6-bit min m_j:
+ *       j < 4 : sc_j = scales[j] & 63,           m_j = scales[j+4] & 63
+ *       j >= 4: sc_j = (scales[j+4] & 15) | ((scales[j-4] >> 6) << 4)
+ *               m_j  = (scales[j+4] >> 4) | ((scales[j]   >> 6) << 4)
+ *     weight i (0..255): c = i/64, r = i%64;
+ *       r < 32 : q = qs[32c+r] & 15,     j = 2c
+ *       r >= 32: q = qs[32c+r-32] >> 4,  j = 2c+1
+ *     w^ = d*sc_j*q - dmin*m_j
+ *  KQ_Q5_K (176 B / 256 weights)
+ *     [0,2) d  [2,4) dmin  [4,16) scales[12] (as Q4_K)  [16,48) qh[32]
+ *     [48,176) qs[128];  weight i: c = i/64, r = i%64, l = r%32;
+ *       low nibble as Q4_K (qs[32c+l], low half if r<32 else high half),
+ *       fifth bit = (qh[l] >> (2c + (r>=32))) & 1,  q = nibble | bit<<4
+ *     w^ = d*sc_j*q - dmin*m_j
+ *  KQ_Q6_K (210 B / 256 weights)
+ *     [0,128) ql  [128,192) qh  [192,208) scales[16] (int8)  [208,210) d
+ *     weight i: h = i/128, t = (i%128)/32, l = i%32;
+ *       nibble = ql[64h + l + 32*(t&1)], low half if t<2 else high half
+ *       2 high bits = (qh[32h + l] >> 2t) & 3,  q = nibble | hb<<4
+ *     w^ = d*scales[i/16]*(q-32)
+ *  KQ_Q4_G128 (136 B / 256 weights, planar; this library's merged layout)
+ *     one buffer = [q plane: N_out*K/2 bytes][param plane: N_out*K/256*8 B]
+ *     q plane: per super-block 128 B laid out exactly as Q4_K's qs;
+ *     param plane: per super-block 8 B {d fp16, dmin fp16, sc0, sc1, m0, m1};
+ *     group g = i/128 (sub-blocks 4g..4g+3 of the Q4_K it came from)
+ *     w^ = d*sc_g*q - dmin*m_g
+ *
+ * Conventions for every entry point.
+ *   - The caller owns all memory.  No entry point allocates device memory.
+ *   - Device pointers: W_blocks must be 16-byte aligned; x is bf16
+ *     [n_tok][K] with contiguous rows (x must be 16-byte aligned and K a
+ *     multiple of 256); y is fp32 [n_tok][N_out] and is overwritten.
+ *   - Requirements: K % 256 == 0, K > 0, N_out > 0, 1 <= n_tok <= 16.  A
+ *     violation returns a status before anything is launched.
+ *   - Calls on a stream are asynchronous, never synchronise, and may be
+ *     captured into a CUDA graph.
+ *   - A CUDA launch failure returns KQ_ERR_CUDA.  Nothing throws or exits
+ *     across this ABI.  NaN/Inf inputs give unspecified (but in-bounds)
+ *     results.
+ */
+#ifndef KQ_H
+#define KQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* kq_stream_t;
+
+typedef enum {
+  KQ_Q4_K = 0,    /* 4-bit q, 8 sub-blocks of 32, 6-bit sc/m, fp16 d/dmin */
+  KQ_Q5_K = 1,    /* as Q4_K with a fifth bit per weight                   */
+  KQ_Q6_K = 2,    /* 6-bit q, 16 sub-blocks of 16, int8 sc, fp16 d          */
+  KQ_Q4_G128 = 3  /* Q4_K with one (sc, m) per 128 weights, planar          */
+} kq_format;
+
+typedef enum {
+  KQ_OK = 0,
+  KQ_ERR_ARG = 1,           /* null pointer, bad enum, n_tok out of range  */
+  KQ_ERR_SHAPE = 2,         /* K % 256 != 0, non-positive sizes, mismatch  */
+  KQ_ERR_ALIGN = 3,         /* a device pointer is not 16-byte aligned     */
+  KQ_ERR_NOT_MERGEABLE = 4, /* kq_merge_g128: sub-blocks differ in (sc, m) */
+  KQ_ERR_RANGE = 5,         /* kq_quantize: a scale exceeds fp16 range     */
+  KQ_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed        */
+  KQ_ERR_UNSUPPORTED = 7    /* valid request this build cannot serve       */
+} kq_status;
+
+/* Bytes of one 256-weight super-block: 144 / 176 / 210 / 136.  0 for a bad
+ * format. */
+size_t kq_block_bytes(kq_format f);
+
+/* Bytes of an N_out x K matrix in format f (N_out*K/256 super-blocks; for
+ * KQ_Q4_G128 both planes).  0 if the shape is invalid. */
+size_t kq_matrix_bytes(kq_format f, int64_t N_out, int64_t K);
+
+/* y[t][n] = sum_k w^[n][k] x[t][k] for t < n_tok, n < N_out.
+ *   W_blocks : device, the N_out x K matrix in format f, 16-B aligned
+ *   x_bf16   : device, bf16 [n_tok][K], 16-B aligned
+ *   y        : device, fp32 [n_tok][N_out], overwritten
+ * Accumulates in fp32.  Source: the daily.dev ExecuTorch summary, answer on
+ * exporting GGUF checkpoints (Q4_K/Q5_K/Q6_K GEMV; group-128 merge). */
+kq_status kq_gemv(kq_format f, const void* W_blocks, const void* x_bf16,
+                  float* y, int64_t N_out, int64_t K, int n_tok,
+                  kq_stream_t stream);
+
+/* One decoder layer's seven projections.  The Muse-Glimmer-30B Core AI card
+ * ("The architecture, and what the port had to do about it") and the SGLang
+ * day-0 post (architecture paragraph) describe GQA attention (q, k, v read the
+ * same hidden state; o reads the attention output) and a SwiGLU FFN (gate, up
+ * read the same hidden state; down reads their product).  kq_layer_step runs
+ * q/k/v as one launch on x_attn, then o on x_o, gate/up as one launch on
+ * x_ffn, then down on x_down, in that order on `stream`. */
+typedef struct {
+  kq_format format;
+  const void* W;   /* device, 16-B aligned */
+  int64_t N_out;
+  int64_t K;
+} kq_matrix;
+
+typedef struct {
+  kq_matrix q, k, v, o, gate, up, down;
+} kq_layer;
+
+typedef struct {
+  const void* x_attn;  /* bf16 [n_tok][q.K]    -> q, k, v    */
+  const void* x_o;     /* bf16 [n_tok][o.K]    -> o          */
+  const void* x_ffn;   /* bf16 [n_tok][gate.K] -> gate, up   */
+  const void* x_down;  /* bf16 [n_tok][down.K] -> down       */
+  float *y_q, *y_k, *y_v, *y_o, *y_gate, *y_up, *y_down; /* fp32 [n_tok][N] */
+} kq_layer_io;
+
+/* Requirements: q.K == k.K == v.K, gate.K == up.K, gate.N_out == up.N_out,
+ * plus each matrix's own requirements.  Returns the first failing status;
+ * on a validation failure nothing is launched. */
+kq_status kq_layer_step(const kq_layer* L, const kq_layer_io* io, int n_tok,
+                        kq_stream_t stream);
+
+/* W_out[n][k] = w^[n][k] as fp32 (device, [N_out][K]).  Every w^ of these
+ * formats is computed with at most one rounding (at the subtraction of the
+ * min term), so the result is bit-exact: the fp32 round-to-nearest-even of
+ * the exact value. */
+kq_status kq_dequantize(kq_format f, const void* W_blocks, float* W_out,
+                        int64_t N_out, int64_t K, kq_stream_t stream);
+
+/* Host-side quantiser for test and benchmark data (runs on the CPU, not on
+ * the hot path).  W_host: fp32 [N_out][K]; blocks_host receives
+ * kq_matrix_bytes(f, N_out, K) bytes.  Rounds q to nearest (ties to even)
+ * and rounds d, dmin up to fp16 so every group's range is covered, which
+ * bounds |w - w^| by half a quantisation step.  Q4_G128 takes its statistics
+ * over 128-weight groups.  Returns KQ_ERR_RANGE if a scale exceeds fp16. */
+kq_status kq_quantize(kq_format f, const float* W_host, int64_t N_out,
+                      int64_t K, void* blocks_host);
+
+/* Host-side lossless merge of Q4_K blocks into the KQ_Q4_G128 layout.
+ * Succeeds only if, in every super-block, sub-blocks 0..3 share one (sc, m)
+ * and sub-blocks 4..7 share one (sc, m); otherwise returns
+ * KQ_ERR_NOT_MERGEABLE and leaves g128_host unspecified.  The merged matrix
+ * dequantises to bit-identical weights.  Source: the daily.dev ExecuTorch
+ * summary (merge "when lossless" up to 128) and the SGLang post ("Q4KM ...
+ * group size of 128"). */
+kq_status kq_merge_g128(const void* q4k_host, int64_t N_out, int64_t K,
+                        void* g128_host);
+
+/* Static string for a status code. */
+const char* kq_status_str(kq_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KQ_H */
