@@ -1,0 +1,470 @@
+"""Benchmark: weight-streaming throughput of the whole decode step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--n-tok T] [--impl kq|reference]
+
+One step = the weight GEMVs of one decode step of the 52-layer decoder
+(per layer: q/k/v, o, gate/up in Q4_K and down in Q6_K; hidden 5120,
+intermediate 32768) plus a Q6_K LM head 200000 x 5120 -- 19.1 GB of packed
+weights streamed once -- captured as one CUDA graph.  The metric is weight
+GB/s (packed bytes streamed per second); microseconds per step and the
+equivalent tokens/s are reported beside it.  Inputs are synthetic (seeded);
+the 19.1 GB working set is far larger than L2, so no flush is needed.
+
+N > 1 (torchrun): every rank runs an independent replica on its own GPU
+(the path has no exchange step); value = total bytes of all ranks / the
+slowest rank's time.  --impl reference times the CPU oracle on a bounded
+sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "K-quant GEMV weight GB/s (% of B300 HBM peak) at 1/8 tokens; us per decode step"
+WORKLOAD = "decode_step_52L_h5120_i32768_q4k_q6k_lmhead200000"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--n-tok", type=int, default=1)
+    p.add_argument("--impl", default="kq", choices=["kq", "reference"])
+    p.add_argument("--layers", type=int, default=wl.LAYERS)
+    p.add_argument("--no-extra", action="store_true", help="skip the n_tok=8 line and e2e")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return rank, local, world
+
+
+def init_dist(world):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("gloo")
+        return dist
+    return None
+
+
+def max_over_ranks(dist, v: float) -> float:
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, v: float) -> float:
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return json.load(fh), "measured"
+    except OSError:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quant_weight_gemv_dequant_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as fh:
+                h.update(name.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel)
+    if not e or e.get("kernel_src_sha") != kernel_source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ inputs
+
+def build_pools_library(device):
+    """Pools of N(0, 0.02) super-blocks quantised by the library's host
+    quantiser (identical bytes to the oracle's, tested)."""
+    import torch
+    import quant_weight_gemv_dequant_b300 as kq
+    pw = wl.pool_weights(wl.derive_seed(900), wl.POOL_BLOCKS)
+    return {f: torch.from_numpy(kq.kq_quantize(f, pw, wl.POOL_BLOCKS, 256)).to(device)
+            for f in (wl.Q4_K, wl.Q6_K)}
+
+
+def build_step(pools_dev, n_tok, layers, device):
+    import torch
+    from quant_weight_gemv_dequant_b300.decode_step import DecodeStep
+    Ls = []
+    for l in range(layers):
+        L = {}
+        for i, m in enumerate(wl.DECODE_LAYER):
+            seed = wl.derive_seed(5, l, i)
+            L[m.name] = (m.fmt, wl.tile_matrix_device(pools_dev[m.fmt], m.fmt, seed, m.N, m.K), m.N, m.K)
+        Ls.append(L)
+    h = wl.LM_HEAD
+    head = (h.fmt, wl.tile_matrix_device(pools_dev[h.fmt], h.fmt, wl.derive_seed(5, 999), h.N, h.K), h.N, h.K)
+    step = DecodeStep(Ls, head, n_tok, device=device)
+    host_x = []
+    for l in range(layers):
+        for j, key in enumerate(("x_attn", "x_o", "x_ffn", "x_down")):
+            xb = wl.activations_bf16(wl.derive_seed(5, l, 100 + j), n_tok, step.x[l][key].shape[1])
+            t = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
+            step.x[l][key].copy_(t)
+            host_x.append((t, step.x[l][key]))
+    xb = wl.activations_bf16(wl.derive_seed(5, 998), n_tok, h.K)
+    t = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    step.x_head.copy_(t)
+    host_x.append((t, step.x_head))
+    torch.cuda.synchronize()
+    return step, host_x
+
+
+def io_bytes(step):
+    xb = sum(t.numel() * 2 for xs in step.x for t in xs.values()) + step.x_head.numel() * 2
+    yb = sum(t.numel() * 4 for ys in step.y for t in ys.values()) + step.y_head.numel() * 4
+    return xb, yb
+
+
+def time_graph(g, stream, steps, warmup, dist):
+    import torch
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    return e0.elapsed_time(e1) / 1e3 / steps
+
+
+def dominant_kernel_timing(step, steps, warmup, stream):
+    """Average duration of the dominant launch (the grouped gate/up Q4_K GEMV
+    of each layer): a graph of the step's own gate/up launches, timed with
+    events on the launching stream."""
+    import torch
+    import quant_weight_gemv_dequant_b300 as kq
+    g = torch.cuda.CUDAGraph()
+    lay = step.layers
+
+    def run():
+        for l, L in enumerate(lay):
+            f, Wg, N, K = L["gate"]
+            kq.kq_gemv_multi(f, [Wg, L["up"][1]], [step.y[l]["gate"], step.y[l]["up"]], [N, L["up"][2]],
+                             step.x[l]["x_ffn"], K, step.n_tok, stream)
+
+    with torch.cuda.stream(stream):
+        run()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        run()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = len(lay)
+    dur = e0.elapsed_time(e1) / 1e3 / (steps * launches)
+    L0 = lay[0]
+    nbytes = (L0["gate"][1].numel() + L0["up"][1].numel() + step.x[0]["x_ffn"].numel() * 2
+              + (L0["gate"][2] + L0["up"][2]) * 4 * step.n_tok)
+    return dur, nbytes, "gemv_q4k_gate_up"
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_samples(pools_host, rounds: int, n_tok: int = 1):
+    """Inputs for the oracle timing: per round, 2 sampled rows of each of the
+    7 layer matrices (layer = round index) and of the LM head, same tiling
+    and activations as the GPU step."""
+    mats = list(enumerate(wl.DECODE_LAYER)) + [(999, wl.LM_HEAD)]
+    xs = {}
+    out = []
+    for r in range(rounds):
+        for i, m in mats:
+            seed = wl.derive_seed(5, r % wl.LAYERS, i) if i != 999 else wl.derive_seed(5, 999)
+            rows = (wl.splitmix64(seed, np.arange(2, dtype=np.uint64)) % np.uint64(m.N)).astype(np.int64)
+            sub = wl.tiled_rows(pools_host[m.fmt], m.fmt, seed, m.N, m.K, rows)
+            if m.K not in xs:
+                xs[m.K] = wl.activations_bf16(wl.derive_seed(5, 0, 100), n_tok, m.K)
+            out.append((m.fmt, sub, len(rows), m.K, xs[m.K]))
+    return out
+
+
+def oracle_sample_rate(samples, budget_s: float):
+    """Weight GB/s of the single-threaded fp64 oracle over the samples,
+    cycling through them for about budget_s seconds (only oracle calls are
+    inside the timed region)."""
+    import oracle
+    done_bytes, el, k = 0, 0.0, 0
+    while el < budget_s:
+        fmt, sub, n, K, x = samples[k % len(samples)]
+        t0 = time.perf_counter()
+        oracle.gemv(fmt, sub, n, K, x)
+        el += time.perf_counter() - t0
+        done_bytes += sub.size
+        k += 1
+    return done_bytes / el / 1e9, el, done_bytes
+
+
+def oracle_pools():
+    import oracle
+    pw = wl.pool_weights(wl.derive_seed(900), wl.POOL_BLOCKS)
+    return {f: oracle.quantize(f, pw, wl.POOL_BLOCKS, 256) for f in (wl.Q4_K, wl.Q6_K)}
+
+
+# ------------------------------------------------------------------- arms
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    samples = oracle_samples(oracle_pools(), 8, args.n_tok)
+    step_bytes = wl.decode_step_bytes(args.layers)
+    per_step = []
+    for _ in range(args.warmup):
+        oracle_sample_rate(samples, 0.2)
+    for _ in range(args.steps):
+        gbs, el, nb = oracle_sample_rate(samples, 1.0)
+        per_step.append((gbs, el, nb))
+    tot_b = sum(p[2] for p in per_step)
+    tot_t = sum(p[1] for p in per_step)
+    value = tot_b / tot_t / 1e9
+    ms = step_bytes / (value * 1e9) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "n_tok": args.n_tok, "layers": args.layers,
+                   "weight_bytes_per_step": step_bytes},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"2 sampled rows of each of the 7 matrices of 8 layers and of the LM head, "
+                                   f"cycled for ~1 s of single-threaded fp64 oracle per step; {tot_b} packed "
+                                   f"bytes total; ms_per_step extrapolates to the full 19.1 GB step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_kq(args):
+    import torch
+    rank, local, world = dist_env()
+    dist = init_dist(world)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import quant_weight_gemv_dequant_b300 as kq
+    kq.lib()
+
+    pools = build_pools_library(device)
+    step, host_x = build_step(pools, args.n_tok, args.layers, device)
+    stream = torch.cuda.Stream(device=device)
+    g = step.capture(stream)
+    wbytes = step.weight_bytes()
+    xb, yb = io_bytes(step)
+
+    with ClockSampler(local) as clk:
+        t_step = time_graph(g, stream, args.steps, max(3, args.warmup), dist)
+    t_max = max_over_ranks(dist, t_step)
+    total_bytes = sum_over_ranks(dist, float(wbytes))
+    value = total_bytes / t_max / 1e9
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+
+    extra = {}
+    if not args.no_extra and args.n_tok == 1:
+        # n_tok = 8 (speculative verify) on the same weights
+        s8 = type(step)(step.layers, step.lm_head, 8, device=device)
+        for l in range(args.layers):
+            for j, key in enumerate(("x_attn", "x_o", "x_ffn", "x_down")):
+                xb8 = wl.activations_bf16(wl.derive_seed(5, l, 200 + j), 8, s8.x[l][key].shape[1])
+                s8.x[l][key].copy_(torch.from_numpy(xb8.view(np.int16)).view(torch.bfloat16))
+        g8 = s8.capture(stream)
+        t8 = max_over_ranks(dist, time_graph(g8, stream, args.steps, 3, dist))
+        extra["n_tok_8"] = {"ms_per_step": t8 * 1e3, "weight_gb_s": wbytes / t8 / 1e9 * world,
+                            "pct_of_hbm_peak": 100 * wbytes / t8 / 1e9 / hbm,
+                            "tok_per_s": 8 / t8 * world}
+        del g8, s8
+
+    # dominant kernel: grouped gate/up Q4_K GEMV launches
+    dur, kbytes, kname = dominant_kernel_timing(step, args.steps, 3, stream)
+    achieved = kbytes / dur / 1e9
+
+    # end to end through the public API with host buffers: per step, H2D of
+    # every activation input from pinned memory, the graph, D2H of the logits
+    e2e = None
+    if not args.no_extra:
+        y_host = torch.empty(step.y_head.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * 2 for t, _ in host_x)
+        d2h = y_host.numel() * 4
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for h, d in host_x:
+                    d.copy_(h, non_blocking=True)
+                g.replay()
+                y_host.copy_(step.y_head, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(3):
+            e2e_step()
+        barrier(dist)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        te = max_over_ranks(dist, (time.perf_counter() - t0) / args.steps)
+        e2e = {"value": total_bytes / te / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": te * 1e3}
+
+    cpu = None
+    if rank == 0 and not args.no_extra:
+        gbs, el, nb = oracle_sample_rate(oracle_samples(oracle_pools(), 8, args.n_tok), 12.0)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"single-threaded fp64 oracle on 2 sampled rows of each of the 7 matrices of 8 "
+                         f"layers and of the LM head, cycled for {el:.1f} s ({nb} packed bytes)"}
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": t_max * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "n_tok": args.n_tok, "layers": args.layers,
+                       "weight_bytes_per_step": wbytes, "x_bytes": xb, "y_bytes": yb,
+                       "l2": "inputs larger than L2 (19.1 GB weights per step)",
+                       "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}"},
+            "us_per_step": t_max * 1e6, "tok_per_s": args.n_tok / t_max * world,
+            "pct_of_hbm_peak": 100 * value / world / hbm,
+            "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": hbm,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": profiled_traffic(kname), "bytes_per_launch": kbytes,
+                         "launch_us": dur * 1e6},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": step.launches() * args.steps,
+            "clocks": clocks, **extra,
+        }
+        print(json.dumps(line), flush=True)
+    barrier(dist)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_kq(args)
+
+
+if __name__ == "__main__":
+    main()

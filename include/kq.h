@@ -112,6 +112,20 @@ kq_status kq_gemv(kq_format f, const void* W_blocks, const void* x_bf16,
                   float* y, int64_t N_out, int64_t K, int n_tok,
                   kq_stream_t stream);
 
+/* Several matrices of one format and one K that read the same activations,
+ * computed in ONE launch: y_i = w^_i x for i < count (1 <= count <= 4).  The
+ * Core AI card for Muse-Glimmer-30B ("The architecture, and what the port had
+ * to do about it") folds q, k, v and the sigmoid attention gate, which all
+ * read the pre-attention hidden state, into one qkvg projection; the SwiGLU
+ * gate and up projections share their input the same way.
+ *   W[i]     : device, N_out[i] x K matrix in format f, 16-B aligned
+ *   y[i]     : device, fp32 [n_tok][N_out[i]], overwritten
+ *   x_bf16   : device, bf16 [n_tok][K], 16-B aligned
+ * Same requirements and statuses as kq_gemv for each matrix. */
+kq_status kq_gemv_multi(kq_format f, int count, const void* const* W, float* const* y,
+                        const int64_t* N_out, const void* x_bf16, int64_t K, int n_tok,
+                        kq_stream_t stream);
+
 /* One decoder layer's seven projections.  The Muse-Glimmer-30B Core AI card
  * ("The architecture, and what the port had to do about it") and the SGLang
  * day-0 post (architecture paragraph) describe GQA attention (q, k, v read the

@@ -156,11 +156,9 @@ def tiled_rows(pool: np.ndarray, fmt: int, seed: int, N: int, K: int, rows) -> n
     P = pool.size // nb
     nsb = K // 256
     pb = pool.reshape(P, nb)
-    out = []
-    for r in np.asarray(rows, dtype=np.int64):
-        idx = tile_indices(seed, nsb, P, start=int(r) * nsb)
-        out.append(pb[idx].reshape(-1))
-    return np.concatenate(out)
+    a, c = tile_params(seed, P)
+    i = np.asarray(rows, dtype=np.int64)[:, None] * nsb + np.arange(nsb, dtype=np.int64)[None, :]
+    return pb[(i * a + c) & (P - 1)].reshape(-1)
 
 
 def pool_weights(seed: int, pool_blocks: int) -> np.ndarray:
@@ -215,3 +213,30 @@ def decode_step_weights(layers: int = LAYERS) -> int:
 def weight_gb_per_s(weight_bytes: float, seconds: float) -> float:
     """Weight traffic in GB/s (1 GB = 1e9 bytes) for bytes streamed per step."""
     return weight_bytes / seconds / 1e9
+
+
+# ------------------------------------------------------ device-side tiling
+
+POOL_BLOCKS = 1 << 17
+
+
+def tile_matrix_device(pool_dev, fmt: int, seed: int, N: int, K: int, out=None):
+    """Device bytes of a tiled N x K matrix: super-block i is pool block
+    (a*i + c) mod P (torch gather on the GPU; same map as tiled_rows)."""
+    import torch
+    assert fmt != Q4_G128
+    nb = BLOCK_BYTES[fmt]
+    P = pool_dev.numel() // nb
+    nblk = N * (K // 256)
+    a, c = tile_params(seed, P)
+    pb = pool_dev.view(P, nb)
+    if out is None:
+        out = torch.empty(nblk * nb, dtype=torch.uint8, device=pool_dev.device)
+    ov = out.view(nblk, nb)
+    step = 1 << 22
+    for s in range(0, nblk, step):
+        m = min(step, nblk - s)
+        i = torch.arange(s, s + m, dtype=torch.int64, device=pool_dev.device)
+        idx = (i * a + c) & (P - 1)
+        torch.index_select(pb, 0, idx, out=ov[s:s + m])
+    return out
