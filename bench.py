@@ -226,18 +226,22 @@ def io_bytes(step):
 
 
 def time_graph(g, stream, steps, warmup, dist):
+    """Seconds per replay: events recorded on the stream the graph is
+    launched on (CUDAGraph.replay launches on the current stream)."""
     import torch
-    for _ in range(warmup):
-        g.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
     torch.cuda.synchronize()
     barrier(dist)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        g.replay()
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
     torch.cuda.synchronize()
     barrier(dist)
     return e0.elapsed_time(e1) / 1e3 / steps
@@ -263,18 +267,9 @@ def dominant_kernel_timing(step, steps, warmup, stream):
     torch.cuda.synchronize()
     with torch.cuda.graph(g, stream=stream):
         run()
-    for _ in range(warmup):
-        g.replay()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        g.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    dur_total = time_graph(g, stream, steps, warmup, None)
     launches = len(lay)
-    dur = e0.elapsed_time(e1) / 1e3 / (steps * launches)
+    dur = dur_total / launches
     L0 = lay[0]
     nbytes = (L0["gate"][1].numel() + L0["up"][1].numel() + step.x[0]["x_ffn"].numel() * 2
               + (L0["gate"][2] + L0["up"][2]) * 4 * step.n_tok)

@@ -91,7 +91,8 @@ typedef enum {
   KQ_ERR_NOT_MERGEABLE = 4, /* kq_merge_g128: sub-blocks differ in (sc, m) */
   KQ_ERR_RANGE = 5,         /* kq_quantize: a scale exceeds fp16 range     */
   KQ_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed        */
-  KQ_ERR_UNSUPPORTED = 7    /* valid request this build cannot serve       */
+  KQ_ERR_UNSUPPORTED = 7,   /* valid request this build cannot serve       */
+  KQ_ERR_TIMEOUT = 8        /* a kernel's bounded wait ran out (see below) */
 } kq_status;
 
 /* Bytes of one 256-weight super-block: 144 / 176 / 210 / 136.  0 for a bad
@@ -183,6 +184,16 @@ kq_status kq_quantize(kq_format f, const float* W_host, int64_t N_out,
  * group size of 128"). */
 kq_status kq_merge_g128(const void* q4k_host, int64_t N_out, int64_t K,
                         void* g128_host);
+
+/* Device-side health check.  The streaming kernels hand data between warps
+ * through shared-memory barriers; every wait is bounded (about two seconds),
+ * and a wait that runs out makes the kernel stop early and count the event
+ * in a device word instead of hanging.  This call synchronises `stream`,
+ * reads and clears that count, and returns KQ_ERR_TIMEOUT if it was non-zero
+ * (the outputs of the kernels since the previous call are then not valid),
+ * KQ_ERR_CUDA if the read failed, KQ_OK otherwise.  Not for use inside
+ * stream capture. */
+kq_status kq_device_status(kq_stream_t stream);
 
 /* Static string for a status code. */
 const char* kq_status_str(kq_status s);

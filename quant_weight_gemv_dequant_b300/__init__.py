@@ -21,7 +21,7 @@ FORMATS = {"Q4_K": Q4_K, "Q5_K": Q5_K, "Q6_K": Q6_K, "Q4_G128": Q4_G128}
 KQ_OK = 0
 STATUS_NAMES = {0: "KQ_OK", 1: "KQ_ERR_ARG", 2: "KQ_ERR_SHAPE", 3: "KQ_ERR_ALIGN",
                 4: "KQ_ERR_NOT_MERGEABLE", 5: "KQ_ERR_RANGE", 6: "KQ_ERR_CUDA",
-                7: "KQ_ERR_UNSUPPORTED"}
+                7: "KQ_ERR_UNSUPPORTED", 8: "KQ_ERR_TIMEOUT"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkq.so")
@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
         L.kq_dequantize.argtypes = [I, P, P, I64, I64, P]
         L.kq_quantize.argtypes = [I, P, I64, I64, P]
         L.kq_merge_g128.argtypes = [P, I64, I64, P]
+        L.kq_device_status.argtypes = [P]
+        L.kq_device_status.restype = I
         L.kq_status_str.argtypes = [I]
         L.kq_status_str.restype = ctypes.c_char_p
         for name in ("kq_gemv", "kq_gemv_multi", "kq_layer_step", "kq_dequantize", "kq_quantize", "kq_merge_g128"):
@@ -104,6 +106,12 @@ def kq_status_str(status: int) -> str:
         return lib().kq_status_str(status).decode()
     except KqError:
         return STATUS_NAMES.get(status, "unknown")
+
+
+def kq_device_status(stream=None, check=True) -> int:
+    """Synchronise the stream and report whether any bounded wait timed out."""
+    st = lib().kq_device_status(_stream(stream))
+    return _check(st, "kq_device_status") if check else st
 
 
 def kq_block_bytes(fmt: int) -> int:

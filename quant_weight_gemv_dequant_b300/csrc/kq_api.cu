@@ -136,4 +136,10 @@ kq_status kq_dequantize(kq_format f, const void* W_blocks, float* W_out, int64_t
   return launch_status();
 }
 
+kq_status kq_device_status(kq_stream_t stream) {
+  unsigned int n = 0;
+  if (!kq::read_wait_timeouts(&n, reinterpret_cast<cudaStream_t>(stream))) return KQ_ERR_CUDA;
+  return n != 0 ? KQ_ERR_TIMEOUT : KQ_OK;
+}
+
 }  // extern "C"

@@ -240,6 +240,9 @@ void launch_f(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStrea
 
 bool launch_gemv(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
                  cudaStream_t s) {
+  // the streaming kernel serves n_tok <= 4 while x fits in shared memory;
+  // everything else takes the warp-per-row kernel below
+  if (n_tok <= 4 && launch_stream(fmt, g, x, K, n_tok, s)) return true;
   switch (fmt) {
     case kQ4K: launch_f<kQ4K>(g, x, K, n_tok, s); return true;
     case kQ5K: launch_f<kQ5K>(g, x, K, n_tok, s); return true;

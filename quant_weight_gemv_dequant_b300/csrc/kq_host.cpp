@@ -246,6 +246,7 @@ const char* kq_status_str(kq_status s) {
     case KQ_ERR_RANGE: return "a scale exceeds the fp16 range";
     case KQ_ERR_CUDA: return "CUDA runtime or launch error";
     case KQ_ERR_UNSUPPORTED: return "unsupported request";
+    case KQ_ERR_TIMEOUT: return "a kernel's bounded shared-memory wait timed out";
   }
   return "unknown status";
 }

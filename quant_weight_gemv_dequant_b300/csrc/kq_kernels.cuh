@@ -22,6 +22,13 @@ struct GemvGroup {
 bool launch_gemv(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
                  cudaStream_t stream);
 
+// The streaming kernel (n_tok <= 4); false if it does not serve the request.
+bool launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
+                   cudaStream_t stream);
+
+// Number of bounded waits that timed out since the last call (then cleared).
+bool read_wait_timeouts(unsigned int* count, cudaStream_t stream);
+
 void launch_dequant(int fmt, const uint8_t* W, float* out, int N, int K, cudaStream_t stream);
 
 }  // namespace kq

@@ -83,5 +83,11 @@ class DecodeStep:
         self.graph = g
         return g
 
-    def replay(self):
-        self.graph.replay()
+    def replay(self, stream=None):
+        """Replay the captured step on `stream` (default: current stream)."""
+        if stream is None:
+            self.graph.replay()
+        else:
+            import torch
+            with torch.cuda.stream(stream):
+                self.graph.replay()

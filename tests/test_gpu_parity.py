@@ -42,7 +42,7 @@ def gpu_gemv(kq, fmt, Wb, x_u16, N, K):
     ybuf = torch.full((T * N + 2 * pad,), CANARY, dtype=torch.float32, device="cuda")
     y = ybuf[pad:pad + T * N]
     kq.kq_gemv(fmt, dev(Wb), dev_x(x_u16), y, N, K, T)
-    torch.cuda.synchronize()
+    kq.kq_device_status()
     out = ybuf.cpu().numpy()
     assert np.all(out[:pad] == np.float32(CANARY)) and np.all(out[pad + T * N:] == np.float32(CANARY))
     return out[pad:pad + T * N].reshape(T, N)
