@@ -206,12 +206,18 @@ __device__ __forceinline__ T pick(const T (&a)[kMaxGroup], int i) {
 struct Params {
   GemvGroup g;
   const uint16_t* x;         // bf16 [nt][K]
-  int K, nsb, slabs, tiles, nt, kpad;
+  int K, nsb, nt;
+  int slabs;                 // slabs of one K segment
+  int kpad;                  // staged x positions per token (one K segment)
+  int ksplit;                // K segments (CTA c works on segment c % ksplit)
+  int tiles;
+  int tile_rows;             // rows per tile (<= the CTA's 2 * kWC * RT)
   int tile_end[kMaxGroup];   // cumulative tile counts per matrix
   uint32_t x_bytes;          // shared bytes of the staged x (+ part sums), 16-aligned
+  float* part;               // split-K partial sums [ksplit][tiles][tile_rows][NT]
+  unsigned int* arrivals;    // split-K per-tile arrival counters (left at zero)
 };
 
-template <int ROWS>
 __device__ __forceinline__ Tile tile_of(const Params& p, int t) {
   int mi = 0, base = 0;
 #pragma unroll
@@ -222,8 +228,8 @@ __device__ __forceinline__ Tile tile_of(const Params& p, int t) {
     }
   Tile r;
   r.mi = mi;
-  r.row0 = (t - base) * ROWS;
-  r.rcnt = min(ROWS, pick(p.g.N, mi) - r.row0);
+  r.row0 = (t - base) * p.tile_rows;
+  r.rcnt = min(p.tile_rows, pick(p.g.N, mi) - r.row0);
   return r;
 }
 
@@ -265,7 +271,7 @@ struct XLayout {
 // X (layout above) followed by SX: [NT][kpad/kPart] fp32 part sums.
 // Entries beyond K or for tokens >= nt are zero.
 template <int F, int NT, int RT, bool XBF>
-__device__ void stage_x(const Params& p, uint8_t* smem) {
+__device__ void stage_x(const Params& p, uint8_t* smem, int kbase) {
   using G = Geo<F, NT, RT>;
   using L = XLayout<F, NT, XBF>;
   constexpr int P = G::kPart;                 // positions per part sum (>= 4)
@@ -276,8 +282,8 @@ __device__ void stage_x(const Params& p, uint8_t* smem) {
   float* sx = reinterpret_cast<float*>(smem + L::bytes(static_cast<size_t>(NT) * p.kpad));
   for (int q = threadIdx.x; q < NT * items_per_tok; q += blockDim.x) {
     const int tk = q / items_per_tok, k0 = (q % items_per_tok) * CH;
-    const uint16_t* xt = p.x + static_cast<int64_t>(tk) * p.K + k0;
-    const bool live = tk < p.nt && k0 < p.K;
+    const uint16_t* xt = p.x + static_cast<int64_t>(tk) * p.K + kbase + k0;
+    const bool live = tk < p.nt && kbase + k0 < p.K;
     float sums[NS];
 #pragma unroll
     for (int n = 0; n < NS; ++n) sums[n] = 0.0f;
@@ -509,15 +515,15 @@ __device__ __forceinline__ void unit_q4(const uint32_t (&w)[NW], const uint32_t 
 
 // One stage of a Q4_K / Q5_K / Q4_G128 tile for this thread's rows.
 template <int F, int NT, int RT, bool XBF>
-__device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl, uint32_t st,
-                                         uint32_t xs, int hw, int sbl, int c, int off,
-                                         float (&acc)[RT][NT]) {
+__device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl, int xsl,
+                                         uint32_t st, uint32_t xs, int hw, int sbl, int c,
+                                         int off, float (&acc)[RT][NT]) {
   using G = Geo<F, NT, RT>;
   using L = XLayout<F, NT, XBF>;
   constexpr int kCW = G::kCW, NW = kCW / 8;
   float2 xl[NT][NW / 2][4], xh[NT][NW / 2][4];
   float sxlo[NT], sxhi[NT];
-  const int k0 = sl * G::kSlabK + sbl * 256 + 64 * c + off;   // first lo position
+  const int k0 = xsl * G::kSlabK + sbl * 256 + 64 * c + off;   // first lo position (staged x)
   const uint32_t sxa = xs + static_cast<uint32_t>(L::bytes(static_cast<size_t>(NT) * p.kpad));
   const int parts = p.kpad / G::kPart;
 #pragma unroll
@@ -596,8 +602,8 @@ __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl
 // With at least two words per t-run the words are paired (64-bit), as in
 // unit_q4; with one word (n_tok 4) each word is used alone.
 template <int NT, int RT, bool XBF>
-__device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl, uint32_t st,
-                                         uint32_t xs, int hw, int sbl, int un,
+__device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl, int xsl,
+                                         uint32_t st, uint32_t xs, int hw, int sbl, int un,
                                          float (&acc)[RT][NT]) {
   using G = Geo<kQ6K, NT, RT>;
   using L = XLayout<kQ6K, NT, XBF>;
@@ -612,7 +618,7 @@ __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl
   // single -> (x0,x1), (x2,x3) in [0], [1]
   float2 xv[NT][4][NX][4];
   float sxt[NT][4];   // sum of x over each t-run (for the -32 of q - 32)
-  const int kb = sl * G::kSlabK + sbl * 256 + 128 * h + l0;
+  const int kb = xsl * G::kSlabK + sbl * 256 + 128 * h + l0;
   const uint32_t sxa = xs + static_cast<uint32_t>(L::bytes(static_cast<size_t>(NT) * p.kpad));
   const int parts = p.kpad / G::kPart;
 #pragma unroll
@@ -718,15 +724,20 @@ __global__ void __launch_bounds__(kThreads) gemv_stream(const Params p, int stag
   using G = Geo<F, NT, RT>;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
+  __shared__ int last_flag;
   const uint32_t bar_full = smem_addr(&bars[0]);
   const uint32_t bar_empty = smem_addr(&bars[kMaxStages]);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t xs = smem_addr(smem);
   uint8_t* ring = smem + p.x_bytes;
   const uint32_t ring_a = xs + p.x_bytes;
-  const int my_tiles = (p.tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                       static_cast<int>(gridDim.x);
+  // CTA c works on K segment c % ksplit and on tiles c / ksplit + i * cps
+  const int kseg = static_cast<int>(blockIdx.x) % p.ksplit;
+  const int cta = static_cast<int>(blockIdx.x) / p.ksplit;
+  const int cps = static_cast<int>(gridDim.x) / p.ksplit;   // CTAs per segment
+  const int my_tiles = (p.tiles - cta + cps - 1) / cps;
   const int total = my_tiles * p.slabs;   // stages of this CTA
+  const int sl0 = kseg * p.slabs;         // first slab (of the row) of the segment
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(bar_full + 8 * s, 32);      // every producer lane arrives
@@ -738,21 +749,22 @@ __global__ void __launch_bounds__(kThreads) gemv_stream(const Params p, int stag
   const bool producer = warp == kWC;
   const int first = total < stages ? total : stages;
   // Programmatic dependent launch: the next kernel on the stream may start
-  // its CTAs as SMs free up; it reads its activations only after its own
-  // griddepcontrol.wait, i.e. after this grid has completed.
+  // its CTAs as SMs free up; it reads its activations and touches the
+  // split-K scratch only after its own griddepcontrol.wait, i.e. after this
+  // grid has completed.
   asm volatile("griddepcontrol.launch_dependents;");
   if (producer) {
     // weights do not depend on the previous kernel: the first ring of stages
     // (no empty wait needed) streams while that kernel may still be running
     for (int it = 0; it < first; ++it) {
-      const Tile tl = tile_of<G::kRows>(p, blockIdx.x + (it / p.slabs) * gridDim.x);
+      const Tile tl = tile_of(p, cta + (it / p.slabs) * cps);
       issue_stage<F, NT, RT>(p, smem, ring_a + it * G::kStage, bar_full + 8 * it, tl,
-                             it % p.slabs);
+                             sl0 + it % p.slabs);
     }
   }
   // x may be produced by the previous kernel: wait for it to complete
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  stage_x<F, NT, RT, XBF>(p, smem);
+  stage_x<F, NT, RT, XBF>(p, smem, kseg * p.kpad);
   __syncthreads();
   if (producer) {
     for (int it = first; it < total; ++it) {
@@ -760,9 +772,9 @@ __global__ void __launch_bounds__(kThreads) gemv_stream(const Params p, int stag
       const uint32_t use = static_cast<uint32_t>(it / stages);
       if (!mbar_wait_warp(bar_empty + 8 * slot, (use - 1) & 1)) return;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      const Tile tl = tile_of<G::kRows>(p, blockIdx.x + (it / p.slabs) * gridDim.x);
+      const Tile tl = tile_of(p, cta + (it / p.slabs) * cps);
       issue_stage<F, NT, RT>(p, smem, ring_a + slot * G::kStage, bar_full + 8 * slot, tl,
-                             it % p.slabs);
+                             sl0 + it % p.slabs);
     }
     return;
   }
@@ -776,10 +788,13 @@ __global__ void __launch_bounds__(kThreads) gemv_stream(const Params p, int stag
   const int off = (un % (64 / kCW)) * (kCW / 2);
   float acc[RT][NT];
   Tile tl{};
+  int t = 0;
   for (int it = 0; it < total; ++it) {
-    const int sl = it % p.slabs;
-    if (sl == 0) {
-      tl = tile_of<G::kRows>(p, blockIdx.x + (it / p.slabs) * gridDim.x);
+    const int xsl = it % p.slabs;   // slab within the segment
+    const int sl = sl0 + xsl;       // slab within the row
+    if (xsl == 0) {
+      t = cta + (it / p.slabs) * cps;
+      tl = tile_of(p, t);
 #pragma unroll
       for (int r = 0; r < RT; ++r)
 #pragma unroll
@@ -791,13 +806,13 @@ __global__ void __launch_bounds__(kThreads) gemv_stream(const Params p, int stag
     const uint32_t st = ring_a + slot * G::kStage;
     if (sl * G::kSlabSB + sbl < p.nsb) {
       if constexpr (F == kQ6K)
-        stage_q6<NT, RT, XBF>(p, tl, sl, st, xs, hw, sbl, un, acc);
+        stage_q6<NT, RT, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, un, acc);
       else
-        stage_q4<F, NT, RT, XBF>(p, tl, sl, st, xs, hw, sbl, c, off, acc);
+        stage_q4<F, NT, RT, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, c, off, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
-    if (sl == p.slabs - 1) {
+    if (xsl == p.slabs - 1) {
 #pragma unroll
       for (int r = 0; r < RT; ++r)
 #pragma unroll
@@ -809,17 +824,57 @@ __global__ void __launch_bounds__(kThreads) gemv_stream(const Params p, int stag
           v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
           acc[r][k] = v;
         }
-      if (ul == 0) {
-        float* y = pick(p.g.y, tl.mi);
-        const int64_t N = pick(p.g.N, tl.mi);
+      float* y = pick(p.g.y, tl.mi);
+      const int64_t N = pick(p.g.N, tl.mi);
+      if (p.ksplit == 1) {
+        if (ul == 0) {
 #pragma unroll
-        for (int r = 0; r < RT; ++r) {
-          const int row = hw + 2 * kWC * r;
-          if (row < tl.rcnt) {
+          for (int r = 0; r < RT; ++r) {
+            const int row = hw + 2 * kWC * r;
+            if (row < tl.rcnt) {
 #pragma unroll
-            for (int k = 0; k < NT; ++k)
-              if (k < p.nt) y[static_cast<int64_t>(k) * N + tl.row0 + row] = acc[r][k];
+              for (int k = 0; k < NT; ++k)
+                if (k < p.nt) y[static_cast<int64_t>(k) * N + tl.row0 + row] = acc[r][k];
+            }
           }
+        }
+      } else {
+        // split-K: publish this segment's partial sums; the last CTA of the
+        // tile to arrive adds the segments in order 0..ksplit-1 (the result
+        // does not depend on arrival order) and re-arms the counter
+        float* part = p.part + static_cast<int64_t>(t) * p.tile_rows * NT;
+        const int64_t seg_stride = static_cast<int64_t>(p.tiles) * p.tile_rows * NT;
+        if (ul == 0) {
+#pragma unroll
+          for (int r = 0; r < RT; ++r) {
+            const int row = hw + 2 * kWC * r;
+            if (row < tl.rcnt) {
+#pragma unroll
+              for (int k = 0; k < NT; ++k) __stcg(part + kseg * seg_stride + row * NT + k, acc[r][k]);
+            }
+          }
+          __threadfence();
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kWC * 32) : "memory");
+        if (threadIdx.x == 0) last_flag = atomicAdd(p.arrivals + t, 1u) == static_cast<unsigned>(p.ksplit - 1);
+        asm volatile("bar.sync 1, %0;" ::"r"(kWC * 32) : "memory");
+        if (last_flag) {
+          __threadfence();
+          if (ul == 0) {
+#pragma unroll
+            for (int r = 0; r < RT; ++r) {
+              const int row = hw + 2 * kWC * r;
+              if (row < tl.rcnt) {
+#pragma unroll
+                for (int k = 0; k < NT; ++k) {
+                  float v = 0.0f;
+                  for (int j = 0; j < p.ksplit; ++j) v += __ldcg(part + j * seg_stride + row * NT + k);
+                  if (k < p.nt) y[static_cast<int64_t>(k) * N + tl.row0 + row] = v;
+                }
+              }
+            }
+          }
+          if (threadIdx.x == 0) p.arrivals[t] = 0u;
         }
       }
     }
@@ -847,9 +902,84 @@ DevInfo& dev_info() {
 
 constexpr size_t kSmemPerSM = 228 * 1024;   // usable shared memory per SM (B300)
 
+// Split-K scratch of the current device: a fixed region of kMaxTiles arrival
+// counters, then the partial sums.  The counter region never moves or
+// shrinks, so counters stay zero across launches of any shape (partial sums
+// of one launch never land on another launch's counters).  Grown on demand
+// (never while the stream is being captured), zero-filled when allocated;
+// kernels leave every counter they use at zero when they finish.
+constexpr int kMaxTiles = 1 << 16;
+constexpr size_t kCounterBytes = size_t{kMaxTiles} * sizeof(unsigned int);
+struct Scratch {
+  void* base = nullptr;
+  size_t bytes = 0;
+};
+Scratch& scratch_of_device() {
+  static Scratch sc[64];
+  int d = 0;
+  cudaGetDevice(&d);
+  return sc[d & 63];
+}
+void* scratch_get(size_t bytes, cudaStream_t s) {
+  Scratch& sc = scratch_of_device();
+  if (sc.bytes >= bytes) return sc.base;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  size_t want = bytes < (size_t{1} << 20) ? (size_t{1} << 20) : bytes;
+  void* p = nullptr;
+  if (sc.base != nullptr) cudaFree(sc.base);   // synchronises with work using it
+  sc.base = nullptr;
+  sc.bytes = 0;
+  if (cudaMalloc(&p, want) != cudaSuccess || cudaMemset(p, 0, want) != cudaSuccess) {
+    (void)cudaGetLastError();
+    if (p != nullptr) cudaFree(p);
+    return nullptr;
+  }
+  sc.base = p;
+  sc.bytes = want;
+  return p;
+}
+
+// Shared-memory plan of one configuration: staged x bytes, CTAs per SM (as
+// many as fit with at least two ring stages, up to three) and ring stages.
+struct Plan {
+  uint32_t x_bytes = 0;
+  int per_sm = 0;
+  int stages = 0;
+  size_t smem = 0;
+};
+
+template <int F, int NT, int RT, bool XBF>
+Plan make_plan(int K, int ksplit) {
+  using G = Geo<F, NT, RT>;
+  Plan pl;
+  const int slabs_row = (K / 256 + G::kSlabSB - 1) / G::kSlabSB;
+  if (slabs_row % ksplit != 0) return pl;
+  const int kpad = slabs_row / ksplit * G::kSlabK;
+  const size_t xb = XLayout<F, NT, XBF>::bytes(static_cast<size_t>(NT) * kpad) +
+                    static_cast<size_t>(NT) * (kpad / G::kPart) * 4;
+  pl.x_bytes = static_cast<uint32_t>((xb + 127) & ~size_t{127});
+  const size_t optin = dev_info().smem_optin;
+  for (int per_sm = 3; per_sm >= 1; --per_sm) {
+    size_t budget = (per_sm == 1 ? optin : kSmemPerSM / per_sm) - 2048;
+    if (budget > optin - 1024) budget = optin - 1024;
+    if (pl.x_bytes + 2 * static_cast<size_t>(G::kStage) > budget) continue;
+    int stages = static_cast<int>((budget - pl.x_bytes) / G::kStage);
+    if (stages > kMaxStages) stages = kMaxStages;
+    pl.per_sm = per_sm;
+    pl.stages = stages;
+    pl.smem = pl.x_bytes + static_cast<size_t>(stages) * G::kStage;
+    return pl;
+  }
+  return pl;
+}
+
 template <int F, int NT, int RT, bool XBF>
 bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
-                int grid_cap) {
+                int ksplit) {
   using G = Geo<F, NT, RT>;
   const DevInfo& di = dev_info();
   Params p;
@@ -857,33 +987,20 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   p.x = x;
   p.K = K;
   p.nsb = K / 256;
-  p.slabs = (p.nsb + G::kSlabSB - 1) / G::kSlabSB;
+  const int slabs_row = (p.nsb + G::kSlabSB - 1) / G::kSlabSB;
+  if (slabs_row % ksplit != 0) return false;
+  p.ksplit = ksplit;
+  p.slabs = slabs_row / ksplit;
   p.kpad = p.slabs * G::kSlabK;
   p.nt = n_tok;
-  p.tiles = 0;
-  for (int i = 0; i < kMaxGroup; ++i) {
-    if (i < g.count) p.tiles += (g.N[i] + G::kRows - 1) / G::kRows;
-    p.tile_end[i] = p.tiles;
-  }
-  const size_t xb = XLayout<F, NT, XBF>::bytes(static_cast<size_t>(NT) * p.kpad) +
-                    static_cast<size_t>(NT) * (p.kpad / G::kPart) * 4;
-  p.x_bytes = static_cast<uint32_t>((xb + 127) & ~size_t{127});
-  // CTAs per SM: three when x plus two stages fit three times (more warps to
-  // hide latency), else two with at least three stages, else one.
-  int per_sm = 3;
-  size_t budget = kSmemPerSM / 3 - 2048;
-  if (p.x_bytes + 2 * G::kStage > budget) {
-    per_sm = 2;
-    budget = kSmemPerSM / 2 - 2048;
-    if (p.x_bytes + 3 * G::kStage > budget) {
-      per_sm = 1;
-      budget = di.smem_optin - 1024;
-    }
-  }
-  if (p.x_bytes + 2 * G::kStage > budget) return false;
-  int stages = static_cast<int>((budget - p.x_bytes) / G::kStage);
-  if (stages > kMaxStages) stages = kMaxStages;
-  const size_t smem = p.x_bytes + static_cast<size_t>(stages) * G::kStage;
+  p.part = nullptr;
+  p.arrivals = nullptr;
+  const Plan pl = make_plan<F, NT, RT, XBF>(K, ksplit);
+  if (pl.per_sm == 0) return false;
+  p.x_bytes = pl.x_bytes;
+  int per_sm = pl.per_sm;
+  const int stages = pl.stages;
+  const size_t smem = pl.smem;
   static size_t configured = 0;   // dynamic shared memory above 48 KB is opt-in
   if (smem > configured) {
     if (cudaFuncSetAttribute(gemv_stream<F, NT, RT, XBF>,
@@ -899,11 +1016,36 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
                                                     smem) == cudaSuccess &&
       occ >= 1 && occ < per_sm)
     per_sm = occ;
-  int grid = per_sm * di.sms;
-  if (grid_cap > 0 && grid > grid_cap) grid = grid_cap;
-  if (grid > p.tiles) grid = p.tiles;
+  // CTAs per K segment, all resident at once
+  int cps = per_sm * di.sms / ksplit;
+  if (cps < 1) cps = 1;
+  // Balanced tiling: every CTA of a segment streams (about) the same number
+  // of equal tiles.  k = tiles per CTA, rows per tile = ceil(rows / (cps k)).
+  int64_t rows = 0;
+  for (int i = 0; i < g.count; ++i) rows += g.N[i];
+  const int64_t k = (rows + static_cast<int64_t>(cps) * G::kRows - 1) /
+                    (static_cast<int64_t>(cps) * G::kRows);
+  int tr = static_cast<int>((rows + cps * k - 1) / (cps * k));
+  if (tr > G::kRows) tr = G::kRows;
+  if (tr < 1) tr = 1;
+  p.tile_rows = tr;
+  p.tiles = 0;
+  for (int i = 0; i < kMaxGroup; ++i) {
+    if (i < g.count) p.tiles += (g.N[i] + tr - 1) / tr;
+    p.tile_end[i] = p.tiles;
+  }
+  if (cps > p.tiles) cps = p.tiles;
+  if (ksplit > 1) {
+    if (p.tiles > kMaxTiles) return false;
+    const size_t part_bytes =
+        static_cast<size_t>(ksplit) * p.tiles * p.tile_rows * NT * sizeof(float);
+    uint8_t* base = static_cast<uint8_t*>(scratch_get(kCounterBytes + part_bytes, s));
+    if (base == nullptr) return false;
+    p.arrivals = reinterpret_cast<unsigned int*>(base);
+    p.part = reinterpret_cast<float*>(base + kCounterBytes);
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.gridDim = dim3(static_cast<unsigned>(cps * ksplit));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -915,21 +1057,47 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   return cudaLaunchKernelEx(&cfg, gemv_stream<F, NT, RT, XBF>, p, stages) == cudaSuccess;
 }
 
+template <int F, int NT, int RT>
+bool launch_rt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s) {
+  using G = Geo<F, NT, RT>;
+  // K segments: the fewest (a power of two dividing the slabs of a row, at
+  // most 16) that reach three CTAs per SM, else the fewest that reach the
+  // most CTAs per SM.  x is staged as bf16 only when its fp32 copy would not
+  // fit at all.
+  const int slabs_row = (K / 256 + G::kSlabSB - 1) / G::kSlabSB;
+  int best_ks = 0, best_sm = 0;
+  bool best_bf = false;
+  for (int ks = 1; ks <= 16 && slabs_row % ks == 0; ks *= 2) {
+    Plan pl = make_plan<F, NT, RT, false>(K, ks);
+    bool bf = false;
+    if (pl.per_sm == 0) {
+      pl = make_plan<F, NT, RT, true>(K, ks);
+      bf = true;
+    }
+    if (pl.per_sm > best_sm) {
+      best_sm = pl.per_sm;
+      best_ks = ks;
+      best_bf = bf;
+    }
+    if (best_sm == 3) break;
+  }
+  if (best_ks == 0) return false;
+  for (int ks = best_ks;; ks = 1) {
+    const bool ok = best_bf ? launch_cfg<F, NT, RT, true>(g, x, K, n_tok, s, ks)
+                            : launch_cfg<F, NT, RT, false>(g, x, K, n_tok, s, ks);
+    if (ok || ks == 1) return ok;   // no scratch (e.g. during capture): unsplit
+    best_bf = static_cast<size_t>(NT) * K * 4 > 96 * 1024;
+  }
+}
+
 template <int F, int NT>
 bool launch_nt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s) {
   const DevInfo& di = dev_info();
-  // rows per thread: 4 unless that leaves fewer than two tiles per SM
-  int tiles4 = 0;
-  for (int i = 0; i < g.count; ++i) tiles4 += (g.N[i] + 2 * kWC * 4 - 1) / (2 * kWC * 4);
-  const bool small = tiles4 < 2 * di.sms;
-  // fp32 x while it leaves room for the ring, bf16 beyond
-  const bool xbf = static_cast<size_t>(NT) * K * 4 > 96 * 1024;
-  if (small) {
-    return xbf ? launch_cfg<F, NT, 2, true>(g, x, K, n_tok, s, 0)
-               : launch_cfg<F, NT, 2, false>(g, x, K, n_tok, s, 0);
-  }
-  return xbf ? launch_cfg<F, NT, 4, true>(g, x, K, n_tok, s, 0)
-             : launch_cfg<F, NT, 4, false>(g, x, K, n_tok, s, 0);
+  // rows per thread: 4, or 2 for small matrices (fewer than 16 rows per SM)
+  int64_t rows = 0;
+  for (int i = 0; i < g.count; ++i) rows += g.N[i];
+  if (rows < 16LL * di.sms) return launch_rt<F, NT, 2>(g, x, K, n_tok, s);
+  return launch_rt<F, NT, 4>(g, x, K, n_tok, s);
 }
 
 }  // namespace
@@ -959,10 +1127,15 @@ bool read_wait_timeouts(unsigned int* count, cudaStream_t s) {
                                 cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return false;
   if (cudaStreamSynchronize(s) != cudaSuccess) return false;
-  if (*count != 0 &&
-      cudaMemcpyToSymbolAsync(g_wait_timeouts, &zero, sizeof(unsigned int), 0,
-                              cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return false;
+  if (*count != 0) {
+    // a kernel stopped early: clear the count and re-arm the split-K
+    // arrival counters it may have left behind
+    if (cudaMemcpyToSymbolAsync(g_wait_timeouts, &zero, sizeof(unsigned int), 0,
+                                cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return false;
+    Scratch& sc = scratch_of_device();
+    if (sc.base != nullptr && cudaMemsetAsync(sc.base, 0, sc.bytes, s) != cudaSuccess) return false;
+  }
   return cudaStreamSynchronize(s) == cudaSuccess;
 }
 
