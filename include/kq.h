@@ -92,7 +92,8 @@ typedef enum {
   KQ_ERR_RANGE = 5,         /* kq_quantize: a scale exceeds fp16 range     */
   KQ_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed        */
   KQ_ERR_UNSUPPORTED = 7,   /* valid request this build cannot serve       */
-  KQ_ERR_TIMEOUT = 8        /* a kernel's bounded wait ran out (see below) */
+  KQ_ERR_TIMEOUT = 8,       /* a kernel's bounded wait ran out (see below) */
+  KQ_ERR_TOO_LARGE = 9      /* kq_gemv_noalloc: beyond its fixed scratch    */
 } kq_status;
 
 /* Bytes of one 256-weight super-block: 144 / 176 / 210 / 136.  0 for a bad
@@ -112,6 +113,33 @@ size_t kq_matrix_bytes(kq_format f, int64_t N_out, int64_t K);
 kq_status kq_gemv(kq_format f, const void* W_blocks, const void* x_bf16,
                   float* y, int64_t N_out, int64_t K, int n_tok,
                   kq_stream_t stream);
+
+/* kq_gemv for callers that must not allocate device memory.  The reference
+ * pages have no counterpart: this entry point exists for users of this
+ * library.  Some callers cannot call cudaMalloc at the moment they compute:
+ * code running while a stream is being captured into a CUDA graph, engines
+ * that hand out all device memory from their own pool and forbid driver
+ * allocations after start-up, and latency-critical loops that cannot afford
+ * an allocation's implicit device synchronisation.  kq_gemv may allocate a
+ * split-K scratch buffer on its first long-row call; this variant never
+ * allocates and keeps that scratch in a fixed 2 MiB array compiled into the
+ * library, which every GPU that loads the library holds until the process
+ * exits.
+ *   Same arguments, requirements and result as kq_gemv (within the same
+ *   tolerance; the same kernels run).
+ *   Limits: a request whose split-K scratch would exceed the array (more
+ *   than 16384 row tiles, or more partial sums than fit in 2 MiB - 64 KiB;
+ *   roughly N_out * n_tok * segments > 500000) returns KQ_ERR_TOO_LARGE and
+ *   launches nothing.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current and caches it; make
+ *   that first call before any stream capture.
+ *   Sharing: every call uses the same array, which keeps the previous
+ *   call's contents; each call clears the counters it needs (a
+ *   stream-ordered memset).  Calls that overlap on the GPU (different
+ *   streams, no ordering between them) race on the array. */
+kq_status kq_gemv_noalloc(kq_format f, const void* W_blocks, const void* x_bf16, float* y,
+                          int64_t N_out, int64_t K, int n_tok, kq_stream_t stream);
 
 /* Several matrices of one format and one K that read the same activations,
  * computed in ONE launch: y_i = w^_i x for i < count (1 <= count <= 4).  The

@@ -21,7 +21,7 @@ FORMATS = {"Q4_K": Q4_K, "Q5_K": Q5_K, "Q6_K": Q6_K, "Q4_G128": Q4_G128}
 KQ_OK = 0
 STATUS_NAMES = {0: "KQ_OK", 1: "KQ_ERR_ARG", 2: "KQ_ERR_SHAPE", 3: "KQ_ERR_ALIGN",
                 4: "KQ_ERR_NOT_MERGEABLE", 5: "KQ_ERR_RANGE", 6: "KQ_ERR_CUDA",
-                7: "KQ_ERR_UNSUPPORTED", 8: "KQ_ERR_TIMEOUT"}
+                7: "KQ_ERR_UNSUPPORTED", 8: "KQ_ERR_TIMEOUT", 9: "KQ_ERR_TOO_LARGE"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkq.so")
@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
         L.kq_matrix_bytes.restype = ctypes.c_size_t
         L.kq_gemv.argtypes = [I, P, P, P, I64, I64, I, P]
         L.kq_gemv_multi.argtypes = [I, I, P, P, P, P, I64, I, P]
+        L.kq_gemv_noalloc.argtypes = [I, P, P, P, I64, I64, I, P]
         L.kq_layer_step.argtypes = [ctypes.POINTER(kq_layer), ctypes.POINTER(kq_layer_io), I, P]
         L.kq_dequantize.argtypes = [I, P, P, I64, I64, P]
         L.kq_quantize.argtypes = [I, P, I64, I64, P]
@@ -72,7 +73,7 @@ def lib() -> ctypes.CDLL:
         L.kq_device_status.restype = I
         L.kq_status_str.argtypes = [I]
         L.kq_status_str.restype = ctypes.c_char_p
-        for name in ("kq_gemv", "kq_gemv_multi", "kq_layer_step", "kq_dequantize", "kq_quantize", "kq_merge_g128"):
+        for name in ("kq_gemv", "kq_gemv_multi", "kq_gemv_noalloc", "kq_layer_step", "kq_dequantize", "kq_quantize", "kq_merge_g128"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -126,6 +127,13 @@ def kq_gemv(fmt, W, x, y, N_out, K, n_tok, stream=None, check=True) -> int:
     """y[t][n] = sum_k w^[n][k] x[t][k] (device tensors; y overwritten)."""
     st = lib().kq_gemv(fmt, _addr(W), _addr(x), _addr(y), N_out, K, n_tok, _stream(stream))
     return _check(st, "kq_gemv") if check else st
+
+
+def kq_gemv_noalloc(fmt, W, x, y, N_out, K, n_tok, stream=None, check=True) -> int:
+    """kq_gemv that never allocates device memory (fixed 2 MiB scratch)."""
+    st = lib().kq_gemv_noalloc(fmt, _addr(W), _addr(x), _addr(y), N_out, K, n_tok,
+                               _stream(stream))
+    return _check(st, "kq_gemv_noalloc") if check else st
 
 
 def kq_gemv_multi(fmt, Ws, ys, N_outs, x, K, n_tok, stream=None, check=True) -> int:

@@ -57,6 +57,36 @@ kq_status kq_gemv(kq_format f, const void* W_blocks, const void* x_bf16, float* 
   return launch_status();
 }
 
+kq_status kq_gemv_noalloc(kq_format f, const void* W_blocks, const void* x_bf16, float* y,
+                          int64_t N_out, int64_t K, int n_tok, kq_stream_t stream) {
+  kq_status st = check_matrix(f, W_blocks, N_out, K);
+  if (st != KQ_OK) return st;
+  st = check_io(x_bf16, y, n_tok);
+  if (st != KQ_OK) return st;
+  kq::GemvGroup g{};
+  g.count = 1;
+  g.W[0] = static_cast<const uint8_t*>(W_blocks);
+  g.y[0] = y;
+  g.N[0] = static_cast<int>(N_out);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (kq::launch_stream_noalloc(f, g, static_cast<const uint16_t*>(x_bf16),
+                                    static_cast<int>(K), n_tok, s)) {
+    case kq::NoAllocResult::kLaunched:
+      return launch_status();
+    case kq::NoAllocResult::kTooLarge:
+      return KQ_ERR_TOO_LARGE;
+    case kq::NoAllocResult::kFailed:
+      return KQ_ERR_CUDA;
+    case kq::NoAllocResult::kNotServed:
+      break;
+  }
+  // requests the streaming kernel does not serve need no scratch
+  if (!kq::launch_gemv(f, g, static_cast<const uint16_t*>(x_bf16), static_cast<int>(K), n_tok,
+                       s))
+    return KQ_ERR_UNSUPPORTED;
+  return launch_status();
+}
+
 kq_status kq_gemv_multi(kq_format f, int count, const void* const* W, float* const* y,
                         const int64_t* N_out, const void* x_bf16, int64_t K, int n_tok,
                         kq_stream_t stream) {

@@ -247,6 +247,7 @@ const char* kq_status_str(kq_status s) {
     case KQ_ERR_CUDA: return "CUDA runtime or launch error";
     case KQ_ERR_UNSUPPORTED: return "unsupported request";
     case KQ_ERR_TIMEOUT: return "a kernel's bounded shared-memory wait timed out";
+    case KQ_ERR_TOO_LARGE: return "request exceeds the fixed scratch of kq_gemv_noalloc";
   }
   return "unknown status";
 }

@@ -26,6 +26,14 @@ bool launch_gemv(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_to
 bool launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
                    cudaStream_t stream);
 
+// kq_gemv_noalloc: the streaming kernel with its split-K scratch in a fixed
+// device array (no allocation).  kNotServed: this request needs no scratch
+// kernel of this family (n_tok > 4, or no configuration fits); the caller
+// may use a kernel that needs no scratch.
+enum class NoAllocResult { kLaunched, kNotServed, kTooLarge, kFailed };
+NoAllocResult launch_stream_noalloc(int fmt, const GemvGroup& g, const uint16_t* x, int K,
+                                    int n_tok, cudaStream_t stream);
+
 // Number of bounded waits that timed out since the last call (then cleared).
 bool read_wait_timeouts(unsigned int* count, cudaStream_t stream);
 

@@ -977,9 +977,22 @@ Plan make_plan(int K, int ksplit) {
   return pl;
 }
 
+// Where split-K partial sums live.  kDevice: the per-device buffer above
+// (grown with cudaMalloc).  kStatic: the fixed array of kq_gemv_noalloc below
+// (never allocates; too_large reports a request beyond its capacity).
+enum class ScratchSrc { kDevice, kStatic };
+struct StaticScratch {
+  uint8_t* base;
+  bool too_large;
+};
+constexpr int kNoAllocMaxTiles = 1 << 14;
+constexpr size_t kNoAllocCounterBytes = size_t{kNoAllocMaxTiles} * sizeof(unsigned int);
+constexpr size_t kNoAllocScratchBytes = size_t{2} << 20;   // 2 MiB per device
+
 template <int F, int NT, int RT, bool XBF>
 bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
-                int ksplit) {
+                int ksplit, ScratchSrc src = ScratchSrc::kDevice,
+                StaticScratch* st = nullptr) {
   using G = Geo<F, NT, RT>;
   const DevInfo& di = dev_info();
   Params p;
@@ -1036,13 +1049,28 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   }
   if (cps > p.tiles) cps = p.tiles;
   if (ksplit > 1) {
-    if (p.tiles > kMaxTiles) return false;
     const size_t part_bytes =
         static_cast<size_t>(ksplit) * p.tiles * p.tile_rows * NT * sizeof(float);
-    uint8_t* base = static_cast<uint8_t*>(scratch_get(kCounterBytes + part_bytes, s));
-    if (base == nullptr) return false;
-    p.arrivals = reinterpret_cast<unsigned int*>(base);
-    p.part = reinterpret_cast<float*>(base + kCounterBytes);
+    if (src == ScratchSrc::kDevice) {
+      if (p.tiles > kMaxTiles) return false;
+      uint8_t* base = static_cast<uint8_t*>(scratch_get(kCounterBytes + part_bytes, s));
+      if (base == nullptr) return false;
+      p.arrivals = reinterpret_cast<unsigned int*>(base);
+      p.part = reinterpret_cast<float*>(base + kCounterBytes);
+    } else {
+      if (p.tiles > kNoAllocMaxTiles ||
+          kNoAllocCounterBytes + part_bytes > kNoAllocScratchBytes) {
+        st->too_large = true;
+        return false;
+      }
+      // the array keeps the previous call's contents: clear the counters
+      // this launch uses (a stream-ordered memset, not an allocation)
+      if (cudaMemsetAsync(st->base, 0, static_cast<size_t>(p.tiles) * sizeof(unsigned int), s) !=
+          cudaSuccess)
+        return false;
+      p.arrivals = reinterpret_cast<unsigned int*>(st->base);
+      p.part = reinterpret_cast<float*>(st->base + kNoAllocCounterBytes);
+    }
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(cps * ksplit));
@@ -1058,7 +1086,8 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
 }
 
 template <int F, int NT, int RT>
-bool launch_rt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s) {
+bool launch_rt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
+               ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
   using G = Geo<F, NT, RT>;
   // K segments: the fewest (a power of two dividing the slabs of a row, at
   // most 16) that reach three CTAs per SM, else the fewest that reach the
@@ -1083,21 +1112,23 @@ bool launch_rt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStre
   }
   if (best_ks == 0) return false;
   for (int ks = best_ks;; ks = 1) {
-    const bool ok = best_bf ? launch_cfg<F, NT, RT, true>(g, x, K, n_tok, s, ks)
-                            : launch_cfg<F, NT, RT, false>(g, x, K, n_tok, s, ks);
+    const bool ok = best_bf ? launch_cfg<F, NT, RT, true>(g, x, K, n_tok, s, ks, src, st)
+                            : launch_cfg<F, NT, RT, false>(g, x, K, n_tok, s, ks, src, st);
     if (ok || ks == 1) return ok;   // no scratch (e.g. during capture): unsplit
+    if (st != nullptr && st->too_large) return false;
     best_bf = static_cast<size_t>(NT) * K * 4 > 96 * 1024;
   }
 }
 
 template <int F, int NT>
-bool launch_nt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s) {
+bool launch_nt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
+               ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
   const DevInfo& di = dev_info();
   // rows per thread: 4, or 2 for small matrices (fewer than 16 rows per SM)
   int64_t rows = 0;
   for (int i = 0; i < g.count; ++i) rows += g.N[i];
-  if (rows < 16LL * di.sms) return launch_rt<F, NT, 2>(g, x, K, n_tok, s);
-  return launch_rt<F, NT, 4>(g, x, K, n_tok, s);
+  if (rows < 16LL * di.sms) return launch_rt<F, NT, 2>(g, x, K, n_tok, s, src, st);
+  return launch_rt<F, NT, 4>(g, x, K, n_tok, s, src, st);
 }
 
 }  // namespace
@@ -1119,6 +1150,64 @@ bool launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_
   }
 #undef KQ_CASE
   return false;
+}
+
+// ------------------------------------------------------- no-allocation path
+//
+// Scratch of kq_gemv_noalloc: a fixed 2 MiB array in every device that loads
+// this library (held until the process exits).  The first 64 KiB hold the
+// split-K arrival counters of at most kNoAllocMaxTiles tiles, the rest the
+// partial sums.  All calls share it; calls that overlap on the GPU race on it.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, never a device address: the
+// address is looked up once per device (with that device current) and
+// cached.  nullptr if the lookup fails.
+void* noalloc_scratch_address() {
+  static void* addr[64] = {};
+  static bool looked_up[64] = {};
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return nullptr;
+  d &= 63;
+  if (!looked_up[d]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    addr[d] = ptr;
+    looked_up[d] = true;
+  }
+  return addr[d];
+}
+}  // namespace
+
+NoAllocResult launch_stream_noalloc(int fmt, const GemvGroup& g, const uint16_t* x, int K,
+                                    int n_tok, cudaStream_t s) {
+  if (n_tok > 4) return NoAllocResult::kNotServed;
+  StaticScratch st{static_cast<uint8_t*>(noalloc_scratch_address()), false};
+  if (st.base == nullptr) return NoAllocResult::kFailed;
+  const int nt = n_tok <= 1 ? 1 : (n_tok <= 2 ? 2 : 4);
+  bool ok = false;
+#define KQ_CASE(F)                                                                          \
+  case F:                                                                                   \
+    ok = nt == 1   ? launch_nt<F, 1>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st)           \
+         : nt == 2 ? launch_nt<F, 2>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st)           \
+                   : launch_nt<F, 4>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st);          \
+    break;
+  switch (fmt) {
+    KQ_CASE(kQ4K)
+    KQ_CASE(kQ5K)
+    KQ_CASE(kQ6K)
+    KQ_CASE(kG128)
+    default:
+      return NoAllocResult::kFailed;
+  }
+#undef KQ_CASE
+  if (st.too_large) return NoAllocResult::kTooLarge;
+  return ok ? NoAllocResult::kLaunched : NoAllocResult::kNotServed;
 }
 
 bool read_wait_timeouts(unsigned int* count, cudaStream_t s) {

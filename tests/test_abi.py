@@ -54,7 +54,7 @@ def test_sizes_and_status_strings(kq):
     assert kq.kq_matrix_bytes(kq.Q6_K, 200000, 5120) == 200000 * 20 * 210
     assert kq.kq_matrix_bytes(kq.Q4_G128, 4096, 5120) == 11141120
     assert kq.kq_matrix_bytes(kq.Q4_K, 4, 300) == 0
-    for s in range(9):
+    for s in range(10):
         assert kq.kq_status_str(s)
 
 
