@@ -241,8 +241,23 @@ void launch_f(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStrea
 bool launch_gemv(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
                  cudaStream_t s) {
   // the streaming kernel serves n_tok <= 4 while x fits in shared memory;
-  // everything else takes the warp-per-row kernel below
-  if (n_tok <= 4 && launch_stream(fmt, g, x, K, n_tok, s)) return true;
+  // more tokens run as consecutive launches of up to 4 tokens each (x and y
+  // rows of a token are contiguous, so a chunk is an offset view); anything
+  // it cannot serve takes the warp-per-row kernel below
+  if (n_tok <= 4) {
+    if (launch_stream(fmt, g, x, K, n_tok, s)) return true;
+  } else {
+    bool ok = true;
+    for (int t0 = 0; t0 < n_tok && ok; t0 += 4) {
+      const int nt = n_tok - t0 < 4 ? n_tok - t0 : 4;
+      GemvGroup gc = g;
+      for (int i = 0; i < g.count; ++i) gc.y[i] = g.y[i] + static_cast<int64_t>(t0) * g.N[i];
+      ok = launch_stream(fmt, gc, x + static_cast<int64_t>(t0) * K, K, nt, s);
+    }
+    if (ok) return true;
+    // a chunk could not be served (nothing launched for it): recompute all
+    // tokens with the kernel below, which overwrites every output
+  }
   switch (fmt) {
     case kQ4K: launch_f<kQ4K>(g, x, K, n_tok, s); return true;
     case kQ5K: launch_f<kQ5K>(g, x, K, n_tok, s); return true;
