@@ -27,6 +27,7 @@
 // Stages are handed over with mbarriers (full: producer -> consumers with the
 // bulk-copy byte count; empty: consumers -> producer).  Every wait is bounded
 // and records a timeout in a device word that kq_device_status reads.
+#include <cuda.h>   // CUtensorMap and its enums (the encoder is fetched at run time)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -42,8 +43,6 @@ __device__ unsigned int g_wait_timeouts = 0;
 
 namespace {
 
-constexpr int kWC = 4;                  // consumer warps per CTA
-constexpr int kThreads = (kWC + 1) * 32;
 constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
 
 // ------------------------------------------------------------ PTX helpers
@@ -171,9 +170,12 @@ __host__ __device__ constexpr float pow2(int e) {
 
 // -------------------------------------------------------------- geometry
 
-template <int F, int NT, int RT>
+template <int F, int NT, int RT, int WC>
 struct Geo {
-  static constexpr int kRows = 2 * kWC * RT;             // rows per tile
+  static constexpr int kF = F;
+  static constexpr int kWC = WC;                         // consumer warps per CTA
+  static constexpr int kThreads = (WC + 1) * 32;         // + one producer warp
+  static constexpr int kRows = 2 * WC * RT;              // rows per tile
   static constexpr int kCW = 64 / NT;                    // weights per unit
   // x positions per part sum: one sub-block part of a unit (Q4 family:
   // kCW/2 low or high nibbles; Q6_K: the kCW/4 weights of one t-run)
@@ -182,13 +184,35 @@ struct Geo {
   static constexpr int kSlabSB = 16 / kUnitsPerSB;       // super-blocks per slab: 4, 2, 1
   static constexpr int kSlabK = 256 * kSlabSB;           // 1024, 512, 256
   static constexpr int kBB = block_bytes(F);
-  // per-row shared slot (16-byte aligned): records (+ halo for unaligned
-  // starts); G128 keeps the q plane and the param plane in separate parts.
+  // Bytes of one row's slab: records (G128: the q plane; its param plane
+  // holds kPBytes more).
   static constexpr int kQBytes = (F == kG128) ? 128 * kSlabSB : kBB * kSlabSB;
-  static constexpr int kSlot = ((kQBytes + 16 + 15) / 16) * 16;
-  static constexpr int kPSlot = (F == kG128) ? ((8 * kSlabSB + 16 + 15) / 16) * 16 : 0;
-  static constexpr int kStage = kRows * (kSlot + kPSlot);
+  static constexpr int kPBytes = (F == kG128) ? 8 * kSlabSB : 0;
+  // Per-row shared slot.  Tensor copies: the slab rounded out to the 16-byte
+  // grid (a slab that does not start on 16 bytes starts up to 15 bytes into
+  // its slot).  Per-row bulk copies: one more 16 bytes of halo.
+  static constexpr int round16(int b) { return (b + 15) / 16 * 16; }
+  static constexpr int kSlotTma = round16(kQBytes + (kQBytes % 16 ? 15 : 0));
+  static constexpr int kPSlotTma = (F == kG128) ? round16(kPBytes + (kPBytes % 16 ? 15 : 0)) : 0;
+  static constexpr int kSlotBulk = round16(kQBytes + 16);
+  static constexpr int kPSlotBulk = (F == kG128) ? round16(kPBytes + 16) : 0;
 };
+
+// Shared-memory shape of one ring stage: rows x slot bytes of records (q
+// plane), then (G128) rows x pslot bytes of params at offset pbase.
+struct StageShape {
+  uint32_t slot, pslot, pbase, bytes;
+};
+template <class G>
+StageShape stage_shape(bool tma) {
+  auto r128 = [](uint32_t b) { return (b + 127u) / 128u * 128u; };
+  StageShape s;
+  s.slot = tma ? G::kSlotTma : G::kSlotBulk;
+  s.pslot = tma ? G::kPSlotTma : G::kPSlotBulk;
+  s.pbase = r128(G::kRows * s.slot);
+  s.bytes = s.pbase + r128(G::kRows * s.pslot);
+  return s;
+}
 
 struct Tile {
   int mi;      // matrix of the group
@@ -211,11 +235,17 @@ struct Params {
   int kpad;                  // staged x positions per token (one K segment)
   int ksplit;                // K segments (CTA c works on segment c % ksplit)
   int tiles;
-  int tile_rows;             // rows per tile (<= the CTA's 2 * kWC * RT)
+  int tile_rows;             // rows per tile (<= the CTA's 2 * WC * RT)
   int tile_end[kMaxGroup];   // cumulative tile counts per matrix
   uint32_t x_bytes;          // shared bytes of the staged x (+ part sums), 16-aligned
   float* part;               // split-K partial sums [ksplit][tiles][tile_rows][NT]
   unsigned int* arrivals;    // split-K per-tile arrival counters (left at zero)
+  int tma;                   // 1: a stage arrives as one tensor copy per plane
+  uint32_t slot, pslot, pbase, stage;   // StageShape of the ring
+  uint32_t tx;               // bytes the tensor copies of one stage deliver
+  // per matrix: 2-D tensor maps (8-byte elements x rows) of the records / the
+  // G128 q plane [0] and the G128 param plane [1]; box = slot bytes x tile_rows
+  CUtensorMap tm[kMaxGroup][2];
 };
 
 __device__ __forceinline__ Tile tile_of(const Params& p, int t) {
@@ -239,23 +269,32 @@ __device__ __forceinline__ Tile tile_of(const Params& p, int t) {
 // byte b (= position % 4) of a word, in the low (lo) or high half of a Q4
 // family chunk.  Q4_K / G128 low nibbles come from w (b0 s=0, b1 s=8, b2
 // s=16) and w >> 12 (b3 s=12); high nibbles from w (b0 s=4, b1 s=12) and
-// w >> 12 (b2 s=8, b3 s=16).  Q5_K and Q6_K extract whole bytes (b3 from
-// w >> 8).  x is staged pre-scaled by 2^-s, so (2^23 + q 2^s) - 2^23 = q 2^s
-// times the staged x is exactly q x.
+// w >> 12 (b2 s=8, b3 s=16).  Q5_K extracts 5-bit fields from two words
+// whose byte b holds the low (lo5) or high (hi5) nibble with its fifth bit:
+// b0..b2 at s = 0, 8, 16 of each, and b3 from one byte-permuted word that
+// holds lo5's b3 at s=0 and hi5's b3 at s=16.  Q6_K extracts whole bytes (b3
+// from w >> 8).  x is staged pre-scaled by 2^-s, so (2^23 + q 2^s) - 2^23 =
+// q 2^s times the staged x is exactly q x.
 template <int F>
 __host__ __device__ constexpr int field_shift(bool lo, int b) {
-  if (F == kQ5K || F == kQ6K) return b == 0 ? 0 : b == 1 ? 8 : 16;
+  if (F == kQ6K) return b == 0 ? 0 : b == 1 ? 8 : 16;
+  if (F == kQ5K) return b == 0 ? 0 : b == 1 ? 8 : b == 2 ? 16 : (lo ? 0 : 16);
   if (lo) return b == 0 ? 0 : b == 1 ? 8 : b == 2 ? 16 : 12;
   return b == 0 ? 4 : b == 1 ? 12 : b == 2 ? 8 : 16;
 }
 
-// Shared-memory layout of the staged activations.  Value i (= token * kpad
-// + position) sits at byte i * kE + kPad * (i / kPer): the padding staggers
-// the 16 units of a half-warp over all bank groups, so every x load of the
-// consumers is conflict-free (Q4 family: 16 B per 64 values, Q6_K: 16 B per
-// 128 values; half of that for bf16).  When kInterleave, each aligned group
-// of 8 positions is stored as x0 x4 x1 x5 x2 x6 x3 x7, so one 16-byte load
-// yields the two (word j, word j+1) pairs that the packed fmas consume.
+// Shared-memory layout of the staged activations.  Slot i (= token * kpad +
+// staged index) sits at byte i * kE + kPad * (i / kPer): the padding
+// staggers the 16 units of a half-warp over all bank groups, so every x load
+// of the consumers is conflict-free (Q4 family: 16 B per 64 slots, Q6_K: 16 B
+// per 128 slots; half of that for bf16).
+//   Q4 family: within each aligned block of 64 positions, position
+//     32h + 4i + b (h < 2, i < 8, b < 4) has staged index 8i + 2b + h, so the
+//     two positions one byte of a chunk multiplies (its low nibble: h = 0,
+//     its high nibble: h = 1) form one fp32 pair for the packed fmas.
+//   Q6_K with kInterleave: each aligned group of 8 positions is stored as
+//     x0 x4 x1 x5 x2 x6 x3 x7 (pairs for two words taken together);
+//     otherwise in order.
 template <int F, int NT, bool XBF>
 struct XLayout {
   static constexpr int kE = XBF ? 2 : 4;
@@ -269,10 +308,84 @@ struct XLayout {
 };
 
 // X (layout above) followed by SX: [NT][kpad/kPart] fp32 part sums.
-// Entries beyond K or for tokens >= nt are zero.
-template <int F, int NT, int RT, bool XBF>
-__device__ void stage_x(const Params& p, uint8_t* smem, int kbase) {
-  using G = Geo<F, NT, RT>;
+// Entries beyond K or for tokens >= nt are zero.  Q6_K: part sums in
+// position order.  Q4 family: within a 64-block, the sum over positions
+// [32h + j kPart, 32h + (j+1) kPart) sits at index 2j + h, so the (low, high)
+// sums of one unit form a pair.
+template <int F, int NT, bool XBF>
+__device__ void stage_x_q4(const Params& p, uint8_t* smem, int kbase) {
+  using G = Geo<F, NT, 1, 1>;
+  using L = XLayout<F, NT, XBF>;
+  constexpr int P = G::kPart;        // 32, 16, 8 positions per part sum
+  constexpr int GP = P / 4;          // 4-position groups per part: 8, 4, 2
+  const int groups_per_tok = p.kpad / 4 / 2;   // one group = 4 low + 4 high positions
+  const int total = NT * groups_per_tok;
+  const int parts_per_tok = p.kpad / P;
+  float* sx = reinterpret_cast<float*>(smem + L::bytes(static_cast<size_t>(NT) * p.kpad));
+  const int lane = threadIdx.x & 31;
+  // trip count uniform per warp (the part sums are reduced with shuffles over
+  // GP consecutive lanes; total and groups_per_tok are multiples of 8)
+  for (int base = static_cast<int>(threadIdx.x) & ~31; base < total; base += blockDim.x) {
+    const int q = base + lane;
+    const bool in = q < total;
+    const int tk = q / groups_per_tok, gi = q % groups_per_tok;
+    const int blk = gi >> 3, i = gi & 7;
+    const int k = blk * 64 + 4 * i;   // low positions k..k+3, high k+32..k+35
+    const bool live = in && tk < p.nt && kbase + k < p.K;
+    uint2 rl = make_uint2(0, 0), rh = make_uint2(0, 0);
+    if (live) {
+      const uint16_t* xt = p.x + static_cast<int64_t>(tk) * p.K + kbase + k;
+      rl = *reinterpret_cast<const uint2*>(xt);
+      rh = *reinterpret_cast<const uint2*>(xt + 32);
+    }
+    float v[8];   // staged order: (lo b, hi b) for b = 0..3
+    v[0] = __uint_as_float(rl.x << 16);
+    v[2] = __uint_as_float(rl.x & 0xFFFF0000u);
+    v[4] = __uint_as_float(rl.y << 16);
+    v[6] = __uint_as_float(rl.y & 0xFFFF0000u);
+    v[1] = __uint_as_float(rh.x << 16);
+    v[3] = __uint_as_float(rh.x & 0xFFFF0000u);
+    v[5] = __uint_as_float(rh.y << 16);
+    v[7] = __uint_as_float(rh.y & 0xFFFF0000u);
+    float slo = (v[0] + v[2]) + (v[4] + v[6]);
+    float shi = (v[1] + v[3]) + (v[5] + v[7]);
+#pragma unroll
+    for (int m = 1; m < GP; m <<= 1) {
+      slo += __shfl_xor_sync(0xFFFFFFFFu, slo, m);
+      shi += __shfl_xor_sync(0xFFFFFFFFu, shi, m);
+    }
+    if (!in) continue;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      v[2 * b] *= pow2(-field_shift<F>(true, b));
+      v[2 * b + 1] *= pow2(-field_shift<F>(false, b));
+    }
+    uint8_t* d = smem + L::addr(tk * p.kpad + blk * 64 + 8 * i);
+    if constexpr (XBF) {
+      uint32_t r[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        r[j] = (__float_as_uint(v[2 * j]) >> 16) | (__float_as_uint(v[2 * j + 1]) & 0xFFFF0000u);
+      // the bf16 layout pads by 8 bytes: a group start is 8-byte aligned
+      uint2* d2 = reinterpret_cast<uint2*>(d);
+      d2[0] = make_uint2(r[0], r[1]);
+      d2[1] = make_uint2(r[2], r[3]);
+    } else {
+      float4* d4 = reinterpret_cast<float4*>(d);
+      d4[0] = make_float4(v[0], v[1], v[2], v[3]);
+      d4[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+    if (i % GP == 0) {
+      float* o = sx + tk * parts_per_tok + blk * (64 / P) + 2 * (i / GP);
+      o[0] = slo;
+      o[1] = shi;
+    }
+  }
+}
+
+template <int F, int NT, bool XBF>
+__device__ void stage_x_q6(const Params& p, uint8_t* smem, int kbase) {
+  using G = Geo<F, NT, 1, 1>;
   using L = XLayout<F, NT, XBF>;
   constexpr int P = G::kPart;                 // positions per part sum (>= 4)
   constexpr int CH = P > 8 ? P : 8;           // positions per work item
@@ -335,6 +448,14 @@ __device__ void stage_x(const Params& p, uint8_t* smem, int kbase) {
   }
 }
 
+template <int F, int NT, bool XBF>
+__device__ __forceinline__ void stage_x(const Params& p, uint8_t* smem, int kbase) {
+  if constexpr (F == kQ6K)
+    stage_x_q6<F, NT, XBF>(p, smem, kbase);
+  else
+    stage_x_q4<F, NT, XBF>(p, smem, kbase);
+}
+
 // The four values stored at slots idx .. idx+3 (idx a multiple of 4) as two
 // float2 pairs.
 template <int F, int NT, bool XBF>
@@ -353,10 +474,32 @@ __device__ __forceinline__ void x_quad(uint32_t xs, int idx, float2& a, float2& 
 
 // ------------------------------------------------------------- producer
 
-template <int F, int NT, int RT>
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+template <class G>
 __device__ __forceinline__ void issue_stage(const Params& p, uint8_t* smem, uint32_t st_a,
                                             uint32_t full, const Tile& tl, int sl) {
-  using G = Geo<F, NT, RT>;
+  constexpr int F = G::kF;
+  if (p.tma) {
+    // one copy per plane: the slab of tile_rows rows, from the 16-byte
+    // boundary at or below the slab's first byte (x in 8-byte elements);
+    // rows past the matrix and bytes past a row are zero-filled and counted
+    if ((threadIdx.x & 31) == 0) {
+      mbar_arrive_tx(full, p.tx);
+      tma_load_2d(st_a, &p.tm[tl.mi][0], ((sl * G::kQBytes) & ~15) / 8, tl.row0, full);
+      if constexpr (F == kG128)
+        tma_load_2d(st_a + p.pbase, &p.tm[tl.mi][1], ((sl * G::kPBytes) & ~15) / 8, tl.row0,
+                    full);
+    }
+    return;
+  }
   const int lane = threadIdx.x & 31;
   const uint8_t* W = pick(p.g.W, tl.mi);
   const int64_t N = pick(p.g.N, tl.mi);
@@ -383,32 +526,17 @@ __device__ __forceinline__ void issue_stage(const Params& p, uint8_t* smem, uint
     };
     if constexpr (F == kG128) {
       const int64_t total = N * p.nsb;
-      copy_span(W, total * 128, idx * 128, nsb_here * 128, st_a + lane * G::kSlot);
+      copy_span(W, total * 128, idx * 128, nsb_here * 128, st_a + lane * p.slot);
       copy_span(W + total * 128, total * 8, idx * 8, nsb_here * 8,
-                st_a + G::kRows * G::kSlot + lane * G::kPSlot);
+                st_a + p.pbase + lane * p.pslot);
     } else {
-      copy_span(W, N * p.nsb * G::kBB, idx * G::kBB, nsb_here * G::kBB, st_a + lane * G::kSlot);
+      copy_span(W, N * p.nsb * G::kBB, idx * G::kBB, nsb_here * G::kBB, st_a + lane * p.slot);
     }
   }
   mbar_arrive_tx(full, tx);   // every producer lane arrives (count 32)
 }
 
 // ------------------------------------------------------------- consumers
-
-// 6-bit (sc, m) of sub-blocks 2c and 2c+1 from the 12-byte field words s0,
-// s1, s2 (bytes 0-3, 4-7, 8-11), two bytes each in the low 16 bits.
-__device__ __forceinline__ void scale_pairs(uint32_t s0, uint32_t s1, uint32_t s2, int c,
-                                            uint32_t& sc, uint32_t& mn) {
-  const int sh = 16 * (c & 1);
-  const uint32_t a0 = s0 >> sh, a1 = s1 >> sh, a2 = s2 >> sh;
-  if (c < 2) {
-    sc = a0 & 0x3F3Fu;
-    mn = a1 & 0x3F3Fu;
-  } else {
-    sc = (a2 & 0x0F0Fu) | ((a0 >> 2) & 0x3030u);
-    mn = ((a2 >> 4) & 0x0F0Fu) | ((a1 >> 2) & 0x3030u);
-  }
-}
 
 template <int NW>
 __device__ __forceinline__ void lds_words(uint32_t a, uint32_t (&w)[NW]) {
@@ -428,170 +556,184 @@ __device__ __forceinline__ void lds_words(uint32_t a, uint32_t (&w)[NW]) {
 __device__ __forceinline__ uint64_t u64(uint32_t lo, uint32_t hi) {
   return (static_cast<uint64_t>(hi) << 32) | lo;
 }
-__device__ __forceinline__ float2 as_f2(uint64_t v) {
-  return make_float2(__uint_as_float(static_cast<uint32_t>(v)),
-                     __uint_as_float(static_cast<uint32_t>(v >> 32)));
-}
 __device__ __forceinline__ uint64_t bitsel64(uint64_t a, uint64_t b, uint32_t m) {
   return u64(bitsel(static_cast<uint32_t>(a), static_cast<uint32_t>(b), m),
              bitsel(static_cast<uint32_t>(a >> 32), static_cast<uint32_t>(b >> 32), m));
 }
-// exact q 2^s for the field at bit s of both halves of v (width mask m):
-// one LOP3 per half builds 2^23 + q 2^s in a register pair, one packed add
-// of (-2^23, -2^23) removes the offset; the same constant pair serves every
-// field position.
-__device__ __forceinline__ float2 conv64(uint64_t v, uint32_t m) {
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  return __byte_perm(a, b, sel);
+}
+
+// Exact (q_a 2^sa, q_b 2^sb) for the field under mask MA of a and under mask
+// MB of b: one LOP3 each builds 2^23 + q 2^s (the mask an immediate, the
+// magic exponent word a register), one packed add of (-2^23, -2^23) removes
+// the offset.
+template <uint32_t MA, uint32_t MB>
+__device__ __forceinline__ float2 cvt_pair(uint32_t a, uint32_t b, uint32_t magic, uint64_t neg) {
   float2 r;
   asm("{\n\t.reg .b32 t0, t1;\n\t.reg .b64 p, q;\n\t"
-      "lop3.b32 t0, %2, %4, %5, 0xEA;\n\t"
-      "lop3.b32 t1, %3, %4, %5, 0xEA;\n\t"
+      "lop3.b32 t0, %2, %4, %6, 0xEA;\n\t"
+      "lop3.b32 t1, %3, %5, %6, 0xEA;\n\t"
       "mov.b64 p, {t0, t1};\n\t"
-      "add.rn.f32x2 q, p, %6;\n\t"
+      "add.rn.f32x2 q, p, %7;\n\t"
       "mov.b64 {%0, %1}, q;\n\t}"
       : "=f"(r.x), "=f"(r.y)
-      : "r"(static_cast<uint32_t>(v)), "r"(static_cast<uint32_t>(v >> 32)), "r"(m),
-        "r"(kMagic), "l"(0xCB000000CB000000ull));
+      : "r"(a), "r"(b), "n"(MA), "n"(MB), "r"(magic), "l"(neg));
   return r;
 }
-
-// Q4_K / Q5_K / Q4_G128 unit: kCW/2 bytes of the qs (chunk c, byte offset
-// off): low nibbles -> sub-block 2c (weights 64c + off + i), high nibbles ->
-// sub-block 2c+1 (weights 64c + 32 + off + i).  Words are taken in pairs
-// (2i, 2i+1) as 64-bit values, so each conversion and each accumulation is
-// one packed fma on a register pair.  xl[t][i][b] / xh[t][i][b] are the x
-// pairs of nibble position b of that word pair; alo/ahi hold two partial
-// sums per sub-block (word pairs alternate between them).
-template <int F, int NT, int NW>
-__device__ __forceinline__ void unit_q4(const uint32_t (&w)[NW], const uint32_t (&h)[NW], int c,
-                                        const float2 (&xl)[NT][NW / 2][4],
-                                        const float2 (&xh)[NT][NW / 2][4], float2 (&alo)[2][NT],
-                                        float2 (&ahi)[2][NT]) {
-#pragma unroll
-  for (int i = 0; i < NW / 2; ++i) {
-    const uint64_t W = u64(w[2 * i], w[2 * i + 1]);
-    float2 ql[4], qh[4];
-    if constexpr (F == kQ5K) {
-      // byte b of lo5 / hi5 = nibble | fifth bit << 4 (bits 5..7 are masked
-      // off by the 5-bit extraction masks below)
-      const int rlo = (2 * c + 28) & 31, rhi = (2 * c + 29) & 31;   // rotate bit 2c(+1) to 4
-      const uint64_t RL = u64(__funnelshift_r(h[2 * i], h[2 * i], rlo),
-                              __funnelshift_r(h[2 * i + 1], h[2 * i + 1], rlo));
-      const uint64_t RH = u64(__funnelshift_r(h[2 * i], h[2 * i], rhi),
-                              __funnelshift_r(h[2 * i + 1], h[2 * i + 1], rhi));
-      const uint32_t M = 0x0F0F0F0Fu;
-      const uint64_t L5 = bitsel64(W, RL, M), H5 = bitsel64(W >> 4, RH, M);
-      const uint64_t L5s = L5 >> 8, H5s = H5 >> 8;
-      ql[0] = conv64(L5, 0x1Fu);
-      ql[1] = conv64(L5, 0x1F00u);
-      ql[2] = conv64(L5, 0x1F0000u);
-      ql[3] = conv64(L5s, 0x1F0000u);
-      qh[0] = conv64(H5, 0x1Fu);
-      qh[1] = conv64(H5, 0x1F00u);
-      qh[2] = conv64(H5, 0x1F0000u);
-      qh[3] = conv64(H5s, 0x1F0000u);
-    } else {
-      // in W: lo b0 s=0, lo b1 s=8, lo b2 s=16, hi b0 s=4, hi b1 s=12;
-      // in W >> 12 (bits crossing the halves land above bit 19 and are
-      // masked off): lo b3 s=12, hi b2 s=8, hi b3 s=16
-      const uint64_t B = W >> 12;
-      ql[0] = conv64(W, 0xFu);
-      ql[1] = conv64(W, 0xF00u);
-      ql[2] = conv64(W, 0xF0000u);
-      ql[3] = conv64(B, 0xF000u);
-      qh[0] = conv64(W, 0xF0u);
-      qh[1] = conv64(W, 0xF000u);
-      qh[2] = conv64(B, 0xF00u);
-      qh[3] = conv64(B, 0xF0000u);
-    }
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        alo[i & 1][t] = __ffma2_rn(ql[b], xl[t][i][b], alo[i & 1][t]);
-        ahi[i & 1][t] = __ffma2_rn(qh[b], xh[t][i][b], ahi[i & 1][t]);
-      }
-  }
+// the same field of both halves of v
+template <uint32_t M>
+__device__ __forceinline__ float2 conv64(uint64_t v, uint32_t magic, uint64_t neg) {
+  return cvt_pair<M, M>(static_cast<uint32_t>(v), static_cast<uint32_t>(v >> 32), magic, neg);
 }
 
-// One stage of a Q4_K / Q5_K / Q4_G128 tile for this thread's rows.
-template <int F, int NT, int RT, bool XBF>
+constexpr uint64_t kNegMagic2 = 0xCB000000CB000000ull;   // (-2^23, -2^23)
+
+// Per-lane constants of the 6-bit (sc, m) decode of Q4_K / Q5_K for the two
+// sub-blocks 2c and 2c+1 of the lane's chunk c (bytes j = 2c, 2c+1 of the
+// 12-byte field, words s0 = bytes 0-3, s1 = 4-7, s2 = 8-11 of the field).
+// j < 4: sc = s0[j] & 63, m = s1[j] & 63; j >= 4: sc = (s2[j-4] & 15) |
+// (s0[j-4] >> 6) << 4, m = (s2[j-4] >> 4) | (s1[j-4] >> 6) << 4.  Both cases
+// are (A & 0x0F0F) | (B & 0x3030) of the byte pair at 16 (c & 1) in suitably
+// shifted words, so every lane runs the same instructions.
+struct ScaleSel {
+  bool hi;        // c >= 2
+  uint32_t sh;    // 16 (c & 1)
+  uint32_t shb;   // shift of the word giving bits 4-5: sh (+2 when hi)
+  uint32_t shm;   // shift of the word giving m's bits 0-3: sh (+4 when hi)
+};
+__device__ __forceinline__ ScaleSel scale_sel(int c) {
+  ScaleSel r;
+  r.hi = c >= 2;
+  r.sh = 16u * static_cast<uint32_t>(c & 1);
+  r.shb = r.sh + (r.hi ? 2u : 0u);
+  r.shm = r.sh + (r.hi ? 4u : 0u);
+  return r;
+}
+// (sc, m) byte pairs (sub-block 2c in byte 0, 2c+1 in byte 1), 6 bits each
+__device__ __forceinline__ void scale_pair6(const ScaleSel& q, uint32_t s0, uint32_t s1,
+                                            uint32_t s2, uint32_t& sc, uint32_t& mn) {
+  const uint32_t a_sc = (q.hi ? s2 : s0) >> q.sh;
+  const uint32_t a_m = (q.hi ? s2 : s1) >> q.shm;
+  sc = (a_sc & 0x0F0Fu) | ((s0 >> q.shb) & 0x3030u);
+  mn = (a_m & 0x0F0Fu) | ((s1 >> q.shb) & 0x3030u);
+}
+
+// One stage of a Q4_K / Q5_K / Q4_G128 tile for this thread's rows.  The
+// lane's unit is bytes off .. off + kCW/2 of chunk c of super-block sbl of
+// the slab: the low nibbles belong to sub-block 2c (weights 64c + off + r),
+// the high nibbles to 2c+1 (weights 64c + 32 + off + r).  Every byte gives
+// one (low, high) pair: converted with one cvt_pair and accumulated with one
+// packed fma against the staged (x_lo, x_hi) pair, so the accumulators hold
+// (sub-block 2c, sub-block 2c+1) sums and the scales apply as pairs too:
+//   acc += (d sc_lo, d sc_hi) * S + (-dmin m_lo, -dmin m_hi) * (sx_lo, sx_hi)
+// acc[r][k] is a pair whose two halves are added at the end of the tile.
+template <int F, int NT, int RT, int WC, int NR, bool XBF>
 __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl, int xsl,
                                          uint32_t st, uint32_t xs, int hw, int sbl, int c,
-                                         int off, float (&acc)[RT][NT]) {
-  using G = Geo<F, NT, RT>;
+                                         int off, const ScaleSel& ss, float2 (&acc)[RT][NT]) {
+  using G = Geo<F, NT, RT, WC>;
   using L = XLayout<F, NT, XBF>;
   constexpr int kCW = G::kCW, NW = kCW / 8;
-  float2 xl[NT][NW / 2][4], xh[NT][NW / 2][4];
-  float sxlo[NT], sxhi[NT];
-  const int k0 = xsl * G::kSlabK + sbl * 256 + 64 * c + off;   // first lo position (staged x)
+  const uint32_t magic = kMagic;
+  const uint64_t neg = kNegMagic2;
+  // x pairs of the unit: xp[k][i][b] = (x_lo, x_hi) of byte b of word i
+  float2 xp[NT][NW][4];
+  float2 sxp[NT];
+  const int kb = xsl * G::kSlabK + sbl * 256 + 64 * c;   // the chunk's 64-block
   const uint32_t sxa = xs + static_cast<uint32_t>(L::bytes(static_cast<size_t>(NT) * p.kpad));
   const int parts = p.kpad / G::kPart;
 #pragma unroll
   for (int k = 0; k < NT; ++k) {
 #pragma unroll
-    for (int i = 0; i < NW / 2; ++i) {
-      const int g = k * p.kpad + k0 + 8 * i;   // aligned group of 8 (interleaved)
-      x_quad<F, NT, XBF>(xs, g, xl[k][i][0], xl[k][i][1]);
-      x_quad<F, NT, XBF>(xs, g + 4, xl[k][i][2], xl[k][i][3]);
-      x_quad<F, NT, XBF>(xs, g + 32, xh[k][i][0], xh[k][i][1]);
-      x_quad<F, NT, XBF>(xs, g + 36, xh[k][i][2], xh[k][i][3]);
+    for (int i = 0; i < NW; ++i) {
+      const int g = k * p.kpad + kb + 2 * off + 8 * i;
+      x_quad<F, NT, XBF>(xs, g, xp[k][i][0], xp[k][i][1]);
+      x_quad<F, NT, XBF>(xs, g + 4, xp[k][i][2], xp[k][i][3]);
     }
-    sxlo[k] = __uint_as_float(lds32(sxa + 4 * (k * parts + k0 / G::kPart)));
-    sxhi[k] = __uint_as_float(lds32(sxa + 4 * (k * parts + (k0 + 32) / G::kPart)));
+    sxp[k] = lds_f2(sxa + 4 * (k * parts + (kb / 64) * (64 / G::kPart) + 2 * (off / G::kPart)));
+  }
+  // the rows' weight words and scale pairs
+  uint32_t w[NR][NW], hq[NR][NW];
+  float2 dsc[NR], ndm[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    const int row = hw + 2 * WC * r;
+    const uint32_t rs = st + row * p.slot;
+#pragma unroll
+    for (int j = 0; j < NW; ++j) hq[r][j] = 0;
+    if constexpr (F == kG128) {
+      lds_words<NW>(rs + 128 * sbl + 32 * c + off, w[r]);
+      const int64_t pstart =
+          ((tl.row0 + row) * static_cast<int64_t>(p.nsb) + sl * G::kSlabSB) * 8;
+      const uint32_t pa = st + p.pbase + row * p.pslot +
+                          static_cast<uint32_t>(pstart & 15) + 8 * sbl;
+      const uint2 pr = lds64(pa);
+      const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
+      const int g = c >> 1;
+      const float sc = static_cast<float>((pr.y >> (8 * g)) & 0xFF);
+      const float mn = static_cast<float>((pr.y >> (16 + 8 * g)) & 0xFF);
+      dsc[r] = make_float2(dd.x * sc, dd.x * sc);
+      ndm[r] = make_float2(-dd.y * mn, -dd.y * mn);
+    } else {
+      const uint32_t rec = rs + G::kBB * sbl;
+      const uint4 hdr = lds128(rec);
+      lds_words<NW>(rec + (F == kQ4K ? 16 : 48) + 32 * c + off, w[r]);
+      if constexpr (F == kQ5K) lds_words<NW>(rec + 16 + off, hq[r]);
+      const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
+      uint32_t scp, mnp;
+      scale_pair6(ss, hdr.y, hdr.z, hdr.w, scp, mnp);
+      dsc[r] = make_float2(dd.x * static_cast<float>(scp & 0xFF),
+                           dd.x * static_cast<float>(scp >> 8));
+      ndm[r] = make_float2(-dd.y * static_cast<float>(mnp & 0xFF),
+                           -dd.y * static_cast<float>(mnp >> 8));
+    }
+  }
+  float2 A[NR][NT][2];
+#pragma unroll
+  for (int r = 0; r < NR; ++r)
+#pragma unroll
+    for (int k = 0; k < NT; ++k) A[r][k][0] = A[r][k][1] = make_float2(0.0f, 0.0f);
+  const int rlo = (2 * c + 28) & 31, rhi = (2 * c + 29) & 31;   // Q5_K: bit 2c(+1) -> bit 4
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      const uint32_t v = w[r][i];
+      float2 q[4];
+      if constexpr (F == kQ5K) {
+        const uint32_t h = hq[r][i];
+        // byte b of lo5 / hi5 = nibble | fifth bit << 4 (bits 5..7 are
+        // masked off by the 5-bit extraction masks)
+        const uint32_t lo5 = bitsel(v, __funnelshift_r(h, h, rlo), 0x0F0F0F0Fu);
+        const uint32_t hi5 = bitsel(v >> 4, __funnelshift_r(h, h, rhi), 0x0F0F0F0Fu);
+        const uint32_t b3 = prmt(lo5, hi5, 0x0703u);   // lo5 byte 3 -> byte 0, hi5 byte 3 -> byte 2
+        q[0] = cvt_pair<0x1Fu, 0x1Fu>(lo5, hi5, magic, neg);
+        q[1] = cvt_pair<0x1F00u, 0x1F00u>(lo5, hi5, magic, neg);
+        q[2] = cvt_pair<0x1F0000u, 0x1F0000u>(lo5, hi5, magic, neg);
+        q[3] = cvt_pair<0x1Fu, 0x1F0000u>(b3, b3, magic, neg);
+      } else {
+        // lo b0 s0, hi b0 s4, lo b1 s8, hi b1 s12, lo b2 s16 from v; from
+        // v >> 12: hi b2 s8, lo b3 s12, hi b3 s16
+        const uint32_t u = v >> 12;
+        q[0] = cvt_pair<0xFu, 0xF0u>(v, v, magic, neg);
+        q[1] = cvt_pair<0xF00u, 0xF000u>(v, v, magic, neg);
+        q[2] = cvt_pair<0xF0000u, 0xF00u>(v, u, magic, neg);
+        q[3] = cvt_pair<0xF000u, 0xF0000u>(u, u, magic, neg);
+      }
+#pragma unroll
+      for (int k = 0; k < NT; ++k)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) A[r][k][i & 1] = __ffma2_rn(q[b], xp[k][i][b], A[r][k][i & 1]);
+    }
   }
 #pragma unroll
-  for (int r = 0; r < RT; ++r) {
-    const int row = hw + 2 * kWC * r;
-    if (row < tl.rcnt) {
-      const uint32_t rs = st + row * G::kSlot;
-      uint32_t w[NW], hq[NW];
-      float2 dsc, dmn;
+  for (int r = 0; r < NR; ++r) {
 #pragma unroll
-      for (int j = 0; j < NW; ++j) hq[j] = 0;
-      if constexpr (F == kG128) {
-        lds_words<NW>(rs + 128 * sbl + 32 * c + off, w);
-        const int64_t pstart =
-            ((tl.row0 + row) * static_cast<int64_t>(p.nsb) + sl * G::kSlabSB) * 8;
-        const uint32_t pa = st + G::kRows * G::kSlot + row * G::kPSlot +
-                            static_cast<uint32_t>(pstart & 15) + 8 * sbl;
-        const uint2 pr = lds64(pa);
-        const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
-        const int g = c >> 1;
-        const float sc = static_cast<float>((pr.y >> (8 * g)) & 0xFF);
-        const float mn = static_cast<float>((pr.y >> (16 + 8 * g)) & 0xFF);
-        dsc = make_float2(dd.x * sc, dd.x * sc);
-        dmn = make_float2(dd.y * mn, dd.y * mn);
-      } else {
-        const uint32_t rec = rs + G::kBB * sbl;
-        const uint4 hdr = lds128(rec);
-        lds_words<NW>(rec + (F == kQ4K ? 16 : 48) + 32 * c + off, w);
-        if constexpr (F == kQ5K) lds_words<NW>(rec + 16 + off, hq);
-        const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
-        uint32_t scp, mnp;
-        scale_pairs(hdr.y, hdr.z, hdr.w, c, scp, mnp);
-        dsc = make_float2(dd.x * static_cast<float>(scp & 0xFF),
-                          dd.x * static_cast<float>(scp >> 8));
-        dmn = make_float2(dd.y * static_cast<float>(mnp & 0xFF),
-                          dd.y * static_cast<float>(mnp >> 8));
-      }
-      float2 alo[2][NT], ahi[2][NT];
-#pragma unroll
-      for (int k = 0; k < NT; ++k) {
-        alo[0][k] = alo[1][k] = make_float2(0.0f, 0.0f);
-        ahi[0][k] = ahi[1][k] = make_float2(0.0f, 0.0f);
-      }
-      unit_q4<F, NT, NW>(w, hq, c, xl, xh, alo, ahi);
-#pragma unroll
-      for (int k = 0; k < NT; ++k) {
-        const float slo = (alo[0][k].x + alo[1][k].x) + (alo[0][k].y + alo[1][k].y);
-        const float shi = (ahi[0][k].x + ahi[1][k].x) + (ahi[0][k].y + ahi[1][k].y);
-        float v = acc[r][k];
-        v = fmaf(dsc.x, slo, v);
-        v = fmaf(dsc.y, shi, v);
-        v = fmaf(-dmn.x, sxlo[k], v);
-        v = fmaf(-dmn.y, sxhi[k], v);
-        acc[r][k] = v;
-      }
+    for (int k = 0; k < NT; ++k) {
+      const float2 S = (NW > 1) ? __fadd2_rn(A[r][k][0], A[r][k][1]) : A[r][k][0];
+      acc[r][k] = __ffma2_rn(dsc[r], S, acc[r][k]);
+      acc[r][k] = __ffma2_rn(ndm[r], sxp[k], acc[r][k]);
     }
   }
 }
@@ -600,12 +742,12 @@ __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl
 // t < 4, i < kCW/4 (l0 = u2 kCW/4); sub-block of (t, l) = 8h + 2t + l/16.
 // Records start on 2-byte boundaries: words are read aligned and shifted.
 // With at least two words per t-run the words are paired (64-bit), as in
-// unit_q4; with one word (n_tok 4) each word is used alone.
-template <int NT, int RT, bool XBF>
+// stage_q4; with one word (n_tok 4) each word is used alone.
+template <int NT, int RT, int WC, bool XBF>
 __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl, int xsl,
                                          uint32_t st, uint32_t xs, int hw, int sbl, int un,
-                                         float (&acc)[RT][NT]) {
-  using G = Geo<kQ6K, NT, RT>;
+                                         float2 (&acc)[RT][NT]) {
+  using G = Geo<kQ6K, NT, RT, WC>;
   using L = XLayout<kQ6K, NT, XBF>;
   constexpr int kCW = G::kCW, QW = kCW / 16;
   constexpr bool kPaired = L::kInterleave;
@@ -638,11 +780,11 @@ __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl
       }
 #pragma unroll
   for (int r = 0; r < RT; ++r) {
-    const int row = hw + 2 * kWC * r;
+    const int row = hw + 2 * WC * r;
     if (row < tl.rcnt) {
       const int64_t start =
           ((tl.row0 + row) * static_cast<int64_t>(p.nsb) + sl * G::kSlabSB) * 210;
-      const uint32_t rec = st + row * G::kSlot + static_cast<uint32_t>(start & 15) + 210 * sbl;
+      const uint32_t rec = st + row * p.slot + static_cast<uint32_t>(start & 15) + 210 * sbl;
       uint32_t A[QW], B[QW], H[QW], S[2], D[1];
       lds_words_a2<QW>(rec + 64 * h + l0, A);
       lds_words_a2<QW>(rec + 64 * h + 32 + l0, B);
@@ -671,10 +813,10 @@ __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl
           for (int tt = 0; tt < 4; ++tt) {
             const uint64_t v = q6[tt], vs = v >> 8;
             float2 q[4];
-            q[0] = conv64(v, 0x3Fu);
-            q[1] = conv64(v, 0x3F00u);
-            q[2] = conv64(v, 0x3F0000u);
-            q[3] = conv64(vs, 0x3F0000u);
+            q[0] = conv64<0x3Fu>(v, kMagic, kNegMagic2);
+            q[1] = conv64<0x3F00u>(v, kMagic, kNegMagic2);
+            q[2] = conv64<0x3F0000u>(v, kMagic, kNegMagic2);
+            q[3] = conv64<0x3F0000u>(vs, kMagic, kNegMagic2);
 #pragma unroll
             for (int k = 0; k < NT; ++k)
 #pragma unroll
@@ -711,7 +853,7 @@ __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl
         const float ds = d * static_cast<float>(sc);
 #pragma unroll
         for (int k = 0; k < NT; ++k)
-          acc[r][k] = fmaf(ds, fmaf(-32.0f, sxt[k][tt], at[k][tt].x + at[k][tt].y), acc[r][k]);
+          acc[r][k].x = fmaf(ds, fmaf(-32.0f, sxt[k][tt], at[k][tt].x + at[k][tt].y), acc[r][k].x);
       }
     }
   }
@@ -719,9 +861,11 @@ __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl
 
 constexpr int kMaxStages = 8;
 
-template <int F, int NT, int RT, bool XBF>
-__global__ void __launch_bounds__(kThreads) gemv_stream(const Params p, int stages) {
-  using G = Geo<F, NT, RT>;
+// Registers capped so that three CTAs fit an SM.
+template <int F, int NT, int RT, int WC, bool XBF>
+__global__ void __launch_bounds__((WC + 1) * 32, 3)
+    gemv_stream(const __grid_constant__ Params p, int stages) {
+  using G = Geo<F, NT, RT, WC>;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
   __shared__ int last_flag;
@@ -729,7 +873,6 @@ __global__ void __launch_bounds__(kThreads) gemv_stream(const Params p, int stag
   const uint32_t bar_empty = smem_addr(&bars[kMaxStages]);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t xs = smem_addr(smem);
-  uint8_t* ring = smem + p.x_bytes;
   const uint32_t ring_a = xs + p.x_bytes;
   // CTA c works on K segment c % ksplit and on tiles c / ksplit + i * cps
   const int kseg = static_cast<int>(blockIdx.x) % p.ksplit;
@@ -740,13 +883,13 @@ __global__ void __launch_bounds__(kThreads) gemv_stream(const Params p, int stag
   const int sl0 = kseg * p.slabs;         // first slab (of the row) of the segment
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(bar_full + 8 * s, 32);      // every producer lane arrives
-      mbar_init(bar_empty + 8 * s, kWC);    // one arrival per consumer warp
+      mbar_init(bar_full + 8 * s, p.tma ? 1 : 32);   // the issuing lane / every producer lane
+      mbar_init(bar_empty + 8 * s, WC);     // one arrival per consumer warp
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  const bool producer = warp == kWC;
+  const bool producer = warp == WC;
   const int first = total < stages ? total : stages;
   // Programmatic dependent launch: the next kernel on the stream may start
   // its CTAs as SMs free up; it reads its activations and touches the
@@ -758,13 +901,12 @@ __global__ void __launch_bounds__(kThreads) gemv_stream(const Params p, int stag
     // (no empty wait needed) streams while that kernel may still be running
     for (int it = 0; it < first; ++it) {
       const Tile tl = tile_of(p, cta + (it / p.slabs) * cps);
-      issue_stage<F, NT, RT>(p, smem, ring_a + it * G::kStage, bar_full + 8 * it, tl,
-                             sl0 + it % p.slabs);
+      issue_stage<G>(p, smem, ring_a + it * p.stage, bar_full + 8 * it, tl, sl0 + it % p.slabs);
     }
   }
   // x may be produced by the previous kernel: wait for it to complete
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  stage_x<F, NT, RT, XBF>(p, smem, kseg * p.kpad);
+  stage_x<F, NT, XBF>(p, smem, kseg * p.kpad);
   __syncthreads();
   if (producer) {
     for (int it = first; it < total; ++it) {
@@ -773,20 +915,21 @@ __global__ void __launch_bounds__(kThreads) gemv_stream(const Params p, int stag
       if (!mbar_wait_warp(bar_empty + 8 * slot, (use - 1) & 1)) return;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       const Tile tl = tile_of(p, cta + (it / p.slabs) * cps);
-      issue_stage<F, NT, RT>(p, smem, ring_a + slot * G::kStage, bar_full + 8 * slot, tl,
-                             sl0 + it % p.slabs);
+      issue_stage<G>(p, smem, ring_a + slot * p.stage, bar_full + 8 * slot, tl,
+                     sl0 + it % p.slabs);
     }
     return;
   }
   // consumers
   constexpr int kCW = G::kCW;
-  const int hw = 2 * warp + (lane >> 4);   // half-warp: rows hw + 8 r of a tile
+  const int hw = 2 * warp + (lane >> 4);   // half-warp: rows hw + 2 WC r of a tile
   const int ul = lane & 15;                // unit position in the slab
   const int sbl = ul / G::kUnitsPerSB;     // super-block in the slab
   const int un = ul % G::kUnitsPerSB;      // unit in the super-block
   const int c = un / (64 / kCW);           // Q4 family: chunk
   const int off = (un % (64 / kCW)) * (kCW / 2);
-  float acc[RT][NT];
+  const ScaleSel ss = scale_sel(c);
+  float2 acc[RT][NT];
   Tile tl{};
   int t = 0;
   for (int it = 0; it < total; ++it) {
@@ -798,31 +941,47 @@ __global__ void __launch_bounds__(kThreads) gemv_stream(const Params p, int stag
 #pragma unroll
       for (int r = 0; r < RT; ++r)
 #pragma unroll
-        for (int k = 0; k < NT; ++k) acc[r][k] = 0.0f;
+        for (int k = 0; k < NT; ++k) acc[r][k] = make_float2(0.0f, 0.0f);
     }
     const int slot = it % stages;
     const uint32_t use = static_cast<uint32_t>(it / stages);
     if (!mbar_wait_warp(bar_full + 8 * slot, use & 1)) return;
-    const uint32_t st = ring_a + slot * G::kStage;
+    const uint32_t st = ring_a + slot * p.stage;
     if (sl * G::kSlabSB + sbl < p.nsb) {
-      if constexpr (F == kQ6K)
-        stage_q6<NT, RT, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, un, acc);
-      else
-        stage_q4<F, NT, RT, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, c, off, acc);
+      if constexpr (F == kQ6K) {
+        stage_q6<NT, RT, WC, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, un, acc);
+      } else {
+        // rows of this half-warp inside the tile (the same for all its lanes)
+        const int nr = tl.rcnt > hw ? min(RT, (tl.rcnt - hw + 2 * WC - 1) / (2 * WC)) : 0;
+        if (nr == RT) {
+          stage_q4<F, NT, RT, WC, RT, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, c, off, ss, acc);
+        } else if constexpr (RT >= 2) {
+          if (nr == 1)
+            stage_q4<F, NT, RT, WC, 1, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, c, off, ss, acc);
+          if constexpr (RT == 4) {
+            if (nr == 2)
+              stage_q4<F, NT, RT, WC, 2, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, c, off, ss, acc);
+            else if (nr == 3)
+              stage_q4<F, NT, RT, WC, 3, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, c, off, ss, acc);
+          }
+        }
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
     if (xsl == p.slabs - 1) {
 #pragma unroll
+      float red[RT][NT];
+#pragma unroll
       for (int r = 0; r < RT; ++r)
 #pragma unroll
         for (int k = 0; k < NT; ++k) {
-          float v = acc[r][k];
+          float v = acc[r][k].x + acc[r][k].y;
           v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
           v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
           v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
           v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-          acc[r][k] = v;
+          red[r][k] = v;
         }
       float* y = pick(p.g.y, tl.mi);
       const int64_t N = pick(p.g.N, tl.mi);
@@ -830,11 +989,11 @@ __global__ void __launch_bounds__(kThreads) gemv_stream(const Params p, int stag
         if (ul == 0) {
 #pragma unroll
           for (int r = 0; r < RT; ++r) {
-            const int row = hw + 2 * kWC * r;
+            const int row = hw + 2 * WC * r;
             if (row < tl.rcnt) {
 #pragma unroll
               for (int k = 0; k < NT; ++k)
-                if (k < p.nt) y[static_cast<int64_t>(k) * N + tl.row0 + row] = acc[r][k];
+                if (k < p.nt) y[static_cast<int64_t>(k) * N + tl.row0 + row] = red[r][k];
             }
           }
         }
@@ -847,23 +1006,23 @@ __global__ void __launch_bounds__(kThreads) gemv_stream(const Params p, int stag
         if (ul == 0) {
 #pragma unroll
           for (int r = 0; r < RT; ++r) {
-            const int row = hw + 2 * kWC * r;
+            const int row = hw + 2 * WC * r;
             if (row < tl.rcnt) {
 #pragma unroll
-              for (int k = 0; k < NT; ++k) __stcg(part + kseg * seg_stride + row * NT + k, acc[r][k]);
+              for (int k = 0; k < NT; ++k) __stcg(part + kseg * seg_stride + row * NT + k, red[r][k]);
             }
           }
           __threadfence();
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(kWC * 32) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"r"(WC * 32) : "memory");
         if (threadIdx.x == 0) last_flag = atomicAdd(p.arrivals + t, 1u) == static_cast<unsigned>(p.ksplit - 1);
-        asm volatile("bar.sync 1, %0;" ::"r"(kWC * 32) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"r"(WC * 32) : "memory");
         if (last_flag) {
           __threadfence();
           if (ul == 0) {
 #pragma unroll
             for (int r = 0; r < RT; ++r) {
-              const int row = hw + 2 * kWC * r;
+              const int row = hw + 2 * WC * r;
               if (row < tl.rcnt) {
 #pragma unroll
                 for (int k = 0; k < NT; ++k) {
@@ -883,7 +1042,9 @@ __global__ void __launch_bounds__(kThreads) gemv_stream(const Params p, int stag
 
 struct DevInfo {
   int sms = 0;
-  size_t smem_optin = 0;
+  size_t smem_optin = 0;      // dynamic + static shared memory one CTA may use
+  size_t smem_sm = 0;         // shared memory of one SM
+  size_t smem_reserved = 0;   // shared memory the driver reserves per CTA
 };
 
 DevInfo& dev_info() {
@@ -896,11 +1057,15 @@ DevInfo& dev_info() {
     int v = 0;
     cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
     i.smem_optin = static_cast<size_t>(v);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d);
+    i.smem_sm = static_cast<size_t>(v);
+    cudaDeviceGetAttribute(&v, cudaDevAttrReservedSharedMemoryPerBlock, d);
+    i.smem_reserved = static_cast<size_t>(v);
   }
   return i;
 }
 
-constexpr size_t kSmemPerSM = 228 * 1024;   // usable shared memory per SM (B300)
+constexpr size_t kStaticSmem = 256;   // the kernel's static shared memory (barriers, flag), rounded up
 
 // Split-K scratch of the current device: a fixed region of kMaxTiles arrival
 // counters, then the partial sums.  The counter region never moves or
@@ -952,9 +1117,10 @@ struct Plan {
   size_t smem = 0;
 };
 
-template <int F, int NT, int RT, bool XBF>
-Plan make_plan(int K, int ksplit) {
-  using G = Geo<F, NT, RT>;
+template <int F, int NT, int RT, int WC, bool XBF>
+Plan make_plan(int K, int ksplit, bool tma) {
+  using G = Geo<F, NT, RT, WC>;
+  const size_t stage = stage_shape<G>(tma).bytes;
   Plan pl;
   const int slabs_row = (K / 256 + G::kSlabSB - 1) / G::kSlabSB;
   if (slabs_row % ksplit != 0) return pl;
@@ -962,16 +1128,18 @@ Plan make_plan(int K, int ksplit) {
   const size_t xb = XLayout<F, NT, XBF>::bytes(static_cast<size_t>(NT) * kpad) +
                     static_cast<size_t>(NT) * (kpad / G::kPart) * 4;
   pl.x_bytes = static_cast<uint32_t>((xb + 127) & ~size_t{127});
-  const size_t optin = dev_info().smem_optin;
+  const DevInfo& di = dev_info();
   for (int per_sm = 3; per_sm >= 1; --per_sm) {
-    size_t budget = (per_sm == 1 ? optin : kSmemPerSM / per_sm) - 2048;
-    if (budget > optin - 1024) budget = optin - 1024;
-    if (pl.x_bytes + 2 * static_cast<size_t>(G::kStage) > budget) continue;
-    int stages = static_cast<int>((budget - pl.x_bytes) / G::kStage);
+    // dynamic shared memory of one CTA when per_sm CTAs share an SM
+    size_t budget = di.smem_sm / per_sm;
+    budget = budget > di.smem_reserved + kStaticSmem ? budget - di.smem_reserved - kStaticSmem : 0;
+    if (budget > di.smem_optin - kStaticSmem) budget = di.smem_optin - kStaticSmem;
+    if (pl.x_bytes + 2 * stage > budget) continue;
+    int stages = static_cast<int>((budget - pl.x_bytes) / stage);
     if (stages > kMaxStages) stages = kMaxStages;
     pl.per_sm = per_sm;
     pl.stages = stages;
-    pl.smem = pl.x_bytes + static_cast<size_t>(stages) * G::kStage;
+    pl.smem = pl.x_bytes + static_cast<size_t>(stages) * stage;
     return pl;
   }
   return pl;
@@ -989,11 +1157,61 @@ constexpr int kNoAllocMaxTiles = 1 << 14;
 constexpr size_t kNoAllocCounterBytes = size_t{kNoAllocMaxTiles} * sizeof(unsigned int);
 constexpr size_t kNoAllocScratchBytes = size_t{2} << 20;   // 2 MiB per device
 
-template <int F, int NT, int RT, bool XBF>
+// cuTensorMapEncodeTiled, fetched from the driver once (nullptr if absent).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// 2-D tensor map of one plane: `rows` rows of row_bytes (a multiple of 16)
+// seen as 8-byte elements; box = box_bytes (a multiple of 16) x box_rows.
+// Out-of-range elements of a box read as zero.
+bool encode_plane(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows,
+                  uint32_t box_bytes, uint32_t box_rows) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr || row_bytes % 16 != 0 || reinterpret_cast<uintptr_t>(base) % 16 != 0 ||
+      box_bytes % 16 != 0 || box_bytes / 8 > 256 || box_rows < 1 || box_rows > 256)
+    return false;
+  const cuuint64_t dims[2] = {row_bytes / 8, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_bytes / 8, box_rows};
+  const cuuint32_t elem[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(base), dims, strides, box,
+            elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor copies need every plane's row stride on the 16-byte grid (always
+// for Q4_K and Q5_K; Q6_K when K / 256 is a multiple of 8; the G128 param
+// plane when K / 256 is even).
+template <class G>
+bool tma_possible(int K) {
+  const int64_t nsb = K / 256;
+  if (encode_tiled() == nullptr) return false;
+  if ((nsb * G::kBB) % 16 != 0 && G::kF != kG128) return false;
+  if (G::kF == kG128 && (nsb * 8) % 16 != 0) return false;
+  return true;
+}
+
+template <int F, int NT, int RT, int WC, bool XBF>
 bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
-                int ksplit, ScratchSrc src = ScratchSrc::kDevice,
+                int ksplit, bool tma, ScratchSrc src = ScratchSrc::kDevice,
                 StaticScratch* st = nullptr) {
-  using G = Geo<F, NT, RT>;
+  using G = Geo<F, NT, RT, WC>;
   const DevInfo& di = dev_info();
   Params p;
   p.g = g;
@@ -1008,15 +1226,21 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   p.nt = n_tok;
   p.part = nullptr;
   p.arrivals = nullptr;
-  const Plan pl = make_plan<F, NT, RT, XBF>(K, ksplit);
+  const Plan pl = make_plan<F, NT, RT, WC, XBF>(K, ksplit, tma);
   if (pl.per_sm == 0) return false;
+  const StageShape ss = stage_shape<G>(tma);
+  p.tma = tma ? 1 : 0;
+  p.slot = ss.slot;
+  p.pslot = ss.pslot;
+  p.pbase = ss.pbase;
+  p.stage = ss.bytes;
   p.x_bytes = pl.x_bytes;
   int per_sm = pl.per_sm;
   const int stages = pl.stages;
   const size_t smem = pl.smem;
   static size_t configured = 0;   // dynamic shared memory above 48 KB is opt-in
   if (smem > configured) {
-    if (cudaFuncSetAttribute(gemv_stream<F, NT, RT, XBF>,
+    if (cudaFuncSetAttribute(gemv_stream<F, NT, RT, WC, XBF>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess) {
       (void)cudaGetLastError();
@@ -1025,7 +1249,7 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
     configured = smem;
   }
   int occ = 0;   // registers may allow fewer CTAs than shared memory does
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_stream<F, NT, RT, XBF>, kThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_stream<F, NT, RT, WC, XBF>, G::kThreads,
                                                     smem) == cudaSuccess &&
       occ >= 1 && occ < per_sm)
     per_sm = occ;
@@ -1048,6 +1272,22 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
     p.tile_end[i] = p.tiles;
   }
   if (cps > p.tiles) cps = p.tiles;
+  p.tx = 0;
+  if (tma) {
+    for (int i = 0; i < g.count; ++i) {
+      const int64_t n = g.N[i];
+      bool ok;
+      if constexpr (F == kG128) {
+        ok = encode_plane(&p.tm[i][0], g.W[i], 128 * static_cast<uint64_t>(p.nsb), n, ss.slot, tr) &&
+             encode_plane(&p.tm[i][1], g.W[i] + n * p.nsb * 128, 8 * static_cast<uint64_t>(p.nsb), n,
+                          ss.pslot, tr);
+      } else {
+        ok = encode_plane(&p.tm[i][0], g.W[i], static_cast<uint64_t>(p.nsb) * G::kBB, n, ss.slot, tr);
+      }
+      if (!ok) return false;
+    }
+    p.tx = static_cast<uint32_t>(tr) * (ss.slot + ss.pslot);
+  }
   if (ksplit > 1) {
     const size_t part_bytes =
         static_cast<size_t>(ksplit) * p.tiles * p.tile_rows * NT * sizeof(float);
@@ -1074,7 +1314,7 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(cps * ksplit));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(G::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1082,25 +1322,26 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_stream<F, NT, RT, XBF>, p, stages) == cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, gemv_stream<F, NT, RT, WC, XBF>, p, stages) == cudaSuccess;
 }
 
-template <int F, int NT, int RT>
+template <int F, int NT, int RT, int WC>
 bool launch_rt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
                ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
-  using G = Geo<F, NT, RT>;
+  using G = Geo<F, NT, RT, WC>;
   // K segments: the fewest (a power of two dividing the slabs of a row, at
   // most 16) that reach three CTAs per SM, else the fewest that reach the
   // most CTAs per SM.  x is staged as bf16 only when its fp32 copy would not
   // fit at all.
   const int slabs_row = (K / 256 + G::kSlabSB - 1) / G::kSlabSB;
+  const bool tma = tma_possible<G>(K);
   int best_ks = 0, best_sm = 0;
   bool best_bf = false;
   for (int ks = 1; ks <= 16 && slabs_row % ks == 0; ks *= 2) {
-    Plan pl = make_plan<F, NT, RT, false>(K, ks);
+    Plan pl = make_plan<F, NT, RT, WC, false>(K, ks, tma);
     bool bf = false;
     if (pl.per_sm == 0) {
-      pl = make_plan<F, NT, RT, true>(K, ks);
+      pl = make_plan<F, NT, RT, WC, true>(K, ks, tma);
       bf = true;
     }
     if (pl.per_sm > best_sm) {
@@ -1112,8 +1353,8 @@ bool launch_rt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStre
   }
   if (best_ks == 0) return false;
   for (int ks = best_ks;; ks = 1) {
-    const bool ok = best_bf ? launch_cfg<F, NT, RT, true>(g, x, K, n_tok, s, ks, src, st)
-                            : launch_cfg<F, NT, RT, false>(g, x, K, n_tok, s, ks, src, st);
+    const bool ok = best_bf ? launch_cfg<F, NT, RT, WC, true>(g, x, K, n_tok, s, ks, tma, src, st)
+                            : launch_cfg<F, NT, RT, WC, false>(g, x, K, n_tok, s, ks, tma, src, st);
     if (ok || ks == 1) return ok;   // no scratch (e.g. during capture): unsplit
     if (st != nullptr && st->too_large) return false;
     best_bf = static_cast<size_t>(NT) * K * 4 > 96 * 1024;
@@ -1124,11 +1365,12 @@ template <int F, int NT>
 bool launch_nt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
                ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
   const DevInfo& di = dev_info();
-  // rows per thread: 4, or 2 for small matrices (fewer than 16 rows per SM)
+  // 4 consumer warps; rows per thread: 4, or 2 for small matrices (fewer
+  // than 16 rows per SM).
   int64_t rows = 0;
   for (int i = 0; i < g.count; ++i) rows += g.N[i];
-  if (rows < 16LL * di.sms) return launch_rt<F, NT, 2>(g, x, K, n_tok, s, src, st);
-  return launch_rt<F, NT, 4>(g, x, K, n_tok, s, src, st);
+  if (rows < 16LL * di.sms) return launch_rt<F, NT, 2, 4>(g, x, K, n_tok, s, src, st);
+  return launch_rt<F, NT, 4, 4>(g, x, K, n_tok, s, src, st);
 }
 
 }  // namespace
