@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "kq_decode.cuh"
 #include "kq_kernels.cuh"
@@ -269,38 +270,35 @@ __device__ __forceinline__ Tile tile_of(const Params& p, int t) {
 // byte b (= position % 4) of a word, in the low (lo) or high half of a Q4
 // family chunk.  Q4_K / G128 low nibbles come from w (b0 s=0, b1 s=8, b2
 // s=16) and w >> 12 (b3 s=12); high nibbles from w (b0 s=4, b1 s=12) and
-// w >> 12 (b2 s=8, b3 s=16).  Q5_K extracts 5-bit fields from two words
-// whose byte b holds the low (lo5) or high (hi5) nibble with its fifth bit:
-// b0..b2 at s = 0, 8, 16 of each, and b3 from one byte-permuted word that
-// holds lo5's b3 at s=0 and hi5's b3 at s=16.  Q6_K extracts whole bytes (b3
-// from w >> 8).  x is staged pre-scaled by 2^-s, so (2^23 + q 2^s) - 2^23 =
-// q 2^s times the staged x is exactly q x.
+// w >> 12 (b2 s=8, b3 s=16).  Q5_K and Q6_K extract 5- or 6-bit fields from
+// two assembled words (Q5_K: low / high nibble with its fifth bit; Q6_K:
+// the t0 / t2 or t1 / t3 values of a byte column): b0..b2 at s = 0, 8, 16 of
+// each, b3 from one byte-permuted word that holds the first word's b3 at
+// s=0 and the second's at s=16 ("lo" = the first word).  x is staged
+// pre-scaled by 2^-s, so (2^23 + q 2^s) - 2^23 = q 2^s times the staged x is
+// exactly q x.
 template <int F>
 __host__ __device__ constexpr int field_shift(bool lo, int b) {
-  if (F == kQ6K) return b == 0 ? 0 : b == 1 ? 8 : 16;
-  if (F == kQ5K) return b == 0 ? 0 : b == 1 ? 8 : b == 2 ? 16 : (lo ? 0 : 16);
+  if (F == kQ5K || F == kQ6K) return b == 0 ? 0 : b == 1 ? 8 : b == 2 ? 16 : (lo ? 0 : 16);
   if (lo) return b == 0 ? 0 : b == 1 ? 8 : b == 2 ? 16 : 12;
   return b == 0 ? 4 : b == 1 ? 12 : b == 2 ? 8 : 16;
 }
 
 // Shared-memory layout of the staged activations.  Slot i (= token * kpad +
 // staged index) sits at byte i * kE + kPad * (i / kPer): the padding
-// staggers the 16 units of a half-warp over all bank groups, so every x load
-// of the consumers is conflict-free (Q4 family: 16 B per 64 slots, Q6_K: 16 B
-// per 128 slots; half of that for bf16).
+// staggers the 16 units of a half-warp over all bank groups (each unit's x
+// is a contiguous run of staged slots), so every x load of the consumers is
+// conflict-free (16 B per 64 slots; 8 B for bf16).
 //   Q4 family: within each aligned block of 64 positions, position
 //     32h + 4i + b (h < 2, i < 8, b < 4) has staged index 8i + 2b + h, so the
 //     two positions one byte of a chunk multiplies (its low nibble: h = 0,
 //     its high nibble: h = 1) form one fp32 pair for the packed fmas.
-//   Q6_K with kInterleave: each aligned group of 8 positions is stored as
-//     x0 x4 x1 x5 x2 x6 x3 x7 (pairs for two words taken together);
-//     otherwise in order.
+//   Q6_K: see stage_x_q6.
 template <int F, int NT, bool XBF>
 struct XLayout {
   static constexpr int kE = XBF ? 2 : 4;
-  static constexpr int kPer = (F == kQ6K) ? 128 : 64;
+  static constexpr int kPer = 64;
   static constexpr int kPad = XBF ? 8 : 16;
-  static constexpr bool kInterleave = (F == kQ6K) ? (NT <= 2) : true;
   __host__ __device__ static constexpr size_t bytes(size_t n) { return n * kE + kPad * (n / kPer); }
   __device__ static uint32_t addr(int i) {
     return static_cast<uint32_t>(i * kE + kPad * (i / kPer));
@@ -383,68 +381,83 @@ __device__ void stage_x_q4(const Params& p, uint8_t* smem, int kbase) {
   }
 }
 
+// Q6_K: within each aligned block of 128 positions (one half h of a
+// super-block), position 32t + 4j + b (t, b < 4, j < 8) has staged index
+// 16j + 4b + (0, 2, 1, 3)[t]: the four positions one byte column of the unit
+// multiplies sit together as the pairs (t0, t2), (t1, t3) -- t0 and t2 come
+// from the low and high nibble of one ql byte, t1 and t3 from another.  Part
+// sums: over positions 32t + [q kPart, (q+1) kPart) at index 4q + (0, 2, 1,
+// 3)[t] of the block, so one unit's four sums load as one float4.
 template <int F, int NT, bool XBF>
 __device__ void stage_x_q6(const Params& p, uint8_t* smem, int kbase) {
   using G = Geo<F, NT, 1, 1>;
   using L = XLayout<F, NT, XBF>;
-  constexpr int P = G::kPart;                 // positions per part sum (>= 4)
-  constexpr int CH = P > 8 ? P : 8;           // positions per work item
-  constexpr int NS = CH / P;                  // part sums per work item
+  constexpr int P = G::kPart;        // 16, 8, 4 positions per part sum
+  constexpr int GP = P / 4;          // 4-position groups per part: 4, 2, 1
+  const int groups_per_tok = p.kpad / 16;   // one group = 4 positions of each t-run
+  const int total = NT * groups_per_tok;
   const int parts_per_tok = p.kpad / P;
-  const int items_per_tok = p.kpad / CH;
   float* sx = reinterpret_cast<float*>(smem + L::bytes(static_cast<size_t>(NT) * p.kpad));
-  for (int q = threadIdx.x; q < NT * items_per_tok; q += blockDim.x) {
-    const int tk = q / items_per_tok, k0 = (q % items_per_tok) * CH;
-    const uint16_t* xt = p.x + static_cast<int64_t>(tk) * p.K + kbase + k0;
-    const bool live = tk < p.nt && kbase + k0 < p.K;
-    float sums[NS];
+  const int lane = threadIdx.x & 31;
+  // trip count uniform per warp (part sums are reduced with shuffles over GP
+  // consecutive lanes; total and groups_per_tok are multiples of 8)
+  for (int base = static_cast<int>(threadIdx.x) & ~31; base < total; base += blockDim.x) {
+    const int q = base + lane;
+    const bool in = q < total;
+    const int tk = q / groups_per_tok, gi = q % groups_per_tok;
+    const int blk = gi >> 3, j = gi & 7;
+    const int k = blk * 128 + 4 * j;   // positions k + 32t .. k + 32t + 3
+    const bool live = in && tk < p.nt && kbase + k < p.K;
+    uint2 r[4] = {};
+    if (live) {
+      const uint16_t* xt = p.x + static_cast<int64_t>(tk) * p.K + kbase + k;
 #pragma unroll
-    for (int n = 0; n < NS; ++n) sums[n] = 0.0f;
+      for (int t = 0; t < 4; ++t) r[t] = *reinterpret_cast<const uint2*>(xt + 32 * t);
+    }
+    float v[4][4];   // [t][b]
+    float sum[4];
 #pragma unroll
-    for (int i = 0; i < CH; i += 8) {
-      uint4 raw = make_uint4(0, 0, 0, 0);
-      if (live) raw = *reinterpret_cast<const uint4*>(xt + i);
-      uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
-      float v[8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        v[2 * j] = __uint_as_float(r[j] << 16);
-        v[2 * j + 1] = __uint_as_float(r[j] & 0xFFFF0000u);
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) sums[(i + j) / P] += v[j];
-      // pre-scale by 2^-s, s = bit position at which the consumers extract
-      // the q of this x (exact: a power of two)
-      const bool lo = ((k0 + i) & 63) < 32;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] *= pow2(-field_shift<F>(lo, j & 3));
-      const int idx = tk * p.kpad + k0 + i;   // first of an aligned group of 8
-      uint8_t* d = smem + L::addr(idx);
-      if constexpr (XBF) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          r[j] = (__float_as_uint(v[2 * j]) >> 16) | (__float_as_uint(v[2 * j + 1]) & 0xFFFF0000u);
-        uint4 o = make_uint4(r[0], r[1], r[2], r[3]);
-        if (L::kInterleave)   // bf16 pairs (x0,x4) (x1,x5) (x2,x6) (x3,x7)
-          o = make_uint4(__byte_perm(r[0], r[2], 0x5410), __byte_perm(r[0], r[2], 0x7632),
-                         __byte_perm(r[1], r[3], 0x5410), __byte_perm(r[1], r[3], 0x7632));
-        // the bf16 layout pads by 8 bytes: a group start is 8-byte aligned
-        uint2* d2 = reinterpret_cast<uint2*>(d);
-        d2[0] = make_uint2(o.x, o.y);
-        d2[1] = make_uint2(o.z, o.w);
-      } else {
-        float4* d4 = reinterpret_cast<float4*>(d);
-        if (L::kInterleave) {
-          d4[0] = make_float4(v[0], v[4], v[1], v[5]);
-          d4[1] = make_float4(v[2], v[6], v[3], v[7]);
-        } else {
-          d4[0] = make_float4(v[0], v[1], v[2], v[3]);
-          d4[1] = make_float4(v[4], v[5], v[6], v[7]);
-        }
-      }
+    for (int t = 0; t < 4; ++t) {
+      v[t][0] = __uint_as_float(r[t].x << 16);
+      v[t][1] = __uint_as_float(r[t].x & 0xFFFF0000u);
+      v[t][2] = __uint_as_float(r[t].y << 16);
+      v[t][3] = __uint_as_float(r[t].y & 0xFFFF0000u);
+      sum[t] = (v[t][0] + v[t][1]) + (v[t][2] + v[t][3]);
     }
 #pragma unroll
-    for (int n = 0; n < NS; ++n) sx[tk * parts_per_tok + k0 / P + n] = sums[n];
+    for (int m = 1; m < GP; m <<= 1)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) sum[t] += __shfl_xor_sync(0xFFFFFFFFu, sum[t], m);
+    if (!in) continue;
+    // pre-scale: t0 / t1 fields sit at s = 0, 8, 16, 0 of their word, t2 /
+    // t3 fields at s = 0, 8, 16, 16 (byte 3 comes from a byte-permuted word)
+    float o[16];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      o[4 * b + 0] = v[0][b] * pow2(-field_shift<F>(true, b));
+      o[4 * b + 1] = v[2][b] * pow2(-field_shift<F>(false, b));
+      o[4 * b + 2] = v[1][b] * pow2(-field_shift<F>(true, b));
+      o[4 * b + 3] = v[3][b] * pow2(-field_shift<F>(false, b));
+    }
+    uint8_t* d = smem + L::addr(tk * p.kpad + blk * 128 + 16 * j);
+    if constexpr (XBF) {
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        w[i] = (__float_as_uint(o[2 * i]) >> 16) | (__float_as_uint(o[2 * i + 1]) & 0xFFFF0000u);
+      // the bf16 layout pads by 8 bytes: a group start is 8-byte aligned
+      uint2* d2 = reinterpret_cast<uint2*>(d);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d2[i] = make_uint2(w[2 * i], w[2 * i + 1]);
+    } else {
+      float4* d4 = reinterpret_cast<float4*>(d);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d4[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    }
+    if (j % GP == 0) {
+      float* sp = sx + tk * parts_per_tok + blk * (128 / P) + 4 * (j / GP);
+      *reinterpret_cast<float4*>(sp) = make_float4(sum[0], sum[2], sum[1], sum[3]);
+    }
   }
 }
 
@@ -456,17 +469,18 @@ __device__ __forceinline__ void stage_x(const Params& p, uint8_t* smem, int kbas
     stage_x_q4<F, NT, XBF>(p, smem, kbase);
 }
 
-// The four values stored at slots idx .. idx+3 (idx a multiple of 4) as two
-// float2 pairs.
+// The four values stored at the shared address addr (slots idx .. idx+3,
+// idx a multiple of 4) as two float2 pairs.  A unit's x is a run of staged
+// slots inside one 64-slot block, so the addresses of a run are its first
+// slot's address plus slot * kE.
 template <int F, int NT, bool XBF>
-__device__ __forceinline__ void x_quad(uint32_t xs, int idx, float2& a, float2& b) {
-  using L = XLayout<F, NT, XBF>;
+__device__ __forceinline__ void x_quad(uint32_t addr, float2& a, float2& b) {
   if constexpr (XBF) {
-    const uint2 r = lds64(xs + L::addr(idx));
+    const uint2 r = lds64(addr);
     a = make_float2(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xFFFF0000u));
     b = make_float2(__uint_as_float(r.y << 16), __uint_as_float(r.y & 0xFFFF0000u));
   } else {
-    const float4 v = lds_f4(xs + L::addr(idx));
+    const float4 v = lds_f4(addr);
     a = make_float2(v.x, v.y);
     b = make_float2(v.z, v.w);
   }
@@ -553,15 +567,13 @@ __device__ __forceinline__ void lds_words(uint32_t a, uint32_t (&w)[NW]) {
   }
 }
 
-__device__ __forceinline__ uint64_t u64(uint32_t lo, uint32_t hi) {
-  return (static_cast<uint64_t>(hi) << 32) | lo;
-}
-__device__ __forceinline__ uint64_t bitsel64(uint64_t a, uint64_t b, uint32_t m) {
-  return u64(bitsel(static_cast<uint32_t>(a), static_cast<uint32_t>(b), m),
-             bitsel(static_cast<uint32_t>(a >> 32), static_cast<uint32_t>(b >> 32), m));
-}
+// prmt.b32 in its default mode: selector nibble n picks byte n of the result
+// from the eight bytes of (b:a); with its bit 3 set, the picked byte's sign
+// bit fills the result byte instead.
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  return __byte_perm(a, b, sel);
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
 }
 
 // Exact (q_a 2^sa, q_b 2^sb) for the field under mask MA of a and under mask
@@ -581,12 +593,6 @@ __device__ __forceinline__ float2 cvt_pair(uint32_t a, uint32_t b, uint32_t magi
       : "r"(a), "r"(b), "n"(MA), "n"(MB), "r"(magic), "l"(neg));
   return r;
 }
-// the same field of both halves of v
-template <uint32_t M>
-__device__ __forceinline__ float2 conv64(uint64_t v, uint32_t magic, uint64_t neg) {
-  return cvt_pair<M, M>(static_cast<uint32_t>(v), static_cast<uint32_t>(v >> 32), magic, neg);
-}
-
 constexpr uint64_t kNegMagic2 = 0xCB000000CB000000ull;   // (-2^23, -2^23)
 
 // Per-lane constants of the 6-bit (sc, m) decode of Q4_K / Q5_K for the two
@@ -619,15 +625,19 @@ __device__ __forceinline__ void scale_pair6(const ScaleSel& q, uint32_t s0, uint
   mn = (a_m & 0x0F0Fu) | ((s1 >> q.shb) & 0x3030u);
 }
 
-// One stage of a Q4_K / Q5_K / Q4_G128 tile for this thread's rows.  The
-// lane's unit is bytes off .. off + kCW/2 of chunk c of super-block sbl of
-// the slab: the low nibbles belong to sub-block 2c (weights 64c + off + r),
-// the high nibbles to 2c+1 (weights 64c + 32 + off + r).  Every byte gives
-// one (low, high) pair: converted with one cvt_pair and accumulated with one
-// packed fma against the staged (x_lo, x_hi) pair, so the accumulators hold
-// (sub-block 2c, sub-block 2c+1) sums and the scales apply as pairs too:
+// One stage of a Q4_K / Q5_K / Q4_G128 tile for the NR live rows of this
+// thread.  The lane's unit is bytes off .. off + kCW/2 of chunk c of
+// super-block sbl of the slab: the low nibbles belong to sub-block 2c
+// (weights 64c + off + r), the high nibbles to 2c+1 (weights 64c + 32 + off +
+// r).  Every byte gives one (low, high) pair: converted with one cvt_pair and
+// accumulated with one packed fma against the staged (x_lo, x_hi) pair, so
+// the accumulators hold (sub-block 2c, sub-block 2c+1) sums and the scales
+// apply as pairs too:
 //   acc += (d sc_lo, d sc_hi) * S + (-dmin m_lo, -dmin m_hi) * (sx_lo, sx_hi)
 // acc[r][k] is a pair whose two halves are added at the end of the tile.
+// Word-outer order: the x pairs of one word are loaded once and used for
+// every row, so only one word's x is live at a time; the scales are decoded
+// after the products.
 template <int F, int NT, int RT, int WC, int NR, bool XBF>
 __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl, int xsl,
                                          uint32_t st, uint32_t xs, int hw, int sbl, int c,
@@ -635,27 +645,16 @@ __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl
   using G = Geo<F, NT, RT, WC>;
   using L = XLayout<F, NT, XBF>;
   constexpr int kCW = G::kCW, NW = kCW / 8;
+  constexpr int CH = NT == 1 ? 2 : 1;   // accumulator chains per (row, token)
   const uint32_t magic = kMagic;
   const uint64_t neg = kNegMagic2;
-  // x pairs of the unit: xp[k][i][b] = (x_lo, x_hi) of byte b of word i
-  float2 xp[NT][NW][4];
-  float2 sxp[NT];
   const int kb = xsl * G::kSlabK + sbl * 256 + 64 * c;   // the chunk's 64-block
-  const uint32_t sxa = xs + static_cast<uint32_t>(L::bytes(static_cast<size_t>(NT) * p.kpad));
-  const int parts = p.kpad / G::kPart;
-#pragma unroll
-  for (int k = 0; k < NT; ++k) {
-#pragma unroll
-    for (int i = 0; i < NW; ++i) {
-      const int g = k * p.kpad + kb + 2 * off + 8 * i;
-      x_quad<F, NT, XBF>(xs, g, xp[k][i][0], xp[k][i][1]);
-      x_quad<F, NT, XBF>(xs, g + 4, xp[k][i][2], xp[k][i][3]);
-    }
-    sxp[k] = lds_f2(sxa + 4 * (k * parts + (kb / 64) * (64 / G::kPart) + 2 * (off / G::kPart)));
-  }
-  // the rows' weight words and scale pairs
+  // first staged slot of the unit's x run (token 0), and the token stride
+  const uint32_t xrun = xs + L::addr(kb + 2 * off);
+  const uint32_t xtok = static_cast<uint32_t>(L::bytes(static_cast<size_t>(p.kpad)));
+  // the rows' weight words
   uint32_t w[NR][NW], hq[NR][NW];
-  float2 dsc[NR], ndm[NR];
+  uint32_t rec[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
     const int row = hw + 2 * WC * r;
@@ -663,40 +662,32 @@ __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl
 #pragma unroll
     for (int j = 0; j < NW; ++j) hq[r][j] = 0;
     if constexpr (F == kG128) {
+      rec[r] = rs;
       lds_words<NW>(rs + 128 * sbl + 32 * c + off, w[r]);
-      const int64_t pstart =
-          ((tl.row0 + row) * static_cast<int64_t>(p.nsb) + sl * G::kSlabSB) * 8;
-      const uint32_t pa = st + p.pbase + row * p.pslot +
-                          static_cast<uint32_t>(pstart & 15) + 8 * sbl;
-      const uint2 pr = lds64(pa);
-      const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
-      const int g = c >> 1;
-      const float sc = static_cast<float>((pr.y >> (8 * g)) & 0xFF);
-      const float mn = static_cast<float>((pr.y >> (16 + 8 * g)) & 0xFF);
-      dsc[r] = make_float2(dd.x * sc, dd.x * sc);
-      ndm[r] = make_float2(-dd.y * mn, -dd.y * mn);
     } else {
-      const uint32_t rec = rs + G::kBB * sbl;
-      const uint4 hdr = lds128(rec);
-      lds_words<NW>(rec + (F == kQ4K ? 16 : 48) + 32 * c + off, w[r]);
-      if constexpr (F == kQ5K) lds_words<NW>(rec + 16 + off, hq[r]);
-      const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
-      uint32_t scp, mnp;
-      scale_pair6(ss, hdr.y, hdr.z, hdr.w, scp, mnp);
-      dsc[r] = make_float2(dd.x * static_cast<float>(scp & 0xFF),
-                           dd.x * static_cast<float>(scp >> 8));
-      ndm[r] = make_float2(-dd.y * static_cast<float>(mnp & 0xFF),
-                           -dd.y * static_cast<float>(mnp >> 8));
+      rec[r] = rs + G::kBB * sbl;
+      lds_words<NW>(rec[r] + (F == kQ4K ? 16 : 48) + 32 * c + off, w[r]);
+      if constexpr (F == kQ5K) lds_words<NW>(rec[r] + 16 + off, hq[r]);
     }
   }
-  float2 A[NR][NT][2];
+  float2 A[NR][NT][CH];
 #pragma unroll
   for (int r = 0; r < NR; ++r)
 #pragma unroll
-    for (int k = 0; k < NT; ++k) A[r][k][0] = A[r][k][1] = make_float2(0.0f, 0.0f);
+    for (int k = 0; k < NT; ++k)
+#pragma unroll
+      for (int h = 0; h < CH; ++h) A[r][k][h] = make_float2(0.0f, 0.0f);
   const int rlo = (2 * c + 28) & 31, rhi = (2 * c + 29) & 31;   // Q5_K: bit 2c(+1) -> bit 4
 #pragma unroll
   for (int i = 0; i < NW; ++i) {
+    // x pairs of word i: xq[k][b] = (x_lo, x_hi) of byte b
+    float2 xq[NT][4];
+#pragma unroll
+    for (int k = 0; k < NT; ++k) {
+      const uint32_t a = xrun + k * xtok + 8 * i * L::kE;
+      x_quad<F, NT, XBF>(a, xq[k][0], xq[k][1]);
+      x_quad<F, NT, XBF>(a + 4 * L::kE, xq[k][2], xq[k][3]);
+    }
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
       const uint32_t v = w[r][i];
@@ -724,146 +715,164 @@ __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl
 #pragma unroll
       for (int k = 0; k < NT; ++k)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) A[r][k][i & 1] = __ffma2_rn(q[b], xp[k][i][b], A[r][k][i & 1]);
+        for (int b = 0; b < 4; ++b)
+          A[r][k][b % CH] = __ffma2_rn(q[b], xq[k][b], A[r][k][b % CH]);
     }
   }
+  // scales, then the stage's contribution
+  const uint32_t sxa = xs + static_cast<uint32_t>(L::bytes(static_cast<size_t>(NT) * p.kpad));
+  const int parts = p.kpad / G::kPart;
+  float2 sxp[NT];
+#pragma unroll
+  for (int k = 0; k < NT; ++k)
+    sxp[k] = lds_f2(sxa + 4 * (k * parts + (kb / 64) * (64 / G::kPart) + 2 * (off / G::kPart)));
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
+    float2 dsc, ndm;
+    if constexpr (F == kG128) {
+      const int row = hw + 2 * WC * r;
+      // byte offset of the slab's params in its 16-byte aligned copy: (row
+      // start + slab start) mod 16, from the row stride mod 16
+      const uint32_t po =
+          (static_cast<uint32_t>(tl.row0 + row) * ((8u * p.nsb) & 15u) + sl * G::kPBytes) & 15u;
+      const uint32_t pa = st + p.pbase + row * p.pslot + po + 8 * sbl;
+      const uint2 pr = lds64(pa);
+      const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
+      const int g = c >> 1;
+      const float sc = static_cast<float>((pr.y >> (8 * g)) & 0xFF);
+      const float mn = static_cast<float>((pr.y >> (16 + 8 * g)) & 0xFF);
+      dsc = make_float2(dd.x * sc, dd.x * sc);
+      ndm = make_float2(-dd.y * mn, -dd.y * mn);
+    } else {
+      const uint4 hdr = lds128(rec[r]);
+      const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
+      uint32_t scp, mnp;
+      scale_pair6(ss, hdr.y, hdr.z, hdr.w, scp, mnp);
+      dsc = make_float2(dd.x * static_cast<float>(scp & 0xFF), dd.x * static_cast<float>(scp >> 8));
+      ndm = make_float2(-dd.y * static_cast<float>(mnp & 0xFF), -dd.y * static_cast<float>(mnp >> 8));
+    }
 #pragma unroll
     for (int k = 0; k < NT; ++k) {
-      const float2 S = (NW > 1) ? __fadd2_rn(A[r][k][0], A[r][k][1]) : A[r][k][0];
-      acc[r][k] = __ffma2_rn(dsc[r], S, acc[r][k]);
-      acc[r][k] = __ffma2_rn(ndm[r], sxp[k], acc[r][k]);
+      const float2 S = CH == 2 ? __fadd2_rn(A[r][k][0], A[r][k][CH - 1]) : A[r][k][0];
+      acc[r][k] = __ffma2_rn(dsc, S, acc[r][k]);
+      acc[r][k] = __ffma2_rn(ndm, sxp[k], acc[r][k]);
     }
   }
 }
 
-// One stage of a Q6_K tile.  Unit (h, u2): weights 128h + 32t + l0 + i for
-// t < 4, i < kCW/4 (l0 = u2 kCW/4); sub-block of (t, l) = 8h + 2t + l/16.
-// Records start on 2-byte boundaries: words are read aligned and shifted.
-// With at least two words per t-run the words are paired (64-bit), as in
-// stage_q4; with one word (n_tok 4) each word is used alone.
-template <int NT, int RT, int WC, bool XBF>
+// One stage of a Q6_K tile for the NR live rows of this thread.  Unit (h,
+// u2): weights 128h + 32t + l0 + l for t < 4, l < kCW/4 (l0 = u2 kCW/4), in
+// sub-block 8h + 2t + l0/16.  Byte column l of the unit: ql[64h + l0 + l]
+// holds t0 (low nibble) and t2 (high), ql[64h + 32 + l0 + l] holds t1 and t3,
+// qh[32h + l0 + l] the two high bits of each.  Each byte column gives the
+// pairs (t0, t2), (t1, t3), accumulated with packed fmas against the staged x
+// pairs; the scales apply as the pairs (d sc_t0, d sc_t2), (d sc_t1, d sc_t3)
+// and q - 32 as ds (S - 32 sx).  Records start on 2-byte boundaries: words
+// are read aligned and shifted.
+template <int NT, int RT, int WC, int NR, bool XBF>
 __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl, int xsl,
                                          uint32_t st, uint32_t xs, int hw, int sbl, int un,
                                          float2 (&acc)[RT][NT]) {
   using G = Geo<kQ6K, NT, RT, WC>;
   using L = XLayout<kQ6K, NT, XBF>;
-  constexpr int kCW = G::kCW, QW = kCW / 16;
-  constexpr bool kPaired = L::kInterleave;
-  constexpr int NX = kPaired ? QW / 2 : QW;   // x groups per t-run
+  constexpr int kCW = G::kCW, QW = kCW / 16;   // words per t-run of the unit: 4, 2, 1
+  const uint32_t magic = kMagic;
+  const uint64_t neg = kNegMagic2;
   const int h = un / (G::kUnitsPerSB / 2);
   const int u2 = un % (G::kUnitsPerSB / 2);
   const int l0 = u2 * (kCW / 4);
-  const int su = l0 >> 4;
-  // xv[t-run tt][group][b]: paired -> pairs of nibble position b (b < 4);
-  // single -> (x0,x1), (x2,x3) in [0], [1]
-  float2 xv[NT][4][NX][4];
-  float sxt[NT][4];   // sum of x over each t-run (for the -32 of q - 32)
-  const int kb = xsl * G::kSlabK + sbl * 256 + 128 * h + l0;
+  const int su = l0 >> 4;   // sub-block of the unit within each t-run
+  // xp[k][j][b][0] = (x_t0, x_t2), [1] = (x_t1, x_t3) of column 4j + b
+  float2 xp[NT][QW][4][2];
+  float2 sx02[NT], sx13[NT];
+  const int kb = xsl * G::kSlabK + sbl * 256 + 128 * h;   // the unit's 128-block
   const uint32_t sxa = xs + static_cast<uint32_t>(L::bytes(static_cast<size_t>(NT) * p.kpad));
   const int parts = p.kpad / G::kPart;
+  const uint32_t xrun = xs + L::addr(kb + 4 * l0);   // the unit's x run (token 0)
+  const uint32_t xtok = static_cast<uint32_t>(L::bytes(static_cast<size_t>(p.kpad)));
 #pragma unroll
-  for (int k = 0; k < NT; ++k)
+  for (int k = 0; k < NT; ++k) {
 #pragma unroll
-    for (int tt = 0; tt < 4; ++tt)
-      sxt[k][tt] = __uint_as_float(lds32(sxa + 4 * (k * parts + (kb + 32 * tt) / G::kPart)));
+    for (int j = 0; j < QW; ++j)
 #pragma unroll
-  for (int k = 0; k < NT; ++k)
+      for (int b = 0; b < 4; ++b)
+        x_quad<kQ6K, NT, XBF>(xrun + k * xtok + (16 * j + 4 * b) * L::kE, xp[k][j][b][0],
+                              xp[k][j][b][1]);
+    const float4 s4 =
+        lds_f4(sxa + 4 * (k * parts + (kb / 128) * (128 / G::kPart) + 4 * (l0 / G::kPart)));
+    sx02[k] = make_float2(s4.x, s4.y);
+    sx13[k] = make_float2(s4.z, s4.w);
+  }
+  const float2 m32 = make_float2(-32.0f, -32.0f);
 #pragma unroll
-    for (int tt = 0; tt < 4; ++tt)
-#pragma unroll
-      for (int j = 0; j < NX; ++j) {
-        const int g = k * p.kpad + kb + 32 * tt + (kPaired ? 8 : 4) * j;
-        x_quad<kQ6K, NT, XBF>(xs, g, xv[k][tt][j][0], xv[k][tt][j][1]);
-        if (kPaired) x_quad<kQ6K, NT, XBF>(xs, g + 4, xv[k][tt][j][2], xv[k][tt][j][3]);
-      }
-#pragma unroll
-  for (int r = 0; r < RT; ++r) {
+  for (int r = 0; r < NR; ++r) {
     const int row = hw + 2 * WC * r;
-    if (row < tl.rcnt) {
-      const int64_t start =
-          ((tl.row0 + row) * static_cast<int64_t>(p.nsb) + sl * G::kSlabSB) * 210;
-      const uint32_t rec = st + row * p.slot + static_cast<uint32_t>(start & 15) + 210 * sbl;
-      uint32_t A[QW], B[QW], H[QW], S[2], D[1];
-      lds_words_a2<QW>(rec + 64 * h + l0, A);
-      lds_words_a2<QW>(rec + 64 * h + 32 + l0, B);
-      lds_words_a2<QW>(rec + 128 + 32 * h + l0, H);
-      lds_words_a2<2>(rec + 192 + 8 * h, S);
-      lds_words_a2<1>(rec + 208, D);
-      float2 at[NT][4];
+    // byte offset of the slab in its 16-byte aligned copy: (row start + slab
+    // start) mod 16, from the row stride mod 16
+    const uint32_t ro =
+        (static_cast<uint32_t>(tl.row0 + row) * ((210u * p.nsb) & 15u) + sl * G::kQBytes) & 15u;
+    const uint32_t rec = st + row * p.slot + ro + 210 * sbl;
+    uint32_t A[QW], B[QW], H[QW], S[2], D[1];
+    lds_words_a2<QW>(rec + 64 * h + l0, A);
+    lds_words_a2<QW>(rec + 64 * h + 32 + l0, B);
+    lds_words_a2<QW>(rec + 128 + 32 * h + l0, H);
+    lds_words_a2<2>(rec + 192 + 8 * h, S);
+    lds_words_a2<1>(rec + 208, D);
+    // scales of the unit's sub-blocks: t0 byte su, t1 su+2 (of S[0]), t2 su,
+    // t3 su+2 (of S[1]); sign-extended with a byte permute
+    const uint32_t sel0 = su | ((8 | su) << 4) | ((8 | su) << 8) | ((8 | su) << 12);
+    const uint32_t sel2 = (su + 2) | ((10 + su) << 4) | ((10 + su) << 8) | ((10 + su) << 12);
+    const float d = half_bits_to_float(D[0] & 0xFFFFu);
+    const float2 ds02 = make_float2(d * static_cast<float>(static_cast<int>(prmt(S[0], 0, sel0))),
+                                    d * static_cast<float>(static_cast<int>(prmt(S[1], 0, sel0))));
+    const float2 ds13 = make_float2(d * static_cast<float>(static_cast<int>(prmt(S[0], 0, sel2))),
+                                    d * static_cast<float>(static_cast<int>(prmt(S[1], 0, sel2))));
+    float2 a02[NT][2], a13[NT][2];
+#pragma unroll
+    for (int k = 0; k < NT; ++k) a02[k][0] = a02[k][1] = a13[k][0] = a13[k][1] = make_float2(0.0f, 0.0f);
+    const uint32_t M = 0x0F0F0F0Fu;
+#pragma unroll
+    for (int j = 0; j < QW; ++j) {
+      // 6-bit values of the four t-runs, one per byte (bits 6-7 are masked
+      // off by the extraction masks)
+      const uint32_t q0 = bitsel(A[j], H[j] << 4, M);
+      const uint32_t q2 = bitsel(A[j] >> 4, H[j], M);
+      const uint32_t q1 = bitsel(B[j], H[j] << 2, M);
+      const uint32_t q3 = bitsel(B[j] >> 4, H[j] >> 2, M);
+      const uint32_t p02 = prmt(q0, q2, 0x0703u);   // byte 3 of q0 -> byte 0, of q2 -> byte 2
+      const uint32_t p13 = prmt(q1, q3, 0x0703u);
+      float2 c02[4], c13[4];
+      c02[0] = cvt_pair<0x3Fu, 0x3Fu>(q0, q2, magic, neg);
+      c02[1] = cvt_pair<0x3F00u, 0x3F00u>(q0, q2, magic, neg);
+      c02[2] = cvt_pair<0x3F0000u, 0x3F0000u>(q0, q2, magic, neg);
+      c02[3] = cvt_pair<0x3Fu, 0x3F0000u>(p02, p02, magic, neg);
+      c13[0] = cvt_pair<0x3Fu, 0x3Fu>(q1, q3, magic, neg);
+      c13[1] = cvt_pair<0x3F00u, 0x3F00u>(q1, q3, magic, neg);
+      c13[2] = cvt_pair<0x3F0000u, 0x3F0000u>(q1, q3, magic, neg);
+      c13[3] = cvt_pair<0x3Fu, 0x3F0000u>(p13, p13, magic, neg);
 #pragma unroll
       for (int k = 0; k < NT; ++k)
 #pragma unroll
-        for (int tt = 0; tt < 4; ++tt) at[k][tt] = make_float2(0.0f, 0.0f);
-      if constexpr (kPaired) {
-        const uint32_t M = 0x0F0F0F0Fu;
-#pragma unroll
-        for (int j = 0; j < NX; ++j) {
-          const uint64_t A64 = u64(A[2 * j], A[2 * j + 1]), B64 = u64(B[2 * j], B[2 * j + 1]);
-          const uint64_t H64 = u64(H[2 * j], H[2 * j + 1]);
-          // 6-bit q per byte (bits that cross the 32-bit halves in the
-          // 64-bit shifts land in bits the masks discard)
-          uint64_t q6[4];
-          q6[0] = bitsel64(A64, H64 << 4, M);
-          q6[1] = bitsel64(B64, H64 << 2, M);
-          q6[2] = bitsel64(A64 >> 4, H64, M);
-          q6[3] = bitsel64(B64 >> 4, H64 >> 2, M);
-#pragma unroll
-          for (int tt = 0; tt < 4; ++tt) {
-            const uint64_t v = q6[tt], vs = v >> 8;
-            float2 q[4];
-            q[0] = conv64<0x3Fu>(v, kMagic, kNegMagic2);
-            q[1] = conv64<0x3F00u>(v, kMagic, kNegMagic2);
-            q[2] = conv64<0x3F0000u>(v, kMagic, kNegMagic2);
-            q[3] = conv64<0x3F0000u>(vs, kMagic, kNegMagic2);
-#pragma unroll
-            for (int k = 0; k < NT; ++k)
-#pragma unroll
-              for (int b = 0; b < 4; ++b) at[k][tt] = __ffma2_rn(q[b], xv[k][tt][j][b], at[k][tt]);
-          }
+        for (int b = 0; b < 4; ++b) {
+          a02[k][b & 1] = __ffma2_rn(c02[b], xp[k][j][b][0], a02[k][b & 1]);
+          a13[k][b & 1] = __ffma2_rn(c13[b], xp[k][j][b][1], a13[k][b & 1]);
         }
-      } else {
-        const float2 nm = make_float2(-8388608.0f, -8388608.0f);
+    }
 #pragma unroll
-        for (int j = 0; j < QW; ++j) {
-          uint32_t q6[4];
-          q6[0] = bitsel(A[j], H[j] << 4, 0x0F0F0F0Fu);
-          q6[1] = bitsel(B[j], H[j] << 2, 0x0F0F0F0Fu);
-          q6[2] = bitsel(A[j] >> 4, H[j], 0x0F0F0F0Fu);
-          q6[3] = bitsel(B[j] >> 4, H[j] >> 2, 0x0F0F0F0Fu);
-#pragma unroll
-          for (int tt = 0; tt < 4; ++tt) {
-            const uint32_t v = q6[tt], vs = v >> 8;
-            const float2 q0 = __fadd2_rn(f2(lop_mask_or(v, 0x3Fu, kMagic), lop_mask_or(v, 0x3F00u, kMagic)), nm);
-            const float2 q1 = __fadd2_rn(f2(lop_mask_or(v, 0x3F0000u, kMagic), lop_mask_or(vs, 0x3F0000u, kMagic)), nm);
-#pragma unroll
-            for (int k = 0; k < NT; ++k) {
-              at[k][tt] = __ffma2_rn(q0, xv[k][tt][j][0], at[k][tt]);
-              at[k][tt] = __ffma2_rn(q1, xv[k][tt][j][1], at[k][tt]);
-            }
-          }
-        }
-      }
-      const float d = half_bits_to_float(D[0] & 0xFFFFu);
-#pragma unroll
-      for (int tt = 0; tt < 4; ++tt) {
-        const int bi = su + 2 * tt;   // byte of the 8 scales of half h
-        const int8_t sc = static_cast<int8_t>((S[bi >> 2] >> (8 * (bi & 3))) & 0xFF);
-        const float ds = d * static_cast<float>(sc);
-#pragma unroll
-        for (int k = 0; k < NT; ++k)
-          acc[r][k].x = fmaf(ds, fmaf(-32.0f, sxt[k][tt], at[k][tt].x + at[k][tt].y), acc[r][k].x);
-      }
+    for (int k = 0; k < NT; ++k) {
+      const float2 s02 = __ffma2_rn(m32, sx02[k], __fadd2_rn(a02[k][0], a02[k][1]));
+      const float2 s13 = __ffma2_rn(m32, sx13[k], __fadd2_rn(a13[k][0], a13[k][1]));
+      acc[r][k] = __ffma2_rn(ds02, s02, acc[r][k]);
+      acc[r][k] = __ffma2_rn(ds13, s13, acc[r][k]);
     }
   }
 }
 
 constexpr int kMaxStages = 8;
 
-// Registers capped so that three CTAs fit an SM.
+// Registers capped so that three CTAs (two with eight consumer warps) fit an SM.
 template <int F, int NT, int RT, int WC, bool XBF>
-__global__ void __launch_bounds__((WC + 1) * 32, 3)
+__global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
     gemv_stream(const __grid_constant__ Params p, int stages) {
   using G = Geo<F, NT, RT, WC>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -948,22 +957,24 @@ __global__ void __launch_bounds__((WC + 1) * 32, 3)
     if (!mbar_wait_warp(bar_full + 8 * slot, use & 1)) return;
     const uint32_t st = ring_a + slot * p.stage;
     if (sl * G::kSlabSB + sbl < p.nsb) {
-      if constexpr (F == kQ6K) {
-        stage_q6<NT, RT, WC, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, un, acc);
-      } else {
-        // rows of this half-warp inside the tile (the same for all its lanes)
-        const int nr = tl.rcnt > hw ? min(RT, (tl.rcnt - hw + 2 * WC - 1) / (2 * WC)) : 0;
-        if (nr == RT) {
-          stage_q4<F, NT, RT, WC, RT, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, c, off, ss, acc);
-        } else if constexpr (RT >= 2) {
-          if (nr == 1)
-            stage_q4<F, NT, RT, WC, 1, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, c, off, ss, acc);
-          if constexpr (RT == 4) {
-            if (nr == 2)
-              stage_q4<F, NT, RT, WC, 2, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, c, off, ss, acc);
-            else if (nr == 3)
-              stage_q4<F, NT, RT, WC, 3, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, c, off, ss, acc);
-          }
+      // rows of this half-warp inside the tile (the same for all its lanes)
+      const int nr = tl.rcnt > hw ? min(RT, (tl.rcnt - hw + 2 * WC - 1) / (2 * WC)) : 0;
+      auto run = [&](auto nrc) {
+        constexpr int NR = decltype(nrc)::value;
+        if constexpr (F == kQ6K)
+          stage_q6<NT, RT, WC, NR, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, un, acc);
+        else
+          stage_q4<F, NT, RT, WC, NR, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, c, off, ss, acc);
+      };
+      if (nr == RT) {
+        run(std::integral_constant<int, RT>{});
+      } else if constexpr (RT >= 2) {
+        if (nr == 1) run(std::integral_constant<int, 1>{});
+        if constexpr (RT == 4) {
+          if (nr == 2)
+            run(std::integral_constant<int, 2>{});
+          else if (nr == 3)
+            run(std::integral_constant<int, 3>{});
         }
       }
     }
@@ -1263,6 +1274,9 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   const int64_t k = (rows + static_cast<int64_t>(cps) * G::kRows - 1) /
                     (static_cast<int64_t>(cps) * G::kRows);
   int tr = static_cast<int>((rows + cps * k - 1) / (cps * k));
+  // even, so that both half-warps of a warp have the same number of rows in
+  // every full tile (no divergence between their row loops)
+  tr += tr & 1;
   if (tr > G::kRows) tr = G::kRows;
   if (tr < 1) tr = 1;
   p.tile_rows = tr;
@@ -1365,12 +1379,19 @@ template <int F, int NT>
 bool launch_nt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
                ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
   const DevInfo& di = dev_info();
-  // 4 consumer warps; rows per thread: 4, or 2 for small matrices (fewer
-  // than 16 rows per SM).
+  // Rows per thread: 4, or 2 for small matrices (fewer than 16 rows per SM)
+  // and at n_tok 4 (whose x values take twice the registers).  Consumer warps
+  // per CTA: 8 for the Q4 family at n_tok 1, 2 on large matrices (two CTAs
+  // per SM: more warps to hide latency), else 4 (three CTAs per SM).
   int64_t rows = 0;
   for (int i = 0; i < g.count; ++i) rows += g.N[i];
-  if (rows < 16LL * di.sms) return launch_rt<F, NT, 2, 4>(g, x, K, n_tok, s, src, st);
-  return launch_rt<F, NT, 4, 4>(g, x, K, n_tok, s, src, st);
+  if (NT == 4 || rows < 16LL * di.sms) return launch_rt<F, NT, 2, 4>(g, x, K, n_tok, s, src, st);
+  if constexpr (NT == 4)
+    return false;
+  else if constexpr (F == kQ6K)
+    return launch_rt<F, NT, 4, 4>(g, x, K, n_tok, s, src, st);
+  else
+    return launch_rt<F, NT, 4, 8>(g, x, K, n_tok, s, src, st);
 }
 
 }  // namespace
