@@ -89,6 +89,15 @@ def barrier(dist):
         dist.barrier()
 
 
+def replica_throughput(dist, bytes_this_rank: float, seconds_this_rank: float):
+    """Whole-job throughput of independent replicas: the bytes every rank
+    streamed divided by the slowest rank's time.  Returns (GB/s, slowest
+    seconds, total bytes)."""
+    t_max = max_over_ranks(dist, seconds_this_rank)
+    total = sum_over_ranks(dist, float(bytes_this_rank))
+    return total / t_max / 1e9, t_max, total
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -370,9 +379,7 @@ def run_kq(args):
 
     with ClockSampler(local) as clk:
         t_step = time_graph(g, stream, args.steps, max(3, args.warmup), dist)
-    t_max = max_over_ranks(dist, t_step)
-    total_bytes = sum_over_ranks(dist, float(wbytes))
-    value = total_bytes / t_max / 1e9
+    value, t_max, total_bytes = replica_throughput(dist, wbytes, t_step)
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
 
