@@ -240,13 +240,13 @@ void launch_f(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStrea
 
 bool launch_gemv(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
                  cudaStream_t s) {
-  // the streaming kernel serves n_tok <= 4 while x fits in shared memory;
-  // more tokens run as consecutive launches of up to 4 tokens each (x and y
-  // rows of a token are contiguous, so a chunk is an offset view); anything
-  // it cannot serve takes the warp-per-row kernel below
-  if (n_tok <= 4) {
-    if (launch_stream(fmt, g, x, K, n_tok, s)) return true;
-  } else {
+  // the streaming kernels serve n_tok <= 4 (CUDA cores, while x fits in
+  // shared memory) and 5..16 (tensor cores).  If the tensor-core kernel does
+  // not serve a request, its tokens run as consecutive CUDA-core launches of
+  // up to 4 tokens each (x and y rows of a token are contiguous, so a chunk
+  // is an offset view); anything else takes the warp-per-row kernel below
+  if (launch_stream(fmt, g, x, K, n_tok, s)) return true;
+  if (n_tok > 4) {
     bool ok = true;
     for (int t0 = 0; t0 < n_tok && ok; t0 += 4) {
       const int nt = n_tok - t0 < 4 ? n_tok - t0 : 4;

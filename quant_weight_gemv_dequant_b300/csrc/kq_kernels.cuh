@@ -22,14 +22,15 @@ struct GemvGroup {
 bool launch_gemv(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
                  cudaStream_t stream);
 
-// The streaming kernel (n_tok <= 4); false if it does not serve the request.
+// The streaming kernels: n_tok <= 4 on the CUDA cores, 5..16 on the tensor
+// cores; false if they do not serve the request.
 bool launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
                    cudaStream_t stream);
 
-// kq_gemv_noalloc: the streaming kernel with its split-K scratch in a fixed
-// device array (no allocation).  kNotServed: this request needs no scratch
-// kernel of this family (n_tok > 4, or no configuration fits); the caller
-// may use a kernel that needs no scratch.
+// kq_gemv_noalloc: the streaming kernels with their split-K scratch in a
+// fixed device array (no allocation).  kNotServed: no configuration of these
+// kernels serves the request; the caller may use a kernel that needs no
+// scratch.
 enum class NoAllocResult { kLaunched, kNotServed, kTooLarge, kFailed };
 NoAllocResult launch_stream_noalloc(int fmt, const GemvGroup& g, const uint16_t* x, int K,
                                     int n_tok, cudaStream_t stream);

@@ -1,5 +1,6 @@
-// kq_stream.cu -- the streaming K-quant GEMV kernel for sm_103a
-// (n_tok = 1, 2, 4 on CUDA cores).
+// kq_stream.cu -- the streaming K-quant GEMV kernels for sm_103a: n_tok 1..4
+// on the CUDA cores (gemv_stream), n_tok 5..16 on the tensor cores
+// (gemv_mma, the speculative-verify widths).
 //
 // y[t][n] = sum_k w^[n][k] x[t][k]  (daily.dev ExecuTorch summary, answer on
 // exporting GGUF checkpoints; the Core AI card's 424 GB/s arithmetic shows the
@@ -126,6 +127,11 @@ __device__ __forceinline__ float4 lds_f4(uint32_t a) {
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "r"(a));
   return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, float4 v) {
+  asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(a), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
 }
 __device__ __forceinline__ float2 lds_f2(uint32_t a) {
   float2 v;
@@ -520,8 +526,8 @@ __device__ __forceinline__ void issue_stage(const Params& p, uint8_t* smem, uint
   const int sb0 = sl * G::kSlabSB;
   const int nsb_here = min(G::kSlabSB, p.nsb - sb0);
   uint32_t tx = 0;
-  if (lane < tl.rcnt) {   // lane r copies row r of the tile
-    const int64_t idx = (tl.row0 + lane) * static_cast<int64_t>(p.nsb) + sb0;
+  for (int r = lane; r < tl.rcnt; r += 32) {   // lane l copies rows l, l + 32, ...
+    const int64_t idx = (tl.row0 + r) * static_cast<int64_t>(p.nsb) + sb0;
     auto copy_span = [&](const uint8_t* plane, int64_t plane_bytes, int64_t off, int len,
                          uint32_t dst) {
       const int64_t lo_off = off & ~int64_t{15};
@@ -540,11 +546,10 @@ __device__ __forceinline__ void issue_stage(const Params& p, uint8_t* smem, uint
     };
     if constexpr (F == kG128) {
       const int64_t total = N * p.nsb;
-      copy_span(W, total * 128, idx * 128, nsb_here * 128, st_a + lane * p.slot);
-      copy_span(W + total * 128, total * 8, idx * 8, nsb_here * 8,
-                st_a + p.pbase + lane * p.pslot);
+      copy_span(W, total * 128, idx * 128, nsb_here * 128, st_a + r * p.slot);
+      copy_span(W + total * 128, total * 8, idx * 8, nsb_here * 8, st_a + p.pbase + r * p.pslot);
     } else {
-      copy_span(W, N * p.nsb * G::kBB, idx * G::kBB, nsb_here * G::kBB, st_a + lane * p.slot);
+      copy_span(W, N * p.nsb * G::kBB, idx * G::kBB, nsb_here * G::kBB, st_a + r * p.slot);
     }
   }
   mbar_arrive_tx(full, tx);   // every producer lane arrives (count 32)
@@ -1051,6 +1056,452 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
   }
 }
 
+// ============================================================ verify kernel
+//
+// n_tok 5..16 (speculative verify): the products run on the tensor cores as
+// mma.sync m16n8k16 (bf16 operands, fp32 accumulators).  A = weights: a warp
+// owns 16 rows of a tile; each qs byte's nibble becomes one bf16 value
+// 128 + q (one LOP3 builds two: (w & 0x000F000F) | 0x43004300), exact.  B = x,
+// eight tokens per mma (two mmas per A fragment for 9..16 tokens), loaded as
+// bf16 straight from global memory (small, shared by every CTA: L1/L2
+// resident).  Per sub-block the accumulator holds D = 128 Sx + sum q x, and a
+// second mma against an all-ones A gives Sx, so
+//   y += s1 D + s2 Sx,  s1 = d sc,  s2 = -(128 s1 + dmin m)       (Q4 family)
+//   y += s1 (D - 160 Sx), s1 = d sc                               (Q6_K: q - 32)
+// s1, s2 per (row, sub-block) are decoded once per stage into a per-warp
+// shared table.  The weight ring, tiling, split-K and bounded waits are those
+// of gemv_stream.
+
+template <int F, int WC_>
+struct MGeo {
+  static constexpr int kF = F;
+  static constexpr int kWC = WC_;
+  static constexpr int kThreads = (WC_ + 1) * 32;
+  static constexpr int kRows = 16 * WC_;     // a warp owns 16 rows of a tile
+  static constexpr int kSlabSB = 2;
+  static constexpr int kSlabK = 512;
+  static constexpr int kBB = block_bytes(F);
+  static constexpr int kQBytes = (F == kG128) ? 128 * kSlabSB : kBB * kSlabSB;
+  static constexpr int kPBytes = (F == kG128) ? 8 * kSlabSB : 0;
+  static constexpr int round16(int b) { return (b + 15) / 16 * 16; }
+  static constexpr int kSlotTma = round16(kQBytes + (kQBytes % 16 ? 15 : 0));
+  static constexpr int kPSlotTma = (F == kG128) ? round16(kPBytes + (kPBytes % 16 ? 15 : 0)) : 0;
+  static constexpr int kSlotBulk = round16(kQBytes + 16);
+  static constexpr int kPSlotBulk = (F == kG128) ? round16(kPBytes + 16) : 0;
+  // per-warp scale table, one row of float4 per weight row (+1 float4 of
+  // padding against bank conflicts):
+  //   Q4 family: (row, s, c) -> (s1, s1, s2, s2) of sub-block 2c, then of 2c+1
+  //   Q6_K:      (row, s, j) -> (s1, s1) of sub-block j (two per float4)
+  static constexpr int kTabRow = (F == kQ6K) ? kSlabSB * 8 + 1 : kSlabSB * 8 + 1;
+  static constexpr int kTabBytes = 16 * kTabRow * 16;
+};
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// (w & mask) | magic as one LOP3 (mask an immediate)
+template <uint32_t M>
+__device__ __forceinline__ uint32_t lop_or(uint32_t w, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(w), "n"(M), "r"(magic));
+  return d;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+constexpr uint32_t kBf16Magic2 = 0x43004300u;   // bf16 (128, 128)
+
+// prmt selector: byte b of the source, sign-extended to 32 bits
+__device__ __forceinline__ uint32_t sext_sel(uint32_t b) { return b | ((8u | b) * 0x1110u); }
+constexpr uint32_t kBf16One2 = 0x3F803F80u;     // bf16 (1, 1)
+
+// bf16 pairs (128 + q) of the fields under mask M in bytes (0, 1) and in
+// bytes (2, 3) of v: the two bytes of a pair are moved to the two halves
+// with a byte permute, so a pair is two consecutive positions.
+template <uint32_t M>
+__device__ __forceinline__ void bf16_pairs(uint32_t v, uint32_t& p01, uint32_t& p23) {
+  p01 = lop_or<M>(prmt(v, 0, 0x4140u), kBf16Magic2);
+  p23 = lop_or<M>(prmt(v, 0, 0x4342u), kBf16Magic2);
+}
+
+// The per-warp scale table of one stage: lane -> (row = lane & 15, super-block
+// s = lane >> 4) of the warp's 16 rows.
+template <class G>
+__device__ __forceinline__ void build_scale_table(const Params& p, const Tile& tl, int sl,
+                                                  uint32_t st, int rbase, uint32_t tab) {
+  constexpr int F = G::kF;
+  const int lane = threadIdx.x & 31;
+  const int row = rbase + (lane & 15), s = lane >> 4;
+  const uint32_t trow = tab + static_cast<uint32_t>((lane & 15) * G::kTabRow * 16);
+  if constexpr (F == kQ6K) {
+    const uint32_t ro =
+        (static_cast<uint32_t>(tl.row0 + row) * ((210u * p.nsb) & 15u) + sl * G::kQBytes) & 15u;
+    const uint32_t rec = st + row * p.slot + ro + 210 * s;
+    uint32_t S[4], D[1];
+    lds_words_a2<4>(rec + 192, S);
+    lds_words_a2<1>(rec + 208, D);
+    const float d = half_bits_to_float(D[0] & 0xFFFFu);
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      const uint32_t w = S[j >> 2];
+      const uint32_t sh = 8 * (j & 3);
+      const float a = d * static_cast<float>(static_cast<int>(prmt(w, 0, sext_sel(sh / 8))));
+      const float b = d * static_cast<float>(static_cast<int>(prmt(w, 0, sext_sel(sh / 8 + 1))));
+      sts128(trow + (s * 8 + j / 2) * 16, make_float4(a, a, b, b));
+    }
+  } else if constexpr (F == kG128) {
+    const uint32_t po =
+        (static_cast<uint32_t>(tl.row0 + row) * ((8u * p.nsb) & 15u) + sl * G::kPBytes) & 15u;
+    const uint2 pr = lds64(st + p.pbase + row * p.pslot + po + 8 * s);
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      const float s1 = dd.x * static_cast<float>((pr.y >> (8 * g)) & 0xFF);
+      const float s2 = -(128.0f * s1 + dd.y * static_cast<float>((pr.y >> (16 + 8 * g)) & 0xFF));
+      const float4 e = make_float4(s1, s1, s2, s2);
+#pragma unroll
+      for (int c = 2 * g; c < 2 * g + 2; ++c) {
+        sts128(trow + ((s * 4 + c) * 2) * 16, e);
+        sts128(trow + ((s * 4 + c) * 2 + 1) * 16, e);
+      }
+    }
+  } else {
+    const uint4 hdr = lds128(st + row * p.slot + G::kBB * s);
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t scp, mnp;
+      scale_pair6(scale_sel(c), hdr.y, hdr.z, hdr.w, scp, mnp);
+      const float s1l = dd.x * static_cast<float>(scp & 0xFF);
+      const float s1h = dd.x * static_cast<float>(scp >> 8);
+      const float s2l = -(128.0f * s1l + dd.y * static_cast<float>(mnp & 0xFF));
+      const float s2h = -(128.0f * s1h + dd.y * static_cast<float>(mnp >> 8));
+      sts128(trow + ((s * 4 + c) * 2) * 16, make_float4(s1l, s1l, s2l, s2l));
+      sts128(trow + ((s * 4 + c) * 2 + 1) * 16, make_float4(s1h, s1h, s2h, s2h));
+    }
+  }
+}
+
+// y += s1 D + s2 Sx for the two rows (g, g+8) of this thread and tokens
+// (2t, 2t+1) of one n8 block; e = the rows' (s1, s1, s2, s2)
+__device__ __forceinline__ void mma_epilogue(float2 (&acc)[2], const float (&d)[4],
+                                             const float (&sx)[4], float4 eg, float4 eg8) {
+  const float2 x01 = make_float2(sx[0], sx[1]);
+  acc[0] = __ffma2_rn(make_float2(eg.x, eg.y), make_float2(d[0], d[1]), acc[0]);
+  acc[0] = __ffma2_rn(make_float2(eg.z, eg.w), x01, acc[0]);
+  acc[1] = __ffma2_rn(make_float2(eg8.x, eg8.y), make_float2(d[2], d[3]), acc[1]);
+  acc[1] = __ffma2_rn(make_float2(eg8.z, eg8.w), x01, acc[1]);
+}
+
+// One stage of the verify kernel for this warp's 16 rows (Q4 family).
+template <class G, int NB>
+__device__ __forceinline__ void mma_stage_q4(const Params& p, const Tile& tl, int sl, int kx,
+                                             uint32_t st, int rbase, uint32_t tab,
+                                             float2 (&acc)[NB][2]) {
+  constexpr int F = G::kF;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t ones = kBf16One2;
+#pragma unroll
+  for (int s = 0; s < G::kSlabSB; ++s) {
+    if (sl * G::kSlabSB + s >= p.nsb) break;
+    // this thread's rows g and g+8: qs bytes 8t .. 8t+7 of every chunk
+    uint32_t rq[2], rh[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = rbase + g + 8 * h;
+      if constexpr (F == kG128) {
+        rq[h] = st + row * p.slot + 128 * s + 8 * t;
+      } else {
+        const uint32_t rec = st + row * p.slot + G::kBB * s;
+        rq[h] = rec + (F == kQ4K ? 16 : 48) + 8 * t;
+        rh[h] = rec + 16 + 8 * t;
+      }
+    }
+    uint2 qh[2] = {};
+    if constexpr (F == kQ5K) {
+      qh[0] = lds64(rh[0]);
+      qh[1] = lds64(rh[1]);
+    }
+    // x of this super-block: tokens g (+8), positions kx + 256 s + 64 c + [8t, 8t+8)
+    const int kpos = kx + 256 * s + 8 * t;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      // A fragments: [h][word][lo01, lo23, hi01, hi23]
+      uint32_t a[2][2][4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint2 wv = lds64(rq[h] + 32 * c);
+        const uint32_t wd[2] = {wv.x, wv.y};
+        const uint32_t hq[2] = {qh[h].x, qh[h].y};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if constexpr (F == kQ5K) {
+            const int rlo = (2 * c + 28) & 31, rhi = (2 * c + 29) & 31;
+            const uint32_t lo5 = bitsel(wd[i], __funnelshift_r(hq[i], hq[i], rlo), 0x0F0F0F0Fu);
+            const uint32_t hi5 = bitsel(wd[i] >> 4, __funnelshift_r(hq[i], hq[i], rhi), 0x0F0F0F0Fu);
+            bf16_pairs<0x001F001Fu>(lo5, a[h][i][0], a[h][i][1]);
+            bf16_pairs<0x001F001Fu>(hi5, a[h][i][2], a[h][i][3]);
+          } else {
+            bf16_pairs<0x000F000Fu>(wd[i], a[h][i][0], a[h][i][1]);
+            bf16_pairs<0x000F000Fu>(wd[i] >> 4, a[h][i][2], a[h][i][3]);
+          }
+        }
+      }
+      const float4 elo = lds_f4(tab + (g * G::kTabRow + (s * 4 + c) * 2) * 16);
+      const float4 ehi = lds_f4(tab + (g * G::kTabRow + (s * 4 + c) * 2 + 1) * 16);
+      const float4 elo8 = lds_f4(tab + ((g + 8) * G::kTabRow + (s * 4 + c) * 2) * 16);
+      const float4 ehi8 = lds_f4(tab + ((g + 8) * G::kTabRow + (s * 4 + c) * 2 + 1) * 16);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const int tok = g + 8 * nb;
+        uint4 blo = make_uint4(0, 0, 0, 0), bhi = make_uint4(0, 0, 0, 0);
+        if (tok < p.nt) {
+          const uint16_t* xr = p.x + static_cast<int64_t>(tok) * p.K + kpos + 64 * c;
+          blo = ldg_nc_v4(xr);
+          bhi = ldg_nc_v4(xr + 32);
+        }
+        float dlo[4] = {0.f, 0.f, 0.f, 0.f}, dhi[4] = {0.f, 0.f, 0.f, 0.f};
+        float slo[4] = {0.f, 0.f, 0.f, 0.f}, shi[4] = {0.f, 0.f, 0.f, 0.f};
+        // k-slots (2t, 2t+1) <- positions 8t + (0,1) of a word, (2t+8, 2t+9)
+        // <- 8t + (2,3); word 1 is positions 8t + 4 .. 8t + 7
+        mma_bf16(dlo, a[0][0][0], a[1][0][0], a[0][0][1], a[1][0][1], blo.x, blo.y);
+        mma_bf16(dlo, a[0][1][0], a[1][1][0], a[0][1][1], a[1][1][1], blo.z, blo.w);
+        mma_bf16(dhi, a[0][0][2], a[1][0][2], a[0][0][3], a[1][0][3], bhi.x, bhi.y);
+        mma_bf16(dhi, a[0][1][2], a[1][1][2], a[0][1][3], a[1][1][3], bhi.z, bhi.w);
+        mma_bf16(slo, ones, ones, ones, ones, blo.x, blo.y);
+        mma_bf16(slo, ones, ones, ones, ones, blo.z, blo.w);
+        mma_bf16(shi, ones, ones, ones, ones, bhi.x, bhi.y);
+        mma_bf16(shi, ones, ones, ones, ones, bhi.z, bhi.w);
+        mma_epilogue(acc[nb], dlo, slo, elo, elo8);
+        mma_epilogue(acc[nb], dhi, shi, ehi, ehi8);
+      }
+    }
+  }
+}
+
+// One stage of the verify kernel for this warp's 16 rows (Q6_K).  Unit of
+// an mma: sub-block j = 8h + 2tr + u (positions 128h + 32tr + 16u + [0,16));
+// thread t takes positions 4t .. 4t+3 of it: ql word A (t-runs 0 / 2), ql
+// word B (t-runs 1 / 3) and qh word H.
+template <class G, int NB>
+__device__ __forceinline__ void mma_stage_q6(const Params& p, const Tile& tl, int sl, int kx,
+                                             uint32_t st, int rbase, uint32_t tab,
+                                             float2 (&acc)[NB][2]) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t ones = kBf16One2;
+  const float2 m160 = make_float2(-160.0f, -160.0f);
+  uint32_t rec[2];
+#pragma unroll
+  for (int s = 0; s < G::kSlabSB; ++s) {
+    if (sl * G::kSlabSB + s >= p.nsb) break;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = rbase + g + 8 * h;
+      const uint32_t ro =
+          (static_cast<uint32_t>(tl.row0 + row) * ((210u * p.nsb) & 15u) + sl * G::kQBytes) & 15u;
+      rec[h] = st + row * p.slot + ro + 210 * s;
+    }
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        // A fragments [row h][t-run][01, 23]
+        uint32_t a[2][4][2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t A[1], B[1], H[1];
+          lds_words_a2<1>(rec[h] + 64 * hf + 16 * u + 4 * t, A);
+          lds_words_a2<1>(rec[h] + 64 * hf + 32 + 16 * u + 4 * t, B);
+          lds_words_a2<1>(rec[h] + 128 + 32 * hf + 16 * u + 4 * t, H);
+          const uint32_t M4 = 0x0F0F0F0Fu;
+          const uint32_t q0 = bitsel(A[0], H[0] << 4, M4);
+          const uint32_t q2 = bitsel(A[0] >> 4, H[0], M4);
+          const uint32_t q1 = bitsel(B[0], H[0] << 2, M4);
+          const uint32_t q3 = bitsel(B[0] >> 4, H[0] >> 2, M4);
+          bf16_pairs<0x003F003Fu>(q0, a[h][0][0], a[h][0][1]);
+          bf16_pairs<0x003F003Fu>(q1, a[h][1][0], a[h][1][1]);
+          bf16_pairs<0x003F003Fu>(q2, a[h][2][0], a[h][2][1]);
+          bf16_pairs<0x003F003Fu>(q3, a[h][3][0], a[h][3][1]);
+        }
+#pragma unroll
+        for (int tr = 0; tr < 4; ++tr) {
+          const int j = 8 * hf + 2 * tr + u;   // sub-block
+          const float4 eg = lds_f4(tab + (g * G::kTabRow + s * 8 + j / 2) * 16);
+          const float4 eg8 = lds_f4(tab + ((g + 8) * G::kTabRow + s * 8 + j / 2) * 16);
+          const float2 s1 = (j & 1) ? make_float2(eg.z, eg.w) : make_float2(eg.x, eg.y);
+          const float2 s18 = (j & 1) ? make_float2(eg8.z, eg8.w) : make_float2(eg8.x, eg8.y);
+          const int kpos = kx + 256 * s + 128 * hf + 32 * tr + 16 * u + 4 * t;
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            const int tok = g + 8 * nb;
+            uint2 b = make_uint2(0, 0);
+            if (tok < p.nt) b = ldg_nc_v2(p.x + static_cast<int64_t>(tok) * p.K + kpos);
+            float d[4] = {0.f, 0.f, 0.f, 0.f}, sx[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_bf16(d, a[0][tr][0], a[1][tr][0], a[0][tr][1], a[1][tr][1], b.x, b.y);
+            mma_bf16(sx, ones, ones, ones, ones, b.x, b.y);
+            const float2 x01 = make_float2(sx[0], sx[1]);
+            const float2 tg = __ffma2_rn(m160, x01, make_float2(d[0], d[1]));
+            const float2 tg8 = __ffma2_rn(m160, x01, make_float2(d[2], d[3]));
+            acc[nb][0] = __ffma2_rn(s1, tg, acc[nb][0]);
+            acc[nb][1] = __ffma2_rn(s18, tg8, acc[nb][1]);
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int F, int NB, int WC>
+__global__ void __launch_bounds__((WC + 1) * 32, 1)
+    gemv_mma(const __grid_constant__ Params p, int stages) {
+  using G = MGeo<F, WC>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
+  __shared__ int last_flag;
+  const uint32_t bar_full = smem_addr(&bars[0]);
+  const uint32_t bar_empty = smem_addr(&bars[kMaxStages]);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t tab0 = smem_addr(smem);                 // WC scale tables
+  const uint32_t ring_a = tab0 + p.x_bytes;
+  const int kseg = static_cast<int>(blockIdx.x) % p.ksplit;
+  const int cta = static_cast<int>(blockIdx.x) / p.ksplit;
+  const int cps = static_cast<int>(gridDim.x) / p.ksplit;
+  const int my_tiles = (p.tiles - cta + cps - 1) / cps;
+  const int total = my_tiles * p.slabs;
+  const int sl0 = kseg * p.slabs;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(bar_full + 8 * s, p.tma ? 1 : 32);
+      mbar_init(bar_empty + 8 * s, WC);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int first = total < stages ? total : stages;
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (warp == WC) {
+    for (int it = 0; it < first; ++it) {
+      const Tile tl = tile_of(p, cta + (it / p.slabs) * cps);
+      issue_stage<G>(p, smem, ring_a + it * p.stage, bar_full + 8 * it, tl, sl0 + it % p.slabs);
+    }
+    for (int it = first; it < total; ++it) {
+      const int slot = it % stages;
+      const uint32_t use = static_cast<uint32_t>(it / stages);
+      if (!mbar_wait_warp(bar_empty + 8 * slot, (use - 1) & 1)) return;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      const Tile tl = tile_of(p, cta + (it / p.slabs) * cps);
+      issue_stage<G>(p, smem, ring_a + slot * p.stage, bar_full + 8 * slot, tl, sl0 + it % p.slabs);
+    }
+    return;
+  }
+  // x is read from global memory: wait for the kernel that produced it
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const uint32_t tab = tab0 + static_cast<uint32_t>(warp * G::kTabBytes);
+  const int rbase = 16 * warp;
+  const int g = lane >> 2, t = lane & 3;
+  float2 acc[NB][2];
+  Tile tl{};
+  int tix = 0;
+  for (int it = 0; it < total; ++it) {
+    const int xsl = it % p.slabs;
+    const int sl = sl0 + xsl;
+    if (xsl == 0) {
+      tix = cta + (it / p.slabs) * cps;
+      tl = tile_of(p, tix);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = make_float2(0.0f, 0.0f);
+    }
+    const int slot = it % stages;
+    const uint32_t use = static_cast<uint32_t>(it / stages);
+    if (!mbar_wait_warp(bar_full + 8 * slot, use & 1)) return;
+    const uint32_t st = ring_a + slot * p.stage;
+    if (rbase < tl.rcnt) {   // warp-uniform
+      build_scale_table<G>(p, tl, sl, st, rbase, tab);
+      __syncwarp();
+      if constexpr (F == kQ6K)
+        mma_stage_q6<G, NB>(p, tl, sl, sl * G::kSlabK, st, rbase, tab, acc);
+      else
+        mma_stage_q4<G, NB>(p, tl, sl, sl * G::kSlabK, st, rbase, tab, acc);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+    if (xsl == p.slabs - 1) {
+      float* y = pick(p.g.y, tl.mi);
+      const int64_t N = pick(p.g.N, tl.mi);
+      constexpr int NTP = 8 * NB;   // tokens per partial-sum row
+      if (p.ksplit == 1) {
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int row = rbase + g + 8 * h;
+            const float v[2] = {acc[nb][h].x, acc[nb][h].y};
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int tok = 8 * nb + 2 * t + e;
+              if (row < tl.rcnt && tok < p.nt) y[static_cast<int64_t>(tok) * N + tl.row0 + row] = v[e];
+            }
+          }
+      } else {
+        float* part = p.part + static_cast<int64_t>(tix) * p.tile_rows * NTP;
+        const int64_t seg_stride = static_cast<int64_t>(p.tiles) * p.tile_rows * NTP;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int row = rbase + g + 8 * h;
+            if (row < tl.rcnt) {
+              float* q = part + kseg * seg_stride + row * NTP + 8 * nb + 2 * t;
+              __stcg(q, acc[nb][h].x);
+              __stcg(q + 1, acc[nb][h].y);
+            }
+          }
+        __threadfence();
+        asm volatile("bar.sync 1, %0;" ::"r"(WC * 32) : "memory");
+        if (threadIdx.x == 0) last_flag = atomicAdd(p.arrivals + tix, 1u) == static_cast<unsigned>(p.ksplit - 1);
+        asm volatile("bar.sync 1, %0;" ::"r"(WC * 32) : "memory");
+        if (last_flag) {
+          __threadfence();
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int row = rbase + g + 8 * h;
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int tok = 8 * nb + 2 * t + e;
+                if (row < tl.rcnt && tok < p.nt) {
+                  float v = 0.0f;
+                  for (int j = 0; j < p.ksplit; ++j) v += __ldcg(part + j * seg_stride + row * NTP + tok);
+                  y[static_cast<int64_t>(tok) * N + tl.row0 + row] = v;
+                }
+              }
+            }
+          if (threadIdx.x == 0) p.arrivals[tix] = 0u;
+        }
+      }
+    }
+  }
+}
+
 struct DevInfo {
   int sms = 0;
   size_t smem_optin = 0;      // dynamic + static shared memory one CTA may use
@@ -1394,11 +1845,171 @@ bool launch_nt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStre
     return launch_rt<F, NT, 4, 8>(g, x, K, n_tok, s, src, st);
 }
 
+// The verify kernel: tiles of 16 WC rows, slabs of two super-blocks, x
+// read from global memory (no staging), so shared memory holds only the
+// per-warp scale tables and the ring.  K segments: the fewest divisors of the
+// slabs of a row (at most 16) that give every resident CTA work.
+template <int F, int NB>
+bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
+                ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
+  constexpr int WC = 8;
+  using G = MGeo<F, WC>;
+  const DevInfo& di = dev_info();
+  const bool tma = tma_possible<G>(K);
+  const StageShape ss = stage_shape<G>(tma);
+  Params p;
+  p.g = g;
+  p.x = x;
+  p.K = K;
+  p.nsb = K / 256;
+  p.nt = n_tok;
+  p.part = nullptr;
+  p.arrivals = nullptr;
+  p.tma = tma ? 1 : 0;
+  p.slot = ss.slot;
+  p.pslot = ss.pslot;
+  p.pbase = ss.pbase;
+  p.stage = ss.bytes;
+  p.x_bytes = static_cast<uint32_t>((WC * G::kTabBytes + 127) / 128 * 128);
+  // shared-memory plan: two CTAs per SM if two stages fit, else one
+  int per_sm = 0, stages = 0;
+  for (int ps = 2; ps >= 1 && per_sm == 0; --ps) {
+    size_t budget = di.smem_sm / ps;
+    budget = budget > di.smem_reserved + kStaticSmem ? budget - di.smem_reserved - kStaticSmem : 0;
+    if (budget > di.smem_optin - kStaticSmem) budget = di.smem_optin - kStaticSmem;
+    if (p.x_bytes + 2 * static_cast<size_t>(ss.bytes) > budget) continue;
+    per_sm = ps;
+    stages = static_cast<int>((budget - p.x_bytes) / ss.bytes);
+    if (stages > kMaxStages) stages = kMaxStages;
+  }
+  if (per_sm == 0) return false;
+  const size_t smem = p.x_bytes + static_cast<size_t>(stages) * ss.bytes;
+  static size_t configured = 0;
+  if (smem > configured) {
+    if (cudaFuncSetAttribute(gemv_mma<F, NB, WC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return false;
+    }
+    configured = smem;
+  }
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_mma<F, NB, WC>, G::kThreads, smem) ==
+          cudaSuccess &&
+      occ >= 1 && occ < per_sm)
+    per_sm = occ;
+  int64_t rows = 0;
+  for (int i = 0; i < g.count; ++i) rows += g.N[i];
+  const int slabs_row = (p.nsb + G::kSlabSB - 1) / G::kSlabSB;
+  const int64_t resident = static_cast<int64_t>(per_sm) * di.sms;
+  const int64_t full_tiles = (rows + G::kRows - 1) / G::kRows;
+  int ksplit = 1;
+  for (int ks = 1; ks <= 16 && ks <= slabs_row; ++ks) {
+    if (slabs_row % ks != 0) continue;
+    ksplit = ks;
+    if (full_tiles * ks >= resident) break;
+  }
+  for (;; ksplit = 1) {
+    p.ksplit = ksplit;
+    p.slabs = slabs_row / ksplit;
+    p.kpad = p.slabs * G::kSlabK;
+    int cps = static_cast<int>(resident / ksplit);
+    if (cps < 1) cps = 1;
+    // balanced tiles of whole 16-row warp blocks
+    const int64_t k = (rows + static_cast<int64_t>(cps) * G::kRows - 1) /
+                      (static_cast<int64_t>(cps) * G::kRows);
+    int tr = static_cast<int>((rows + cps * k - 1) / (cps * k));
+    tr = (tr + 15) / 16 * 16;
+    if (tr > G::kRows) tr = G::kRows;
+    p.tile_rows = tr;
+    p.tiles = 0;
+    for (int i = 0; i < kMaxGroup; ++i) {
+      if (i < g.count) p.tiles += (g.N[i] + tr - 1) / tr;
+      p.tile_end[i] = p.tiles;
+    }
+    if (cps > p.tiles) cps = p.tiles;
+    bool ok = true;
+    if (ksplit > 1) {
+      const size_t part_bytes =
+          static_cast<size_t>(ksplit) * p.tiles * p.tile_rows * (8 * NB) * sizeof(float);
+      if (src == ScratchSrc::kDevice) {
+        uint8_t* base = p.tiles <= kMaxTiles
+                            ? static_cast<uint8_t*>(scratch_get(kCounterBytes + part_bytes, s))
+                            : nullptr;
+        if (base == nullptr) {
+          ok = false;
+        } else {
+          p.arrivals = reinterpret_cast<unsigned int*>(base);
+          p.part = reinterpret_cast<float*>(base + kCounterBytes);
+        }
+      } else {
+        if (p.tiles > kNoAllocMaxTiles ||
+            kNoAllocCounterBytes + part_bytes > kNoAllocScratchBytes) {
+          st->too_large = true;
+          return false;
+        }
+        if (cudaMemsetAsync(st->base, 0, static_cast<size_t>(p.tiles) * sizeof(unsigned int), s) !=
+            cudaSuccess)
+          return false;
+        p.arrivals = reinterpret_cast<unsigned int*>(st->base);
+        p.part = reinterpret_cast<float*>(st->base + kNoAllocCounterBytes);
+      }
+    }
+    if (!ok) {
+      if (ksplit == 1) return false;
+      continue;   // no scratch (e.g. during capture): unsplit
+    }
+    p.tx = 0;
+    if (tma) {
+      for (int i = 0; i < g.count; ++i) {
+        const int64_t n = g.N[i];
+        bool enc;
+        if constexpr (F == kG128) {
+          enc = encode_plane(&p.tm[i][0], g.W[i], 128 * static_cast<uint64_t>(p.nsb), n, ss.slot, tr) &&
+                encode_plane(&p.tm[i][1], g.W[i] + n * p.nsb * 128, 8 * static_cast<uint64_t>(p.nsb),
+                             n, ss.pslot, tr);
+        } else {
+          enc = encode_plane(&p.tm[i][0], g.W[i], static_cast<uint64_t>(p.nsb) * G::kBB, n, ss.slot, tr);
+        }
+        if (!enc) return false;
+      }
+      p.tx = static_cast<uint32_t>(tr) * (ss.slot + ss.pslot);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cps * ksplit));
+    cfg.blockDim = dim3(G::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_mma<F, NB, WC>, p, stages) == cudaSuccess;
+  }
+}
+
+template <int F>
+bool launch_verify(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
+                   ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
+  return n_tok <= 8 ? launch_mma<F, 1>(g, x, K, n_tok, s, src, st)
+                    : launch_mma<F, 2>(g, x, K, n_tok, s, src, st);
+}
+
 }  // namespace
 
 bool launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
                    cudaStream_t s) {
-  if (n_tok > 4) return false;
+  if (n_tok > 16) return false;
+  if (n_tok > 4) {
+    switch (fmt) {
+      case kQ4K: return launch_verify<kQ4K>(g, x, K, n_tok, s);
+      case kQ5K: return launch_verify<kQ5K>(g, x, K, n_tok, s);
+      case kQ6K: return launch_verify<kQ6K>(g, x, K, n_tok, s);
+      case kG128: return launch_verify<kG128>(g, x, K, n_tok, s);
+    }
+    return false;
+  }
   const int nt = n_tok <= 1 ? 1 : (n_tok <= 2 ? 2 : 4);
 #define KQ_CASE(F)                                                  \
   case F:                                                           \
@@ -1449,11 +2060,22 @@ void* noalloc_scratch_address() {
 
 NoAllocResult launch_stream_noalloc(int fmt, const GemvGroup& g, const uint16_t* x, int K,
                                     int n_tok, cudaStream_t s) {
-  if (n_tok > 4) return NoAllocResult::kNotServed;
+  if (n_tok > 16) return NoAllocResult::kNotServed;
   StaticScratch st{static_cast<uint8_t*>(noalloc_scratch_address()), false};
   if (st.base == nullptr) return NoAllocResult::kFailed;
-  const int nt = n_tok <= 1 ? 1 : (n_tok <= 2 ? 2 : 4);
   bool ok = false;
+  if (n_tok > 4) {
+    switch (fmt) {
+      case kQ4K: ok = launch_verify<kQ4K>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st); break;
+      case kQ5K: ok = launch_verify<kQ5K>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st); break;
+      case kQ6K: ok = launch_verify<kQ6K>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st); break;
+      case kG128: ok = launch_verify<kG128>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st); break;
+      default: return NoAllocResult::kFailed;
+    }
+    if (st.too_large) return NoAllocResult::kTooLarge;
+    return ok ? NoAllocResult::kLaunched : NoAllocResult::kNotServed;
+  }
+  const int nt = n_tok <= 1 ? 1 : (n_tok <= 2 ? 2 : 4);
 #define KQ_CASE(F)                                                                          \
   case F:                                                                                   \
     ok = nt == 1   ? launch_nt<F, 1>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st)           \
