@@ -128,6 +128,11 @@ __device__ __forceinline__ float4 lds_f4(uint32_t a) {
                : "r"(a));
   return v;
 }
+__device__ __forceinline__ void sts128u(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
 __device__ __forceinline__ void sts128(uint32_t a, float4 v) {
   asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(a), "f"(v.x), "f"(v.y), "f"(v.z),
                "f"(v.w)
@@ -146,6 +151,19 @@ __device__ __forceinline__ void lds_words_a2(uint32_t a, uint32_t (&w)[N]) {
   uint32_t raw[N + 1];
 #pragma unroll
   for (int i = 0; i <= N; ++i) raw[i] = lds32(base + 4 * i);
+#pragma unroll
+  for (int i = 0; i < N; ++i) w[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
+}
+
+// n consecutive 32-bit words at byte offset off (a multiple of 4) of a
+// record that starts on a 2-byte boundary: base = record & ~3, sh = 8 *
+// (record & 3), both computed once per record.
+template <int N>
+__device__ __forceinline__ void lds_words_rec(uint32_t base, uint32_t sh, uint32_t off,
+                                              uint32_t (&w)[N]) {
+  uint32_t raw[N + 1];
+#pragma unroll
+  for (int i = 0; i <= N; ++i) raw[i] = lds32(base + off + 4 * i);
 #pragma unroll
   for (int i = 0; i < N; ++i) w[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
 }
@@ -211,13 +229,13 @@ struct StageShape {
   uint32_t slot, pslot, pbase, bytes;
 };
 template <class G>
-StageShape stage_shape(bool tma) {
+StageShape stage_shape(bool tma, int rows = G::kRows) {
   auto r128 = [](uint32_t b) { return (b + 127u) / 128u * 128u; };
   StageShape s;
   s.slot = tma ? G::kSlotTma : G::kSlotBulk;
   s.pslot = tma ? G::kPSlotTma : G::kPSlotBulk;
-  s.pbase = r128(G::kRows * s.slot);
-  s.bytes = s.pbase + r128(G::kRows * s.pslot);
+  s.pbase = r128(rows * s.slot);
+  s.bytes = s.pbase + r128(rows * s.pslot);
   return s;
 }
 
@@ -817,12 +835,13 @@ __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl
     const uint32_t ro =
         (static_cast<uint32_t>(tl.row0 + row) * ((210u * p.nsb) & 15u) + sl * G::kQBytes) & 15u;
     const uint32_t rec = st + row * p.slot + ro + 210 * sbl;
+    const uint32_t rb = rec & ~3u, rsh = (rec & 3u) * 8u;
     uint32_t A[QW], B[QW], H[QW], S[2], D[1];
-    lds_words_a2<QW>(rec + 64 * h + l0, A);
-    lds_words_a2<QW>(rec + 64 * h + 32 + l0, B);
-    lds_words_a2<QW>(rec + 128 + 32 * h + l0, H);
-    lds_words_a2<2>(rec + 192 + 8 * h, S);
-    lds_words_a2<1>(rec + 208, D);
+    lds_words_rec<QW>(rb, rsh, 64 * h + l0, A);
+    lds_words_rec<QW>(rb, rsh, 64 * h + 32 + l0, B);
+    lds_words_rec<QW>(rb, rsh, 128 + 32 * h + l0, H);
+    lds_words_rec<2>(rb, rsh, 192 + 8 * h, S);
+    lds_words_rec<1>(rb, rsh, 208, D);
     // scales of the unit's sub-blocks: t0 byte su, t1 su+2 (of S[0]), t2 su,
     // t3 su+2 (of S[1]); sign-extended with a byte permute
     const uint32_t sel0 = su | ((8 | su) << 4) | ((8 | su) << 8) | ((8 | su) << 12);
@@ -1062,9 +1081,10 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
 // mma.sync m16n8k16 (bf16 operands, fp32 accumulators).  A = weights: a warp
 // owns 16 rows of a tile; each qs byte's nibble becomes one bf16 value
 // 128 + q (one LOP3 builds two: (w & 0x000F000F) | 0x43004300), exact.  B = x,
-// eight tokens per mma (two mmas per A fragment for 9..16 tokens), loaded as
-// bf16 straight from global memory (small, shared by every CTA: L1/L2
-// resident).  Per sub-block the accumulator holds D = 128 Sx + sum q x, and a
+// eight tokens per mma (two mmas per A fragment for 9..16 tokens): the CTA's
+// K segment of x is staged once as bf16 in shared memory, one row per token
+// padded by 64 bytes so that the eight tokens of a fragment load hit
+// different banks.  Per sub-block the accumulator holds D = 128 Sx + sum q x, and a
 // second mma against an all-ones A gives Sx, so
 //   y += s1 D + s2 Sx,  s1 = d sc,  s2 = -(128 s1 + dmin m)       (Q4 family)
 //   y += s1 (D - 160 Sx), s1 = d sc                               (Q6_K: q - 32)
@@ -1094,6 +1114,10 @@ struct MGeo {
   //   Q6_K:      (row, s, j) -> (s1, s1) of sub-block j (two per float4)
   static constexpr int kTabRow = (F == kQ6K) ? kSlabSB * 8 + 1 : kSlabSB * 8 + 1;
   static constexpr int kTabBytes = 16 * kTabRow * 16;
+  // bytes of padding per staged token row of x: the B loads of the eight
+  // tokens of a fragment (16-byte loads in 8-lane phases for the Q4 family,
+  // 8-byte loads in 16-lane phases for Q6_K) fall in distinct banks
+  static constexpr int kXPad = (F == kQ6K) ? 32 : 64;
 };
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -1212,8 +1236,8 @@ __device__ __forceinline__ void mma_epilogue(float2 (&acc)[2], const float (&d)[
 // One stage of the verify kernel for this warp's 16 rows (Q4 family).
 template <class G, int NB>
 __device__ __forceinline__ void mma_stage_q4(const Params& p, const Tile& tl, int sl, int kx,
-                                             uint32_t st, int rbase, uint32_t tab,
-                                             float2 (&acc)[NB][2]) {
+                                             uint32_t st, int rbase, uint32_t tab, uint32_t xsh,
+                                             uint32_t xstride, float2 (&acc)[NB][2]) {
   constexpr int F = G::kF;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -1239,8 +1263,9 @@ __device__ __forceinline__ void mma_stage_q4(const Params& p, const Tile& tl, in
       qh[0] = lds64(rh[0]);
       qh[1] = lds64(rh[1]);
     }
-    // x of this super-block: tokens g (+8), positions kx + 256 s + 64 c + [8t, 8t+8)
-    const int kpos = kx + 256 * s + 8 * t;
+    // staged x of this super-block: tokens g (+8), positions kx + 256 s + 64 c
+    // + [8t, 8t+8) of the segment
+    const uint32_t xb = xsh + g * xstride + 2 * (kx + 256 * s + 8 * t);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       // A fragments: [h][word][lo01, lo23, hi01, hi23]
@@ -1270,13 +1295,8 @@ __device__ __forceinline__ void mma_stage_q4(const Params& p, const Tile& tl, in
       const float4 ehi8 = lds_f4(tab + ((g + 8) * G::kTabRow + (s * 4 + c) * 2 + 1) * 16);
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
-        const int tok = g + 8 * nb;
-        uint4 blo = make_uint4(0, 0, 0, 0), bhi = make_uint4(0, 0, 0, 0);
-        if (tok < p.nt) {
-          const uint16_t* xr = p.x + static_cast<int64_t>(tok) * p.K + kpos + 64 * c;
-          blo = ldg_nc_v4(xr);
-          bhi = ldg_nc_v4(xr + 32);
-        }
+        const uint4 blo = lds128(xb + nb * 8 * xstride + 128 * c);
+        const uint4 bhi = lds128(xb + nb * 8 * xstride + 128 * c + 64);
         float dlo[4] = {0.f, 0.f, 0.f, 0.f}, dhi[4] = {0.f, 0.f, 0.f, 0.f};
         float slo[4] = {0.f, 0.f, 0.f, 0.f}, shi[4] = {0.f, 0.f, 0.f, 0.f};
         // k-slots (2t, 2t+1) <- positions 8t + (0,1) of a word, (2t+8, 2t+9)
@@ -1302,8 +1322,8 @@ __device__ __forceinline__ void mma_stage_q4(const Params& p, const Tile& tl, in
 // word B (t-runs 1 / 3) and qh word H.
 template <class G, int NB>
 __device__ __forceinline__ void mma_stage_q6(const Params& p, const Tile& tl, int sl, int kx,
-                                             uint32_t st, int rbase, uint32_t tab,
-                                             float2 (&acc)[NB][2]) {
+                                             uint32_t st, int rbase, uint32_t tab, uint32_t xsh,
+                                             uint32_t xstride, float2 (&acc)[NB][2]) {
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const uint32_t ones = kBf16One2;
@@ -1328,9 +1348,10 @@ __device__ __forceinline__ void mma_stage_q6(const Params& p, const Tile& tl, in
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t A[1], B[1], H[1];
-          lds_words_a2<1>(rec[h] + 64 * hf + 16 * u + 4 * t, A);
-          lds_words_a2<1>(rec[h] + 64 * hf + 32 + 16 * u + 4 * t, B);
-          lds_words_a2<1>(rec[h] + 128 + 32 * hf + 16 * u + 4 * t, H);
+          const uint32_t rb = rec[h] & ~3u, rsh = (rec[h] & 3u) * 8u;
+          lds_words_rec<1>(rb, rsh, 64 * hf + 16 * u + 4 * t, A);
+          lds_words_rec<1>(rb, rsh, 64 * hf + 32 + 16 * u + 4 * t, B);
+          lds_words_rec<1>(rb, rsh, 128 + 32 * hf + 16 * u + 4 * t, H);
           const uint32_t M4 = 0x0F0F0F0Fu;
           const uint32_t q0 = bitsel(A[0], H[0] << 4, M4);
           const uint32_t q2 = bitsel(A[0] >> 4, H[0], M4);
@@ -1348,12 +1369,11 @@ __device__ __forceinline__ void mma_stage_q6(const Params& p, const Tile& tl, in
           const float4 eg8 = lds_f4(tab + ((g + 8) * G::kTabRow + s * 8 + j / 2) * 16);
           const float2 s1 = (j & 1) ? make_float2(eg.z, eg.w) : make_float2(eg.x, eg.y);
           const float2 s18 = (j & 1) ? make_float2(eg8.z, eg8.w) : make_float2(eg8.x, eg8.y);
-          const int kpos = kx + 256 * s + 128 * hf + 32 * tr + 16 * u + 4 * t;
+          const uint32_t xb =
+              xsh + g * xstride + 2 * (kx + 256 * s + 128 * hf + 32 * tr + 16 * u + 4 * t);
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
-            const int tok = g + 8 * nb;
-            uint2 b = make_uint2(0, 0);
-            if (tok < p.nt) b = ldg_nc_v2(p.x + static_cast<int64_t>(tok) * p.K + kpos);
+            const uint2 b = lds64(xb + nb * 8 * xstride);
             float d[4] = {0.f, 0.f, 0.f, 0.f}, sx[4] = {0.f, 0.f, 0.f, 0.f};
             mma_bf16(d, a[0][tr][0], a[1][tr][0], a[0][tr][1], a[1][tr][1], b.x, b.y);
             mma_bf16(sx, ones, ones, ones, ones, b.x, b.y);
@@ -1379,7 +1399,10 @@ __global__ void __launch_bounds__((WC + 1) * 32, 1)
   const uint32_t bar_full = smem_addr(&bars[0]);
   const uint32_t bar_empty = smem_addr(&bars[kMaxStages]);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t tab0 = smem_addr(smem);                 // WC scale tables
+  constexpr int NTP = 8 * NB;   // staged token rows
+  const uint32_t tab0 = smem_addr(smem);                            // WC scale tables
+  const uint32_t xsh = tab0 + static_cast<uint32_t>(WC * G::kTabBytes);   // x segment
+  const uint32_t xstride = static_cast<uint32_t>(p.kpad * 2 + G::kXPad);
   const uint32_t ring_a = tab0 + p.x_bytes;
   const int kseg = static_cast<int>(blockIdx.x) % p.ksplit;
   const int cta = static_cast<int>(blockIdx.x) / p.ksplit;
@@ -1402,6 +1425,34 @@ __global__ void __launch_bounds__((WC + 1) * 32, 1)
       const Tile tl = tile_of(p, cta + (it / p.slabs) * cps);
       issue_stage<G>(p, smem, ring_a + it * p.stage, bar_full + 8 * it, tl, sl0 + it % p.slabs);
     }
+  }
+  // x may be produced by the previous kernel: wait for it, then stage the
+  // segment (bf16, zeros past K and for tokens >= n_tok), four 16-byte
+  // chunks per thread in flight
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  {
+    const int kbase = kseg * p.kpad;
+    const int per_tok = p.kpad / 8;
+    const int items = NTP * per_tok;
+    for (int q0 = threadIdx.x; q0 < items; q0 += 4 * blockDim.x) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = q0 + u * blockDim.x;
+        const int tok = q / per_tok, j = q % per_tok;
+        v[u] = make_uint4(0, 0, 0, 0);
+        if (q < items && tok < p.nt && kbase + 8 * j < p.K)
+          v[u] = ldg_nc_v4(p.x + static_cast<int64_t>(tok) * p.K + kbase + 8 * j);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = q0 + u * blockDim.x;
+        if (q < items) sts128u(xsh + (q / per_tok) * xstride + 16 * (q % per_tok), v[u]);
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == WC) {
     for (int it = first; it < total; ++it) {
       const int slot = it % stages;
       const uint32_t use = static_cast<uint32_t>(it / stages);
@@ -1412,8 +1463,6 @@ __global__ void __launch_bounds__((WC + 1) * 32, 1)
     }
     return;
   }
-  // x is read from global memory: wait for the kernel that produced it
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t tab = tab0 + static_cast<uint32_t>(warp * G::kTabBytes);
   const int rbase = 16 * warp;
   const int g = lane >> 2, t = lane & 3;
@@ -1437,16 +1486,15 @@ __global__ void __launch_bounds__((WC + 1) * 32, 1)
       build_scale_table<G>(p, tl, sl, st, rbase, tab);
       __syncwarp();
       if constexpr (F == kQ6K)
-        mma_stage_q6<G, NB>(p, tl, sl, sl * G::kSlabK, st, rbase, tab, acc);
+        mma_stage_q6<G, NB>(p, tl, sl, xsl * G::kSlabK, st, rbase, tab, xsh, xstride, acc);
       else
-        mma_stage_q4<G, NB>(p, tl, sl, sl * G::kSlabK, st, rbase, tab, acc);
+        mma_stage_q4<G, NB>(p, tl, sl, xsl * G::kSlabK, st, rbase, tab, xsh, xstride, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
     if (xsl == p.slabs - 1) {
       float* y = pick(p.g.y, tl.mi);
       const int64_t N = pick(p.g.N, tl.mi);
-      constexpr int NTP = 8 * NB;   // tokens per partial-sum row
       if (p.ksplit == 1) {
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
@@ -1577,6 +1625,7 @@ struct Plan {
   int per_sm = 0;
   int stages = 0;
   size_t smem = 0;
+  size_t budget = 0;   // dynamic shared memory one CTA may use at per_sm CTAs per SM
 };
 
 template <int F, int NT, int RT, int WC, bool XBF>
@@ -1602,6 +1651,7 @@ Plan make_plan(int K, int ksplit, bool tma) {
     pl.per_sm = per_sm;
     pl.stages = stages;
     pl.smem = pl.x_bytes + static_cast<size_t>(stages) * stage;
+    pl.budget = budget;
     return pl;
   }
   return pl;
@@ -1690,31 +1740,17 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   p.arrivals = nullptr;
   const Plan pl = make_plan<F, NT, RT, WC, XBF>(K, ksplit, tma);
   if (pl.per_sm == 0) return false;
-  const StageShape ss = stage_shape<G>(tma);
   p.tma = tma ? 1 : 0;
-  p.slot = ss.slot;
-  p.pslot = ss.pslot;
-  p.pbase = ss.pbase;
-  p.stage = ss.bytes;
   p.x_bytes = pl.x_bytes;
   int per_sm = pl.per_sm;
-  const int stages = pl.stages;
-  const size_t smem = pl.smem;
-  static size_t configured = 0;   // dynamic shared memory above 48 KB is opt-in
-  if (smem > configured) {
-    if (cudaFuncSetAttribute(gemv_stream<F, NT, RT, WC, XBF>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return false;
-    }
-    configured = smem;
+  {
+    int occ = 0;   // registers may allow fewer CTAs than shared memory does
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_stream<F, NT, RT, WC, XBF>,
+                                                      G::kThreads, pl.smem) == cudaSuccess &&
+        occ >= 1 && occ < per_sm)
+      per_sm = occ;
+    (void)cudaGetLastError();
   }
-  int occ = 0;   // registers may allow fewer CTAs than shared memory does
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_stream<F, NT, RT, WC, XBF>, G::kThreads,
-                                                    smem) == cudaSuccess &&
-      occ >= 1 && occ < per_sm)
-    per_sm = occ;
   // CTAs per K segment, all resident at once
   int cps = per_sm * di.sms / ksplit;
   if (cps < 1) cps = 1;
@@ -1737,6 +1773,27 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
     p.tile_end[i] = p.tiles;
   }
   if (cps > p.tiles) cps = p.tiles;
+  // stages hold tile_rows rows: as many as the CTA's share of shared memory
+  // takes (small tiles get a deep ring and request most of their K at once)
+  const StageShape ss = stage_shape<G>(tma, tr);
+  p.slot = ss.slot;
+  p.pslot = ss.pslot;
+  p.pbase = ss.pbase;
+  p.stage = ss.bytes;
+  int stages = static_cast<int>((pl.budget - p.x_bytes) / ss.bytes);
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < pl.stages) stages = pl.stages;
+  const size_t smem = p.x_bytes + static_cast<size_t>(stages) * ss.bytes;
+  static size_t configured = 0;   // dynamic shared memory above 48 KB is opt-in
+  if (smem > configured) {
+    if (cudaFuncSetAttribute(gemv_stream<F, NT, RT, WC, XBF>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return false;
+    }
+    configured = smem;
+  }
   p.tx = 0;
   if (tma) {
     for (int i = 0; i < g.count; ++i) {
@@ -1845,18 +1902,20 @@ bool launch_nt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStre
     return launch_rt<F, NT, 4, 8>(g, x, K, n_tok, s, src, st);
 }
 
-// The verify kernel: tiles of 16 WC rows, slabs of two super-blocks, x
-// read from global memory (no staging), so shared memory holds only the
-// per-warp scale tables and the ring.  K segments: the fewest divisors of the
-// slabs of a row (at most 16) that give every resident CTA work.
+// The verify kernel: tiles of 16 WC rows, slabs of two super-blocks; shared
+// memory holds the per-warp scale tables, the CTA's K segment of x (bf16,
+// 8 or 16 token rows) and the weight ring.  K segments: among the divisors
+// of the slabs of a row (at most 16) whose x segment fits with two stages,
+// the fewest that give every resident CTA work.
 template <int F, int NB>
 bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
                 ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
   constexpr int WC = 8;
+  constexpr int NTP = 8 * NB;
   using G = MGeo<F, WC>;
   const DevInfo& di = dev_info();
   const bool tma = tma_possible<G>(K);
-  const StageShape ss = stage_shape<G>(tma);
+  const StageShape full = stage_shape<G>(tma);
   Params p;
   p.g = g;
   p.x = x;
@@ -1866,53 +1925,57 @@ bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   p.part = nullptr;
   p.arrivals = nullptr;
   p.tma = tma ? 1 : 0;
-  p.slot = ss.slot;
-  p.pslot = ss.pslot;
-  p.pbase = ss.pbase;
-  p.stage = ss.bytes;
-  p.x_bytes = static_cast<uint32_t>((WC * G::kTabBytes + 127) / 128 * 128);
-  // shared-memory plan: two CTAs per SM if two stages fit, else one
-  int per_sm = 0, stages = 0;
-  for (int ps = 2; ps >= 1 && per_sm == 0; --ps) {
-    size_t budget = di.smem_sm / ps;
-    budget = budget > di.smem_reserved + kStaticSmem ? budget - di.smem_reserved - kStaticSmem : 0;
-    if (budget > di.smem_optin - kStaticSmem) budget = di.smem_optin - kStaticSmem;
-    if (p.x_bytes + 2 * static_cast<size_t>(ss.bytes) > budget) continue;
-    per_sm = ps;
-    stages = static_cast<int>((budget - p.x_bytes) / ss.bytes);
-    if (stages > kMaxStages) stages = kMaxStages;
-  }
-  if (per_sm == 0) return false;
-  const size_t smem = p.x_bytes + static_cast<size_t>(stages) * ss.bytes;
-  static size_t configured = 0;
-  if (smem > configured) {
-    if (cudaFuncSetAttribute(gemv_mma<F, NB, WC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return false;
-    }
-    configured = smem;
-  }
-  int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_mma<F, NB, WC>, G::kThreads, smem) ==
-          cudaSuccess &&
-      occ >= 1 && occ < per_sm)
-    per_sm = occ;
+  p.slot = full.slot;
+  p.pslot = full.pslot;
+  p.pbase = full.pbase;
+  p.stage = full.bytes;
   int64_t rows = 0;
   for (int i = 0; i < g.count; ++i) rows += g.N[i];
   const int slabs_row = (p.nsb + G::kSlabSB - 1) / G::kSlabSB;
+  auto x_bytes_of = [&](int ks) {
+    const size_t seg = static_cast<size_t>(slabs_row / ks) * G::kSlabK;
+    return (static_cast<size_t>(WC) * G::kTabBytes + NTP * (seg * 2 + G::kXPad) + 127) / 128 * 128;
+  };
+  // (CTAs per SM, fitting K-segment counts): two CTAs per SM if anything fits
+  int per_sm = 0;
+  size_t budget = 0;
+  int fits[16];
+  int nfit = 0;
+  for (int ps = 2; ps >= 1 && per_sm == 0; --ps) {
+    budget = di.smem_sm / ps;
+    budget = budget > di.smem_reserved + kStaticSmem ? budget - di.smem_reserved - kStaticSmem : 0;
+    if (budget > di.smem_optin - kStaticSmem) budget = di.smem_optin - kStaticSmem;
+    nfit = 0;
+    for (int ks = 1; ks <= 16 && ks <= slabs_row; ++ks)
+      if (slabs_row % ks == 0 && x_bytes_of(ks) + 2 * static_cast<size_t>(full.bytes) <= budget)
+        fits[nfit++] = ks;
+    if (nfit > 0) per_sm = ps;
+  }
+  if (per_sm == 0) return false;
+  {
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &occ, gemv_mma<F, NB, WC>, G::kThreads,
+            x_bytes_of(fits[0]) + 2 * static_cast<size_t>(full.bytes)) == cudaSuccess &&
+        occ >= 1 && occ < per_sm)
+      per_sm = occ;
+    (void)cudaGetLastError();
+  }
   const int64_t resident = static_cast<int64_t>(per_sm) * di.sms;
   const int64_t full_tiles = (rows + G::kRows - 1) / G::kRows;
-  int ksplit = 1;
-  for (int ks = 1; ks <= 16 && ks <= slabs_row; ++ks) {
-    if (slabs_row % ks != 0) continue;
-    ksplit = ks;
-    if (full_tiles * ks >= resident) break;
-  }
-  for (;; ksplit = 1) {
+  int pick_i = nfit - 1;
+  for (int i = 0; i < nfit; ++i)
+    if (full_tiles * fits[i] >= resident) {
+      pick_i = i;
+      break;
+    }
+  for (;; --pick_i) {
+    if (pick_i < 0) return false;
+    const int ksplit = fits[pick_i];
     p.ksplit = ksplit;
     p.slabs = slabs_row / ksplit;
     p.kpad = p.slabs * G::kSlabK;
+    p.x_bytes = static_cast<uint32_t>(x_bytes_of(ksplit));
     int cps = static_cast<int>(resident / ksplit);
     if (cps < 1) cps = 1;
     // balanced tiles of whole 16-row warp blocks
@@ -1928,20 +1991,28 @@ bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
       p.tile_end[i] = p.tiles;
     }
     if (cps > p.tiles) cps = p.tiles;
-    bool ok = true;
+    int stages = static_cast<int>((budget - p.x_bytes) / full.bytes);
+    if (stages > kMaxStages) stages = kMaxStages;
+    const size_t smem = p.x_bytes + static_cast<size_t>(stages) * full.bytes;
+    static size_t configured = 0;
+    if (smem > configured) {
+      if (cudaFuncSetAttribute(gemv_mma<F, NB, WC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+      }
+      configured = smem;
+    }
     if (ksplit > 1) {
       const size_t part_bytes =
-          static_cast<size_t>(ksplit) * p.tiles * p.tile_rows * (8 * NB) * sizeof(float);
+          static_cast<size_t>(ksplit) * p.tiles * p.tile_rows * NTP * sizeof(float);
       if (src == ScratchSrc::kDevice) {
         uint8_t* base = p.tiles <= kMaxTiles
                             ? static_cast<uint8_t*>(scratch_get(kCounterBytes + part_bytes, s))
                             : nullptr;
-        if (base == nullptr) {
-          ok = false;
-        } else {
-          p.arrivals = reinterpret_cast<unsigned int*>(base);
-          p.part = reinterpret_cast<float*>(base + kCounterBytes);
-        }
+        if (base == nullptr) continue;   // no scratch (e.g. during capture): fewer segments
+        p.arrivals = reinterpret_cast<unsigned int*>(base);
+        p.part = reinterpret_cast<float*>(base + kCounterBytes);
       } else {
         if (p.tiles > kNoAllocMaxTiles ||
             kNoAllocCounterBytes + part_bytes > kNoAllocScratchBytes) {
@@ -1955,25 +2026,21 @@ bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
         p.part = reinterpret_cast<float*>(st->base + kNoAllocCounterBytes);
       }
     }
-    if (!ok) {
-      if (ksplit == 1) return false;
-      continue;   // no scratch (e.g. during capture): unsplit
-    }
     p.tx = 0;
     if (tma) {
       for (int i = 0; i < g.count; ++i) {
         const int64_t n = g.N[i];
         bool enc;
         if constexpr (F == kG128) {
-          enc = encode_plane(&p.tm[i][0], g.W[i], 128 * static_cast<uint64_t>(p.nsb), n, ss.slot, tr) &&
+          enc = encode_plane(&p.tm[i][0], g.W[i], 128 * static_cast<uint64_t>(p.nsb), n, full.slot, tr) &&
                 encode_plane(&p.tm[i][1], g.W[i] + n * p.nsb * 128, 8 * static_cast<uint64_t>(p.nsb),
-                             n, ss.pslot, tr);
+                             n, full.pslot, tr);
         } else {
-          enc = encode_plane(&p.tm[i][0], g.W[i], static_cast<uint64_t>(p.nsb) * G::kBB, n, ss.slot, tr);
+          enc = encode_plane(&p.tm[i][0], g.W[i], static_cast<uint64_t>(p.nsb) * G::kBB, n, full.slot, tr);
         }
         if (!enc) return false;
       }
-      p.tx = static_cast<uint32_t>(tr) * (ss.slot + ss.pslot);
+      p.tx = static_cast<uint32_t>(tr) * (full.slot + full.pslot);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(cps * ksplit));
