@@ -35,6 +35,10 @@ sys.path.insert(0, ROOT)
 import workloads as wl  # noqa: E402
 
 METRIC = "K-quant GEMV weight GB/s (% of B300 HBM peak) at 1/8 tokens; us per decode step"
+# single launches of one decoder layer (layer 0's weights), for profiling:
+# the matrices that share the launch
+CASES = {"qkv": ("q", "k", "v"), "o": ("o",), "gate_up": ("gate", "up"), "down": ("down",),
+         "lm_head": ("lm_head",)}
 WORKLOAD = "decode_step_52L_h5120_i32768_q4k_q6k_lmhead200000"
 
 
@@ -47,6 +51,8 @@ def parse():
     p.add_argument("--impl", default="kq", choices=["kq", "reference"])
     p.add_argument("--layers", type=int, default=wl.LAYERS)
     p.add_argument("--no-extra", action="store_true", help="skip the n_tok=8 line and e2e")
+    p.add_argument("--case", default="step", choices=["step"] + sorted(CASES),
+                   help="one launch of the decode step instead of the whole step (for profiling)")
     return p.parse_args()
 
 
@@ -460,10 +466,55 @@ def run_kq(args):
     barrier(dist)
 
 
+def run_case(args):
+    """--case NAME: warm-up + `steps` launches of one grouped launch of the
+    decode step on its full-size matrices (the same weights every launch;
+    q/k/v and o fit in L2), timed with CUDA events; one JSON line."""
+    import torch
+    import quant_weight_gemv_dequant_b300 as kq
+    _, local, _ = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    kq.lib()
+    pools = build_pools_library(device)
+    names = CASES[args.case]
+    mats = [wl.LM_HEAD] if names == ("lm_head",) else [m for m in wl.DECODE_LAYER if m.name in names]
+    Ws = [wl.tile_matrix_device(pools[m.fmt], m.fmt, wl.derive_seed(5, 0, i), m.N, m.K)
+          for i, m in enumerate(mats)]
+    fmt, K, T = mats[0].fmt, mats[0].K, args.n_tok
+    xb = wl.activations_bf16(wl.derive_seed(5, 0, 100), T, K)
+    x = torch.from_numpy(xb.view(np.int16)).to(device).view(torch.bfloat16)
+    ys = [torch.empty((T, m.N), dtype=torch.float32, device=device) for m in mats]
+    Ns = [m.N for m in mats]
+    stream = torch.cuda.current_stream(device)
+
+    def launch():
+        kq.kq_gemv_multi(fmt, Ws, ys, Ns, x, K, T)
+
+    for _ in range(max(3, args.warmup)):
+        launch()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        launch()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / args.steps
+    nbytes = sum(m.nbytes for m in mats)
+    print(json.dumps({"case": args.case, "matrices": [f"{m.name} {m.N}x{m.K} fmt {m.fmt}" for m in mats],
+                      "n_tok": T, "launches": args.steps, "us_per_launch": t * 1e6,
+                      "weight_gb_s": nbytes / t / 1e9,
+                      "l2": "weights resident in L2" if nbytes < 100e6 else "weights larger than L2",
+                      "status": kq.kq_device_status(check=False)}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.case != "step":
+        run_case(args)
     else:
         run_kq(args)
 

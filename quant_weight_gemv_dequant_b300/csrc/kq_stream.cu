@@ -791,7 +791,8 @@ __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl
 // pairs (t0, t2), (t1, t3), accumulated with packed fmas against the staged x
 // pairs; the scales apply as the pairs (d sc_t0, d sc_t2), (d sc_t1, d sc_t3)
 // and q - 32 as ds (S - 32 sx).  Records start on 2-byte boundaries: words
-// are read aligned and shifted.
+// are read aligned and shifted.  Word-outer order, as in stage_q4: one
+// word's x is live at a time and the scales are decoded after the products.
 template <int NT, int RT, int WC, int NR, bool XBF>
 __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl, int xsl,
                                          uint32_t st, uint32_t xs, int hw, int sbl, int un,
@@ -805,64 +806,47 @@ __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl
   const int u2 = un % (G::kUnitsPerSB / 2);
   const int l0 = u2 * (kCW / 4);
   const int su = l0 >> 4;   // sub-block of the unit within each t-run
-  // xp[k][j][b][0] = (x_t0, x_t2), [1] = (x_t1, x_t3) of column 4j + b
-  float2 xp[NT][QW][4][2];
-  float2 sx02[NT], sx13[NT];
   const int kb = xsl * G::kSlabK + sbl * 256 + 128 * h;   // the unit's 128-block
-  const uint32_t sxa = xs + static_cast<uint32_t>(L::bytes(static_cast<size_t>(NT) * p.kpad));
-  const int parts = p.kpad / G::kPart;
   const uint32_t xrun = xs + L::addr(kb + 4 * l0);   // the unit's x run (token 0)
   const uint32_t xtok = static_cast<uint32_t>(L::bytes(static_cast<size_t>(p.kpad)));
-#pragma unroll
-  for (int k = 0; k < NT; ++k) {
-#pragma unroll
-    for (int j = 0; j < QW; ++j)
-#pragma unroll
-      for (int b = 0; b < 4; ++b)
-        x_quad<kQ6K, NT, XBF>(xrun + k * xtok + (16 * j + 4 * b) * L::kE, xp[k][j][b][0],
-                              xp[k][j][b][1]);
-    const float4 s4 =
-        lds_f4(sxa + 4 * (k * parts + (kb / 128) * (128 / G::kPart) + 4 * (l0 / G::kPart)));
-    sx02[k] = make_float2(s4.x, s4.y);
-    sx13[k] = make_float2(s4.z, s4.w);
-  }
-  const float2 m32 = make_float2(-32.0f, -32.0f);
+  // the rows' words: record base (4-byte aligned) and shift of each row
+  uint32_t rb[NR], rsh[NR];
+  uint32_t A[NR][QW], B[NR][QW], H[NR][QW];
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
     const int row = hw + 2 * WC * r;
-    // byte offset of the slab in its 16-byte aligned copy: (row start + slab
-    // start) mod 16, from the row stride mod 16
     const uint32_t ro =
         (static_cast<uint32_t>(tl.row0 + row) * ((210u * p.nsb) & 15u) + sl * G::kQBytes) & 15u;
     const uint32_t rec = st + row * p.slot + ro + 210 * sbl;
-    const uint32_t rb = rec & ~3u, rsh = (rec & 3u) * 8u;
-    uint32_t A[QW], B[QW], H[QW], S[2], D[1];
-    lds_words_rec<QW>(rb, rsh, 64 * h + l0, A);
-    lds_words_rec<QW>(rb, rsh, 64 * h + 32 + l0, B);
-    lds_words_rec<QW>(rb, rsh, 128 + 32 * h + l0, H);
-    lds_words_rec<2>(rb, rsh, 192 + 8 * h, S);
-    lds_words_rec<1>(rb, rsh, 208, D);
-    // scales of the unit's sub-blocks: t0 byte su, t1 su+2 (of S[0]), t2 su,
-    // t3 su+2 (of S[1]); sign-extended with a byte permute
-    const uint32_t sel0 = su | ((8 | su) << 4) | ((8 | su) << 8) | ((8 | su) << 12);
-    const uint32_t sel2 = (su + 2) | ((10 + su) << 4) | ((10 + su) << 8) | ((10 + su) << 12);
-    const float d = half_bits_to_float(D[0] & 0xFFFFu);
-    const float2 ds02 = make_float2(d * static_cast<float>(static_cast<int>(prmt(S[0], 0, sel0))),
-                                    d * static_cast<float>(static_cast<int>(prmt(S[1], 0, sel0))));
-    const float2 ds13 = make_float2(d * static_cast<float>(static_cast<int>(prmt(S[0], 0, sel2))),
-                                    d * static_cast<float>(static_cast<int>(prmt(S[1], 0, sel2))));
-    float2 a02[NT][2], a13[NT][2];
+    rb[r] = rec & ~3u;
+    rsh[r] = (rec & 3u) * 8u;
+    lds_words_rec<QW>(rb[r], rsh[r], 64 * h + l0, A[r]);
+    lds_words_rec<QW>(rb[r], rsh[r], 64 * h + 32 + l0, B[r]);
+    lds_words_rec<QW>(rb[r], rsh[r], 128 + 32 * h + l0, H[r]);
+  }
+  float2 a02[NR][NT], a13[NR][NT];
 #pragma unroll
-    for (int k = 0; k < NT; ++k) a02[k][0] = a02[k][1] = a13[k][0] = a13[k][1] = make_float2(0.0f, 0.0f);
-    const uint32_t M = 0x0F0F0F0Fu;
+  for (int r = 0; r < NR; ++r)
 #pragma unroll
-    for (int j = 0; j < QW; ++j) {
+    for (int k = 0; k < NT; ++k) a02[r][k] = a13[r][k] = make_float2(0.0f, 0.0f);
+  const uint32_t M = 0x0F0F0F0Fu;
+#pragma unroll
+  for (int j = 0; j < QW; ++j) {
+    // x pairs of word j: xq[k][b][0] = (x_t0, x_t2), [1] = (x_t1, x_t3) of column 4j + b
+    float2 xq[NT][4][2];
+#pragma unroll
+    for (int k = 0; k < NT; ++k)
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        x_quad<kQ6K, NT, XBF>(xrun + k * xtok + (16 * j + 4 * b) * L::kE, xq[k][b][0], xq[k][b][1]);
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
       // 6-bit values of the four t-runs, one per byte (bits 6-7 are masked
       // off by the extraction masks)
-      const uint32_t q0 = bitsel(A[j], H[j] << 4, M);
-      const uint32_t q2 = bitsel(A[j] >> 4, H[j], M);
-      const uint32_t q1 = bitsel(B[j], H[j] << 2, M);
-      const uint32_t q3 = bitsel(B[j] >> 4, H[j] >> 2, M);
+      const uint32_t q0 = bitsel(A[r][j], H[r][j] << 4, M);
+      const uint32_t q2 = bitsel(A[r][j] >> 4, H[r][j], M);
+      const uint32_t q1 = bitsel(B[r][j], H[r][j] << 2, M);
+      const uint32_t q3 = bitsel(B[r][j] >> 4, H[r][j] >> 2, M);
       const uint32_t p02 = prmt(q0, q2, 0x0703u);   // byte 3 of q0 -> byte 0, of q2 -> byte 2
       const uint32_t p13 = prmt(q1, q3, 0x0703u);
       float2 c02[4], c13[4];
@@ -878,16 +862,41 @@ __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl
       for (int k = 0; k < NT; ++k)
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          a02[k][b & 1] = __ffma2_rn(c02[b], xp[k][j][b][0], a02[k][b & 1]);
-          a13[k][b & 1] = __ffma2_rn(c13[b], xp[k][j][b][1], a13[k][b & 1]);
+          a02[r][k] = __ffma2_rn(c02[b], xq[k][b][0], a02[r][k]);
+          a13[r][k] = __ffma2_rn(c13[b], xq[k][b][1], a13[r][k]);
         }
     }
+  }
+  // sums of x over the unit's four t-runs, then the scales and q - 32
+  const uint32_t sxa = xs + static_cast<uint32_t>(L::bytes(static_cast<size_t>(NT) * p.kpad));
+  const int parts = p.kpad / G::kPart;
+  float2 sx02[NT], sx13[NT];
+#pragma unroll
+  for (int k = 0; k < NT; ++k) {
+    const float4 s4 =
+        lds_f4(sxa + 4 * (k * parts + (kb / 128) * (128 / G::kPart) + 4 * (l0 / G::kPart)));
+    sx02[k] = make_float2(s4.x, s4.y);
+    sx13[k] = make_float2(s4.z, s4.w);
+  }
+  const float2 m32 = make_float2(-32.0f, -32.0f);
+  // scales of the unit's sub-blocks: t0 byte su, t1 su+2 (of S[0]), t2 su,
+  // t3 su+2 (of S[1]); sign-extended with a byte permute
+  const uint32_t sel0 = su | ((8 | su) << 4) | ((8 | su) << 8) | ((8 | su) << 12);
+  const uint32_t sel2 = (su + 2) | ((10 + su) << 4) | ((10 + su) << 8) | ((10 + su) << 12);
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    uint32_t S[2], D[1];
+    lds_words_rec<2>(rb[r], rsh[r], 192 + 8 * h, S);
+    lds_words_rec<1>(rb[r], rsh[r], 208, D);
+    const float d = half_bits_to_float(D[0] & 0xFFFFu);
+    const float2 ds02 = make_float2(d * static_cast<float>(static_cast<int>(prmt(S[0], 0, sel0))),
+                                    d * static_cast<float>(static_cast<int>(prmt(S[1], 0, sel0))));
+    const float2 ds13 = make_float2(d * static_cast<float>(static_cast<int>(prmt(S[0], 0, sel2))),
+                                    d * static_cast<float>(static_cast<int>(prmt(S[1], 0, sel2))));
 #pragma unroll
     for (int k = 0; k < NT; ++k) {
-      const float2 s02 = __ffma2_rn(m32, sx02[k], __fadd2_rn(a02[k][0], a02[k][1]));
-      const float2 s13 = __ffma2_rn(m32, sx13[k], __fadd2_rn(a13[k][0], a13[k][1]));
-      acc[r][k] = __ffma2_rn(ds02, s02, acc[r][k]);
-      acc[r][k] = __ffma2_rn(ds13, s13, acc[r][k]);
+      acc[r][k] = __ffma2_rn(ds02, __ffma2_rn(m32, sx02[k], a02[r][k]), acc[r][k]);
+      acc[r][k] = __ffma2_rn(ds13, __ffma2_rn(m32, sx13[k], a13[r][k]), acc[r][k]);
     }
   }
 }
@@ -1887,10 +1896,11 @@ template <int F, int NT>
 bool launch_nt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
                ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
   const DevInfo& di = dev_info();
-  // Rows per thread: 4, or 2 for small matrices (fewer than 16 rows per SM)
-  // and at n_tok 4 (whose x values take twice the registers).  Consumer warps
-  // per CTA: 8 for the Q4 family at n_tok 1, 2 on large matrices (two CTAs
-  // per SM: more warps to hide latency), else 4 (three CTAs per SM).
+  // Small matrices (fewer than 16 rows per SM) and n_tok 4 (whose x values
+  // take twice the registers): 4 consumer warps x 2 rows per thread.  Large
+  // matrices at n_tok 1, 2: 4 rows per thread, with 8 consumer warps for the
+  // Q4 family (two CTAs per SM: more warps to hide latency) and 4 for Q6_K
+  // (three CTAs per SM; measured faster than eight warps for its records).
   int64_t rows = 0;
   for (int i = 0; i < g.count; ++i) rows += g.N[i];
   if (NT == 4 || rows < 16LL * di.sms) return launch_rt<F, NT, 2, 4>(g, x, K, n_tok, s, src, st);
