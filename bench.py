@@ -45,7 +45,7 @@ WORKLOAD = "decode_step_52L_h5120_i32768_q4k_q6k_lmhead200000"
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--n-tok", type=int, default=1)
     p.add_argument("--impl", default="kq", choices=["kq", "reference"])
@@ -113,7 +113,7 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -128,7 +128,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
@@ -219,17 +219,16 @@ def build_step(pools_dev, n_tok, layers, device):
     h = wl.LM_HEAD
     head = (h.fmt, wl.tile_matrix_device(pools_dev[h.fmt], h.fmt, wl.derive_seed(5, 999), h.N, h.K), h.N, h.K)
     step = DecodeStep(Ls, head, n_tok, device=device)
-    host_x = []
+    # the step's activation inputs, in the order of step.x_all (layer by layer:
+    # x_attn, x_o, x_ffn, x_down; then the head), in one pinned host buffer
+    parts = []
     for l in range(layers):
         for j, key in enumerate(("x_attn", "x_o", "x_ffn", "x_down")):
-            xb = wl.activations_bf16(wl.derive_seed(5, l, 100 + j), n_tok, step.x[l][key].shape[1])
-            t = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
-            step.x[l][key].copy_(t)
-            host_x.append((t, step.x[l][key]))
-    xb = wl.activations_bf16(wl.derive_seed(5, 998), n_tok, h.K)
-    t = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
-    step.x_head.copy_(t)
-    host_x.append((t, step.x_head))
+            parts.append(wl.activations_bf16(wl.derive_seed(5, l, 100 + j), n_tok, step.x[l][key].shape[1]))
+    parts.append(wl.activations_bf16(wl.derive_seed(5, 998), n_tok, h.K))
+    flat = np.concatenate([p_.reshape(-1) for p_ in parts])
+    host_x = torch.from_numpy(flat.view(np.int16)).view(torch.bfloat16).pin_memory()
+    step.x_all.copy_(host_x)
     torch.cuda.synchronize()
     return step, host_x
 
@@ -399,10 +398,24 @@ def run_kq(args):
                 s8.x[l][key].copy_(torch.from_numpy(xb8.view(np.int16)).view(torch.bfloat16))
         g8 = s8.capture(stream)
         t8 = max_over_ranks(dist, time_graph(g8, stream, args.steps, 3, dist))
+        del g8, s8
+        # the CUDA-core path at this width: two 4-token passes over the same
+        # weights (what the library falls back to without the tensor-core
+        # kernel), i.e. twice the n_tok = 4 step
+        s4 = type(step)(step.layers, step.lm_head, 4, device=device)
+        for l in range(args.layers):
+            for j, key in enumerate(("x_attn", "x_o", "x_ffn", "x_down")):
+                xb4 = wl.activations_bf16(wl.derive_seed(5, l, 200 + j), 4, s4.x[l][key].shape[1])
+                s4.x[l][key].copy_(torch.from_numpy(xb4.view(np.int16)).view(torch.bfloat16))
+        g4 = s4.capture(stream)
+        t4 = max_over_ranks(dist, time_graph(g4, stream, max(10, args.steps // 4), 3, dist))
+        del g4, s4
         extra["n_tok_8"] = {"ms_per_step": t8 * 1e3, "weight_gb_s": wbytes / t8 / 1e9 * world,
                             "pct_of_hbm_peak": 100 * wbytes / t8 / 1e9 / hbm,
-                            "tok_per_s": 8 / t8 * world}
-        del g8, s8
+                            "tok_per_s": 8 / t8 * world, "path": "tensor cores (mma.sync bf16)",
+                            "cuda_core_ms_per_step": 2 * t4 * 1e3,
+                            "cuda_core_path": "two n_tok=4 passes (CUDA cores)",
+                            "n_tok_4_ms_per_step": t4 * 1e3}
 
     # dominant kernel: grouped gate/up Q4_K GEMV launches
     dur, kbytes, kname = dominant_kernel_timing(step, args.steps, 3, stream)
@@ -413,13 +426,13 @@ def run_kq(args):
     e2e = None
     if not args.no_extra:
         y_host = torch.empty(step.y_head.shape, dtype=torch.float32).pin_memory()
-        h2d = sum(t.numel() * 2 for t, _ in host_x)
+        h2d = host_x.numel() * 2
         d2h = y_host.numel() * 4
 
         def e2e_step():
+            # one H2D copy of every activation input, the graph, the logits
             with torch.cuda.stream(stream):
-                for h, d in host_x:
-                    d.copy_(h, non_blocking=True)
+                step.x_all.copy_(host_x, non_blocking=True)
                 g.replay()
                 y_host.copy_(step.y_head, non_blocking=True)
             stream.synchronize()

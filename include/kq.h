@@ -109,7 +109,14 @@ size_t kq_matrix_bytes(kq_format f, int64_t N_out, int64_t K);
  *   x_bf16   : device, bf16 [n_tok][K], 16-B aligned
  *   y        : device, fp32 [n_tok][N_out], overwritten
  * Accumulates in fp32.  Source: the daily.dev ExecuTorch summary, answer on
- * exporting GGUF checkpoints (Q4_K/Q5_K/Q6_K GEMV; group-128 merge). */
+ * exporting GGUF checkpoints (Q4_K/Q5_K/Q6_K GEMV; group-128 merge).
+ * Long rows are split over several CTAs whose partial sums go to a split-K
+ * scratch buffer of the current device, allocated by the library on first
+ * need (never while the stream is being captured; a capture then runs the
+ * unsplit configuration) and grown by allocating a larger one; buffers are
+ * never freed, so CUDA graphs captured earlier stay valid.  The buffer is
+ * shared by all calls on a device: calls that overlap on the GPU (different
+ * streams, no ordering between them) race on it. */
 kq_status kq_gemv(kq_format f, const void* W_blocks, const void* x_bf16,
                   float* y, int64_t N_out, int64_t K, int n_tok,
                   kq_stream_t stream);

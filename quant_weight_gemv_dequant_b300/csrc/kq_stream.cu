@@ -346,20 +346,31 @@ __device__ void stage_x_q4(const Params& p, uint8_t* smem, int kbase) {
   float* sx = reinterpret_cast<float*>(smem + L::bytes(static_cast<size_t>(NT) * p.kpad));
   const int lane = threadIdx.x & 31;
   // trip count uniform per warp (the part sums are reduced with shuffles over
-  // GP consecutive lanes; total and groups_per_tok are multiples of 8)
-  for (int base = static_cast<int>(threadIdx.x) & ~31; base < total; base += blockDim.x) {
-    const int q = base + lane;
+  // GP consecutive lanes; total and groups_per_tok are multiples of 8); the
+  // loads of four items are in flight together
+  constexpr int U = 4;
+  for (int base0 = static_cast<int>(threadIdx.x) & ~31; base0 < total;
+       base0 += U * static_cast<int>(blockDim.x)) {
+    uint2 rlu[U], rhu[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int q = base0 + u * static_cast<int>(blockDim.x) + lane;
+      const int tk = q / groups_per_tok, gi = q % groups_per_tok;
+      const int k = (gi >> 3) * 64 + 4 * (gi & 7);
+      rlu[u] = rhu[u] = make_uint2(0, 0);
+      if (q < total && tk < p.nt && kbase + k < p.K) {
+        const uint16_t* xt = p.x + static_cast<int64_t>(tk) * p.K + kbase + k;
+        rlu[u] = *reinterpret_cast<const uint2*>(xt);
+        rhu[u] = *reinterpret_cast<const uint2*>(xt + 32);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+    const int q = base0 + u * static_cast<int>(blockDim.x) + lane;
     const bool in = q < total;
     const int tk = q / groups_per_tok, gi = q % groups_per_tok;
     const int blk = gi >> 3, i = gi & 7;
-    const int k = blk * 64 + 4 * i;   // low positions k..k+3, high k+32..k+35
-    const bool live = in && tk < p.nt && kbase + k < p.K;
-    uint2 rl = make_uint2(0, 0), rh = make_uint2(0, 0);
-    if (live) {
-      const uint16_t* xt = p.x + static_cast<int64_t>(tk) * p.K + kbase + k;
-      rl = *reinterpret_cast<const uint2*>(xt);
-      rh = *reinterpret_cast<const uint2*>(xt + 32);
-    }
+    const uint2 rl = rlu[u], rh = rhu[u];
     float v[8];   // staged order: (lo b, hi b) for b = 0..3
     v[0] = __uint_as_float(rl.x << 16);
     v[2] = __uint_as_float(rl.x & 0xFFFF0000u);
@@ -402,6 +413,7 @@ __device__ void stage_x_q4(const Params& p, uint8_t* smem, int kbase) {
       o[0] = slo;
       o[1] = shi;
     }
+    }
   }
 }
 
@@ -424,20 +436,32 @@ __device__ void stage_x_q6(const Params& p, uint8_t* smem, int kbase) {
   float* sx = reinterpret_cast<float*>(smem + L::bytes(static_cast<size_t>(NT) * p.kpad));
   const int lane = threadIdx.x & 31;
   // trip count uniform per warp (part sums are reduced with shuffles over GP
-  // consecutive lanes; total and groups_per_tok are multiples of 8)
-  for (int base = static_cast<int>(threadIdx.x) & ~31; base < total; base += blockDim.x) {
-    const int q = base + lane;
+  // consecutive lanes; total and groups_per_tok are multiples of 8); the
+  // loads of two items are in flight together
+  constexpr int U = 2;
+  for (int base0 = static_cast<int>(threadIdx.x) & ~31; base0 < total;
+       base0 += U * static_cast<int>(blockDim.x)) {
+    uint2 ru[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int q = base0 + u * static_cast<int>(blockDim.x) + lane;
+      const int tk = q / groups_per_tok, gi = q % groups_per_tok;
+      const int k = (gi >> 3) * 128 + 4 * (gi & 7);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) ru[u][t] = make_uint2(0, 0);
+      if (q < total && tk < p.nt && kbase + k < p.K) {
+        const uint16_t* xt = p.x + static_cast<int64_t>(tk) * p.K + kbase + k;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) ru[u][t] = *reinterpret_cast<const uint2*>(xt + 32 * t);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+    const int q = base0 + u * static_cast<int>(blockDim.x) + lane;
     const bool in = q < total;
     const int tk = q / groups_per_tok, gi = q % groups_per_tok;
     const int blk = gi >> 3, j = gi & 7;
-    const int k = blk * 128 + 4 * j;   // positions k + 32t .. k + 32t + 3
-    const bool live = in && tk < p.nt && kbase + k < p.K;
-    uint2 r[4] = {};
-    if (live) {
-      const uint16_t* xt = p.x + static_cast<int64_t>(tk) * p.K + kbase + k;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) r[t] = *reinterpret_cast<const uint2*>(xt + 32 * t);
-    }
+    const uint2 (&r)[4] = ru[u];
     float v[4][4];   // [t][b]
     float sum[4];
 #pragma unroll
@@ -481,6 +505,7 @@ __device__ void stage_x_q6(const Params& p, uint8_t* smem, int kbase) {
     if (j % GP == 0) {
       float* sp = sx + tk * parts_per_tok + blk * (128 / P) + 4 * (j / GP);
       *reinterpret_cast<float4*>(sp) = make_float4(sum[0], sum[2], sum[1], sum[3]);
+    }
     }
   }
 }
@@ -1056,10 +1081,14 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
               for (int k = 0; k < NT; ++k) __stcg(part + kseg * seg_stride + row * NT + k, red[r][k]);
             }
           }
-          __threadfence();
         }
+        // the consumer barrier orders every warp's stores before thread 0's
+        // fence, which makes them visible device-wide before its arrival
         asm volatile("bar.sync 1, %0;" ::"r"(WC * 32) : "memory");
-        if (threadIdx.x == 0) last_flag = atomicAdd(p.arrivals + t, 1u) == static_cast<unsigned>(p.ksplit - 1);
+        if (threadIdx.x == 0) {
+          __threadfence();
+          last_flag = atomicAdd(p.arrivals + t, 1u) == static_cast<unsigned>(p.ksplit - 1);
+        }
         asm volatile("bar.sync 1, %0;" ::"r"(WC * 32) : "memory");
         if (last_flag) {
           __threadfence();
@@ -1531,9 +1560,13 @@ __global__ void __launch_bounds__((WC + 1) * 32, 1)
               __stcg(q + 1, acc[nb][h].y);
             }
           }
-        __threadfence();
+        // the consumer barrier orders every warp's stores before thread 0's
+        // fence, which makes them visible device-wide before its arrival
         asm volatile("bar.sync 1, %0;" ::"r"(WC * 32) : "memory");
-        if (threadIdx.x == 0) last_flag = atomicAdd(p.arrivals + tix, 1u) == static_cast<unsigned>(p.ksplit - 1);
+        if (threadIdx.x == 0) {
+          __threadfence();
+          last_flag = atomicAdd(p.arrivals + tix, 1u) == static_cast<unsigned>(p.ksplit - 1);
+        }
         asm volatile("bar.sync 1, %0;" ::"r"(WC * 32) : "memory");
         if (last_flag) {
           __threadfence();
@@ -1587,11 +1620,13 @@ DevInfo& dev_info() {
 constexpr size_t kStaticSmem = 256;   // the kernel's static shared memory (barriers, flag), rounded up
 
 // Split-K scratch of the current device: a fixed region of kMaxTiles arrival
-// counters, then the partial sums.  The counter region never moves or
-// shrinks, so counters stay zero across launches of any shape (partial sums
-// of one launch never land on another launch's counters).  Grown on demand
+// counters, then the partial sums.  The counter region never moves within a
+// buffer, so counters stay zero across launches of any shape (partial sums of
+// one launch never land on another launch's counters).  Grown on demand
 // (never while the stream is being captured), zero-filled when allocated;
-// kernels leave every counter they use at zero when they finish.
+// kernels leave every counter they use at zero when they finish.  A grown
+// buffer replaces the current one for new launches, but the old one is never
+// freed: CUDA graphs captured earlier keep using it, so they stay valid.
 constexpr int kMaxTiles = 1 << 16;
 constexpr size_t kCounterBytes = size_t{kMaxTiles} * sizeof(unsigned int);
 struct Scratch {
@@ -1612,17 +1647,16 @@ void* scratch_get(size_t bytes, cudaStream_t s) {
     (void)cudaGetLastError();
     return nullptr;
   }
-  size_t want = bytes < (size_t{1} << 20) ? (size_t{1} << 20) : bytes;
+  // at least 16 MB, and at least twice the previous size, so growth is rare
+  size_t want = bytes < (size_t{16} << 20) ? (size_t{16} << 20) : bytes;
+  if (want < 2 * sc.bytes) want = 2 * sc.bytes;
   void* p = nullptr;
-  if (sc.base != nullptr) cudaFree(sc.base);   // synchronises with work using it
-  sc.base = nullptr;
-  sc.bytes = 0;
   if (cudaMalloc(&p, want) != cudaSuccess || cudaMemset(p, 0, want) != cudaSuccess) {
     (void)cudaGetLastError();
     if (p != nullptr) cudaFree(p);
     return nullptr;
   }
-  sc.base = p;
+  sc.base = p;   // the previous buffer stays allocated (see above)
   sc.bytes = want;
   return p;
 }

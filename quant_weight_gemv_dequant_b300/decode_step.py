@@ -30,13 +30,19 @@ class DecodeStep:
         self.lm_head = lm_head
         self.x, self.y = [], []
         self._structs = []
-        for L in layers:
-            xs = {
-                "x_attn": torch.zeros((n_tok, L["q"][3]), dtype=torch.bfloat16, device=device),
-                "x_o": torch.zeros((n_tok, L["o"][3]), dtype=torch.bfloat16, device=device),
-                "x_ffn": torch.zeros((n_tok, L["gate"][3]), dtype=torch.bfloat16, device=device),
-                "x_down": torch.zeros((n_tok, L["down"][3]), dtype=torch.bfloat16, device=device),
-            }
+        # every activation input of the step is a view into one contiguous
+        # bf16 buffer (x_all), so a caller fills all of them with one copy;
+        # each view starts on a 16-byte boundary (K is a multiple of 256)
+        widths = [L[n][3] for L in layers for n in ("q", "o", "gate", "down")]
+        if lm_head is not None:
+            widths.append(lm_head[3])
+        self.x_all = torch.zeros(n_tok * sum(widths), dtype=torch.bfloat16, device=device)
+        views, off = [], 0
+        for w in widths:
+            views.append(self.x_all[off:off + n_tok * w].view(n_tok, w))
+            off += n_tok * w
+        for li, L in enumerate(layers):
+            xs = dict(zip(("x_attn", "x_o", "x_ffn", "x_down"), views[4 * li:4 * li + 4]))
             ys = {n: torch.empty((n_tok, L[n][2]), dtype=torch.float32, device=device)
                   for n in LAYER_NAMES}
             layer = kq_layer(*[make_matrix(L[n][0], L[n][1], L[n][2], L[n][3]) for n in LAYER_NAMES])
@@ -46,7 +52,7 @@ class DecodeStep:
             self.y.append(ys)
             self._structs.append((layer, io))
         if lm_head is not None:
-            self.x_head = torch.zeros((n_tok, lm_head[3]), dtype=torch.bfloat16, device=device)
+            self.x_head = views[-1]
             self.y_head = torch.empty((n_tok, lm_head[2]), dtype=torch.float32, device=device)
         self.graph = None
 

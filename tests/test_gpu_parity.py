@@ -299,3 +299,38 @@ def test_whole_decode_step_graph(kq, oracle, pools, n_tok):
     sub = wl.tiled_rows(pools[h.fmt], h.fmt, hs, h.N, h.K, rows)
     yref, A = oracle.gemv(h.fmt, sub, len(rows), h.K, xh)
     assert_parity(step.y_head.cpu().numpy()[:, rows], yref, A, "lm_head")
+
+
+def test_graph_survives_scratch_growth(kq, oracle, pools):
+    """A captured launch that splits K keeps its split-K scratch: after a
+    later, larger split-K request makes the library allocate a bigger
+    buffer, replaying the earlier graph still gives the right result."""
+    fmt, N, K, T = 2, 600, 32768, 1
+    Wb = weights(oracle, fmt, N, K, wl.derive_seed(131))
+    x = wl.activations_bf16(wl.derive_seed(132), T, K)
+    W, xd = dev(Wb), dev_x(x)
+    y = torch.empty((T, N), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    kq.kq_gemv(fmt, W, xd, y, N, K, T, s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        kq.kq_gemv(fmt, W, xd, y, N, K, T, s)
+    # 20000 x 32768 Q6_K at 16 tokens: about 20 MB of partial sums, more than
+    # the scratch held so far
+    Nb, Tb, sb = 20000, 16, wl.derive_seed(133)
+    big = wl.tile_matrix_device(dev(pools[fmt]), fmt, sb, Nb, K)
+    xb = wl.activations_bf16(wl.derive_seed(134), Tb, K)
+    yb = torch.full((Tb, Nb), CANARY, dtype=torch.float32, device="cuda")
+    kq.kq_gemv(fmt, big, dev_x(xb), yb, Nb, K, Tb, s)
+    torch.cuda.synchronize()
+    y.fill_(CANARY)
+    g.replay()
+    torch.cuda.synchronize()
+    assert kq.kq_device_status() == 0
+    yref, A = oracle.gemv(fmt, Wb, N, K, x)
+    assert_parity(y.cpu().numpy(), yref, A, "graph replay after scratch growth")
+    rows = _sample_rows(Nb, 16, sb)
+    sub = wl.tiled_rows(pools[fmt], fmt, sb, Nb, K, rows)
+    yref, A = oracle.gemv(fmt, sub, len(rows), K, xb)
+    assert_parity(yb.cpu().numpy()[:, rows], yref, A, "large split-K request")
