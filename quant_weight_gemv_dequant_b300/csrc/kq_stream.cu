@@ -718,13 +718,7 @@ __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl
       if constexpr (F == kQ5K) lds_words<NW>(rec[r] + 16 + off, hq[r]);
     }
   }
-  float2 A[NR][NT][CH];
-#pragma unroll
-  for (int r = 0; r < NR; ++r)
-#pragma unroll
-    for (int k = 0; k < NT; ++k)
-#pragma unroll
-      for (int h = 0; h < CH; ++h) A[r][k][h] = make_float2(0.0f, 0.0f);
+  float2 A[NR][NT][CH];   // set by the first word's products
   const int rlo = (2 * c + 28) & 31, rhi = (2 * c + 29) & 31;   // Q5_K: bit 2c(+1) -> bit 4
 #pragma unroll
   for (int i = 0; i < NW; ++i) {
@@ -764,7 +758,8 @@ __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl
       for (int k = 0; k < NT; ++k)
 #pragma unroll
         for (int b = 0; b < 4; ++b)
-          A[r][k][b % CH] = __ffma2_rn(q[b], xq[k][b], A[r][k][b % CH]);
+          A[r][k][b % CH] = (i == 0 && b < CH) ? __fmul2_rn(q[b], xq[k][b])
+                                               : __ffma2_rn(q[b], xq[k][b], A[r][k][b % CH]);
     }
   }
   // scales, then the stage's contribution
@@ -976,14 +971,23 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
   stage_x<F, NT, XBF>(p, smem, kseg * p.kpad);
   __syncthreads();
   if (producer) {
+    // ring position, empty-barrier parity and (tile, slab) of stage `first`,
+    // advanced by counting (no division per stage)
+    int slot = 0, xsl = first % p.slabs, tn = first / p.slabs;
+    uint32_t parity = 0;
     for (int it = first; it < total; ++it) {
-      const int slot = it % stages;
-      const uint32_t use = static_cast<uint32_t>(it / stages);
-      if (!mbar_wait_warp(bar_empty + 8 * slot, (use - 1) & 1)) return;
+      if (!mbar_wait_warp(bar_empty + 8 * slot, parity)) return;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      const Tile tl = tile_of(p, cta + (it / p.slabs) * cps);
-      issue_stage<G>(p, smem, ring_a + slot * p.stage, bar_full + 8 * slot, tl,
-                     sl0 + it % p.slabs);
+      const Tile tl = tile_of(p, cta + tn * cps);
+      issue_stage<G>(p, smem, ring_a + slot * p.stage, bar_full + 8 * slot, tl, sl0 + xsl);
+      if (++xsl == p.slabs) {
+        xsl = 0;
+        ++tn;
+      }
+      if (++slot == stages) {
+        slot = 0;
+        parity ^= 1u;
+      }
     }
     return;
   }
@@ -999,20 +1003,21 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
   float2 acc[RT][NT];
   Tile tl{};
   int t = 0;
+  // slab within the segment, tile count, ring slot and full-barrier parity,
+  // advanced by counting (no division per stage)
+  int xsl = 0, tn = 0, slot = 0;
+  uint32_t parity = 0;
   for (int it = 0; it < total; ++it) {
-    const int xsl = it % p.slabs;   // slab within the segment
     const int sl = sl0 + xsl;       // slab within the row
     if (xsl == 0) {
-      t = cta + (it / p.slabs) * cps;
+      t = cta + tn * cps;
       tl = tile_of(p, t);
 #pragma unroll
       for (int r = 0; r < RT; ++r)
 #pragma unroll
         for (int k = 0; k < NT; ++k) acc[r][k] = make_float2(0.0f, 0.0f);
     }
-    const int slot = it % stages;
-    const uint32_t use = static_cast<uint32_t>(it / stages);
-    if (!mbar_wait_warp(bar_full + 8 * slot, use & 1)) return;
+    if (!mbar_wait_warp(bar_full + 8 * slot, parity)) return;
     const uint32_t st = ring_a + slot * p.stage;
     if (sl * G::kSlabSB + sbl < p.nsb) {
       // rows of this half-warp inside the tile (the same for all its lanes)
@@ -1109,6 +1114,14 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
           if (threadIdx.x == 0) p.arrivals[t] = 0u;
         }
       }
+    }
+    if (++xsl == p.slabs) {
+      xsl = 0;
+      ++tn;
+    }
+    if (++slot == stages) {
+      slot = 0;
+      parity ^= 1u;
     }
   }
 }
@@ -1491,13 +1504,23 @@ __global__ void __launch_bounds__((WC + 1) * 32, 1)
   }
   __syncthreads();
   if (warp == WC) {
+    // ring position, empty-barrier parity and (tile, slab) of stage `first`,
+    // advanced by counting (no division per stage)
+    int slot = 0, xsl = first % p.slabs, tn = first / p.slabs;
+    uint32_t parity = 0;
     for (int it = first; it < total; ++it) {
-      const int slot = it % stages;
-      const uint32_t use = static_cast<uint32_t>(it / stages);
-      if (!mbar_wait_warp(bar_empty + 8 * slot, (use - 1) & 1)) return;
+      if (!mbar_wait_warp(bar_empty + 8 * slot, parity)) return;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      const Tile tl = tile_of(p, cta + (it / p.slabs) * cps);
-      issue_stage<G>(p, smem, ring_a + slot * p.stage, bar_full + 8 * slot, tl, sl0 + it % p.slabs);
+      const Tile tl = tile_of(p, cta + tn * cps);
+      issue_stage<G>(p, smem, ring_a + slot * p.stage, bar_full + 8 * slot, tl, sl0 + xsl);
+      if (++xsl == p.slabs) {
+        xsl = 0;
+        ++tn;
+      }
+      if (++slot == stages) {
+        slot = 0;
+        parity ^= 1u;
+      }
     }
     return;
   }
@@ -1507,18 +1530,17 @@ __global__ void __launch_bounds__((WC + 1) * 32, 1)
   float2 acc[NB][2];
   Tile tl{};
   int tix = 0;
+  int xsl = 0, tn = 0, slot = 0;   // advanced by counting (no division per stage)
+  uint32_t parity = 0;
   for (int it = 0; it < total; ++it) {
-    const int xsl = it % p.slabs;
     const int sl = sl0 + xsl;
     if (xsl == 0) {
-      tix = cta + (it / p.slabs) * cps;
+      tix = cta + tn * cps;
       tl = tile_of(p, tix);
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = make_float2(0.0f, 0.0f);
     }
-    const int slot = it % stages;
-    const uint32_t use = static_cast<uint32_t>(it / stages);
-    if (!mbar_wait_warp(bar_full + 8 * slot, use & 1)) return;
+    if (!mbar_wait_warp(bar_full + 8 * slot, parity)) return;
     const uint32_t st = ring_a + slot * p.stage;
     if (rbase < tl.rcnt) {   // warp-uniform
       build_scale_table<G>(p, tl, sl, st, rbase, tab);
@@ -1588,6 +1610,14 @@ __global__ void __launch_bounds__((WC + 1) * 32, 1)
           if (threadIdx.x == 0) p.arrivals[tix] = 0u;
         }
       }
+    }
+    if (++xsl == p.slabs) {
+      xsl = 0;
+      ++tn;
+    }
+    if (++slot == stages) {
+      slot = 0;
+      parity ^= 1u;
     }
   }
 }
