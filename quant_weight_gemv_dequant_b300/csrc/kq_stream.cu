@@ -643,6 +643,58 @@ __device__ __forceinline__ float2 cvt_pair(uint32_t a, uint32_t b, uint32_t magi
 }
 constexpr uint64_t kNegMagic2 = 0xCB000000CB000000ull;   // (-2^23, -2^23)
 
+// The same on 64-bit register pairs: a .b64 operand of the packed f32x2
+// instructions is one aligned register pair by construction, so the hot loop
+// never needs moves to form pairs.
+template <uint32_t MA, uint32_t MB>
+__device__ __forceinline__ uint64_t cvt_pair64(uint32_t a, uint32_t b, uint32_t magic,
+                                               uint64_t neg) {
+  uint64_t r;
+  asm("{\n\t.reg .b32 t0, t1;\n\t.reg .b64 p;\n\t"
+      "lop3.b32 t0, %1, %3, %5, 0xEA;\n\t"
+      "lop3.b32 t1, %2, %4, %5, 0xEA;\n\t"
+      "mov.b64 p, {t0, t1};\n\t"
+      "add.rn.f32x2 %0, p, %6;\n\t}"
+      : "=l"(r)
+      : "r"(a), "r"(b), "n"(MA), "n"(MB), "r"(magic), "l"(neg));
+  return r;
+}
+__device__ __forceinline__ void fma2u(uint64_t& d, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ uint64_t mul2u(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2u(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float2 u2f2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t pack2u(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+
+// x_quad on 64-bit register pairs
+template <bool XBF>
+__device__ __forceinline__ void x_quad64(uint32_t addr, uint64_t& a, uint64_t& b) {
+  if constexpr (XBF) {
+    const uint2 r = lds64(addr);
+    a = pack2u(r.x << 16, r.x & 0xFFFF0000u);
+    b = pack2u(r.y << 16, r.y & 0xFFFF0000u);
+  } else {
+    asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
+  }
+}
+
 // Per-lane constants of the 6-bit (sc, m) decode of Q4_K / Q5_K for the two
 // sub-blocks 2c and 2c+1 of the lane's chunk c (bytes j = 2c, 2c+1 of the
 // 12-byte field, words s0 = bytes 0-3, s1 = 4-7, s2 = 8-11 of the field).
@@ -718,22 +770,22 @@ __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl
       if constexpr (F == kQ5K) lds_words<NW>(rec[r] + 16 + off, hq[r]);
     }
   }
-  float2 A[NR][NT][CH];   // set by the first word's products
+  uint64_t A[NR][NT][CH];   // (lo, hi) pairs, set by the first word's products
   const int rlo = (2 * c + 28) & 31, rhi = (2 * c + 29) & 31;   // Q5_K: bit 2c(+1) -> bit 4
 #pragma unroll
   for (int i = 0; i < NW; ++i) {
     // x pairs of word i: xq[k][b] = (x_lo, x_hi) of byte b
-    float2 xq[NT][4];
+    uint64_t xq[NT][4];
 #pragma unroll
     for (int k = 0; k < NT; ++k) {
       const uint32_t a = xrun + k * xtok + 8 * i * L::kE;
-      x_quad<F, NT, XBF>(a, xq[k][0], xq[k][1]);
-      x_quad<F, NT, XBF>(a + 4 * L::kE, xq[k][2], xq[k][3]);
+      x_quad64<XBF>(a, xq[k][0], xq[k][1]);
+      x_quad64<XBF>(a + 4 * L::kE, xq[k][2], xq[k][3]);
     }
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
       const uint32_t v = w[r][i];
-      float2 q[4];
+      uint64_t q[4];
       if constexpr (F == kQ5K) {
         const uint32_t h = hq[r][i];
         // byte b of lo5 / hi5 = nibble | fifth bit << 4 (bits 5..7 are
@@ -741,25 +793,28 @@ __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl
         const uint32_t lo5 = bitsel(v, __funnelshift_r(h, h, rlo), 0x0F0F0F0Fu);
         const uint32_t hi5 = bitsel(v >> 4, __funnelshift_r(h, h, rhi), 0x0F0F0F0Fu);
         const uint32_t b3 = prmt(lo5, hi5, 0x0703u);   // lo5 byte 3 -> byte 0, hi5 byte 3 -> byte 2
-        q[0] = cvt_pair<0x1Fu, 0x1Fu>(lo5, hi5, magic, neg);
-        q[1] = cvt_pair<0x1F00u, 0x1F00u>(lo5, hi5, magic, neg);
-        q[2] = cvt_pair<0x1F0000u, 0x1F0000u>(lo5, hi5, magic, neg);
-        q[3] = cvt_pair<0x1Fu, 0x1F0000u>(b3, b3, magic, neg);
+        q[0] = cvt_pair64<0x1Fu, 0x1Fu>(lo5, hi5, magic, neg);
+        q[1] = cvt_pair64<0x1F00u, 0x1F00u>(lo5, hi5, magic, neg);
+        q[2] = cvt_pair64<0x1F0000u, 0x1F0000u>(lo5, hi5, magic, neg);
+        q[3] = cvt_pair64<0x1Fu, 0x1F0000u>(b3, b3, magic, neg);
       } else {
         // lo b0 s0, hi b0 s4, lo b1 s8, hi b1 s12, lo b2 s16 from v; from
         // v >> 12: hi b2 s8, lo b3 s12, hi b3 s16
         const uint32_t u = v >> 12;
-        q[0] = cvt_pair<0xFu, 0xF0u>(v, v, magic, neg);
-        q[1] = cvt_pair<0xF00u, 0xF000u>(v, v, magic, neg);
-        q[2] = cvt_pair<0xF0000u, 0xF00u>(v, u, magic, neg);
-        q[3] = cvt_pair<0xF000u, 0xF0000u>(u, u, magic, neg);
+        q[0] = cvt_pair64<0xFu, 0xF0u>(v, v, magic, neg);
+        q[1] = cvt_pair64<0xF00u, 0xF000u>(v, v, magic, neg);
+        q[2] = cvt_pair64<0xF0000u, 0xF00u>(v, u, magic, neg);
+        q[3] = cvt_pair64<0xF000u, 0xF0000u>(u, u, magic, neg);
       }
 #pragma unroll
       for (int k = 0; k < NT; ++k)
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
-          A[r][k][b % CH] = (i == 0 && b < CH) ? __fmul2_rn(q[b], xq[k][b])
-                                               : __ffma2_rn(q[b], xq[k][b], A[r][k][b % CH]);
+        for (int b = 0; b < 4; ++b) {
+          if (i == 0 && b < CH)
+            A[r][k][b % CH] = mul2u(q[b], xq[k][b]);
+          else
+            fma2u(A[r][k][b % CH], q[b], xq[k][b]);
+        }
     }
   }
   // scales, then the stage's contribution
@@ -796,7 +851,7 @@ __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl
     }
 #pragma unroll
     for (int k = 0; k < NT; ++k) {
-      const float2 S = CH == 2 ? __fadd2_rn(A[r][k][0], A[r][k][CH - 1]) : A[r][k][0];
+      const float2 S = u2f2(CH == 2 ? add2u(A[r][k][0], A[r][k][CH - 1]) : A[r][k][0]);
       acc[r][k] = __ffma2_rn(dsc, S, acc[r][k]);
       acc[r][k] = __ffma2_rn(ndm, sxp[k], acc[r][k]);
     }
