@@ -1496,7 +1496,7 @@ __device__ __forceinline__ void mma_stage_q6(const Params& p, const Tile& tl, in
 }
 
 template <int F, int NB, int WC>
-__global__ void __launch_bounds__((WC + 1) * 32, 1)
+__global__ void __launch_bounds__((WC + 1) * 32, WC <= 4 ? 2 : 1)
     gemv_mma(const __grid_constant__ Params p, int stages) {
   using G = MGeo<F, WC>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -2036,10 +2036,9 @@ bool launch_nt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStre
 // 8 or 16 token rows) and the weight ring.  K segments: among the divisors
 // of the slabs of a row (at most 16) whose x segment fits with two stages,
 // the fewest that give every resident CTA work.
-template <int F, int NB>
+template <int F, int NB, int WC>
 bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
                 ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
-  constexpr int WC = 8;
   constexpr int NTP = 8 * NB;
   using G = MGeo<F, WC>;
   const DevInfo& di = dev_info();
@@ -2185,11 +2184,20 @@ bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   }
 }
 
+// Consumer warps per CTA: 8 (one CTA per SM) for launches of 64 M weights
+// or more; 4 (two CTAs per SM, 64-row tiles) for smaller ones such as the
+// attention projections, where more, smaller tiles fill the GPU better.
 template <int F>
 bool launch_verify(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
                    ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
-  return n_tok <= 8 ? launch_mma<F, 1>(g, x, K, n_tok, s, src, st)
-                    : launch_mma<F, 2>(g, x, K, n_tok, s, src, st);
+  int64_t rows = 0;
+  for (int i = 0; i < g.count; ++i) rows += g.N[i];
+  const bool small = rows * K < (int64_t{64} << 20);
+  if (n_tok <= 8)
+    return small ? launch_mma<F, 1, 4>(g, x, K, n_tok, s, src, st)
+                 : launch_mma<F, 1, 8>(g, x, K, n_tok, s, src, st);
+  return small ? launch_mma<F, 2, 4>(g, x, K, n_tok, s, src, st)
+               : launch_mma<F, 2, 8>(g, x, K, n_tok, s, src, st);
 }
 
 }  // namespace
