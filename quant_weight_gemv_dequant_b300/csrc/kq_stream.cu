@@ -9,7 +9,9 @@
 // Structure.  The rows of the (grouped) matrices are cut into tiles of
 // 2 * kWC * RT rows; a tile is streamed in slabs of 16 "units" (a unit = kCW
 // weights of one row, kCW = 64 / NT).  One CTA = kWC consumer warps + 1
-// producer warp, persistent over its tiles:
+// producer warp, persistent over its tiles (a first fixed tile, then tiles
+// claimed from a per-K-segment counter, so CTAs that get more of the SM and
+// of the memory system take more tiles):
 //   * at start, all warps convert x (bf16) once into shared memory (fp32, or
 //     bf16 when fp32 would not fit) together with the sum of x over every
 //     sub-block part (for the min term), while the first stages' weights are
@@ -42,6 +44,14 @@
 namespace kq {
 
 __device__ unsigned int g_wait_timeouts = 0;
+
+// Dynamic tile scheduling of the streaming kernels.  Per K segment j:
+// g_sched[j] counts the tiles claimed past the fixed ones, g_sched[kMaxSegs
+// + j] the producers that found none left; the last of those re-arms both, so
+// they are zero between launches.  Launches touch them only after
+// griddepcontrol.wait, i.e. after the previous kernel on the stream is done.
+constexpr int kMaxSegs = 16;
+__device__ unsigned int g_sched[2 * kMaxSegs];
 
 namespace {
 
@@ -265,6 +275,7 @@ struct Params {
   uint32_t x_bytes;          // shared bytes of the staged x (+ part sums), 16-aligned
   float* part;               // split-K partial sums [ksplit][tiles][tile_rows][NT]
   unsigned int* arrivals;    // split-K per-tile arrival counters (left at zero)
+  int static_tiles;          // tiles a CTA takes without claiming: cta + i * cps, i < this
   int tma;                   // 1: a stage arrives as one tensor copy per plane
   uint32_t slot, pslot, pbase, stage;   // StageShape of the ring
   uint32_t tx;               // bytes the tensor copies of one stage deliver
@@ -986,17 +997,19 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
   __shared__ int last_flag;
+  __shared__ int stage_tile[kMaxStages];   // tile of each ring slot; -1: no more tiles
   const uint32_t bar_full = smem_addr(&bars[0]);
   const uint32_t bar_empty = smem_addr(&bars[kMaxStages]);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t xs = smem_addr(smem);
   const uint32_t ring_a = xs + p.x_bytes;
-  // CTA c works on K segment c % ksplit and on tiles c / ksplit + i * cps
+  // CTA c works on K segment c % ksplit: first on its fixed tiles
+  // c / ksplit + i * cps (i < static_tiles), then on tiles it claims from
+  // the segment's counter until none is left, so that CTAs which stream
+  // faster take more tiles
   const int kseg = static_cast<int>(blockIdx.x) % p.ksplit;
   const int cta = static_cast<int>(blockIdx.x) / p.ksplit;
   const int cps = static_cast<int>(gridDim.x) / p.ksplit;   // CTAs per segment
-  const int my_tiles = (p.tiles - cta + cps - 1) / cps;
-  const int total = my_tiles * p.slabs;   // stages of this CTA
   const int sl0 = kseg * p.slabs;         // first slab (of the row) of the segment
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -1007,18 +1020,39 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
   }
   __syncthreads();
   const bool producer = warp == WC;
-  const int first = total < stages ? total : stages;
   // Programmatic dependent launch: the next kernel on the stream may start
-  // its CTAs as SMs free up; it reads its activations and touches the
-  // split-K scratch only after its own griddepcontrol.wait, i.e. after this
-  // grid has completed.
+  // its CTAs as SMs free up; it reads its activations, the scheduler counters
+  // and the split-K scratch only after its own griddepcontrol.wait, i.e.
+  // after this grid has completed.
   asm volatile("griddepcontrol.launch_dependents;");
+  // Producer state: tile of the stage being issued, tiles taken, slab within
+  // the segment, ring slot, stages issued, parity of the empty wait (waited
+  // from the second lap of the ring on) and the claim made ahead.
+  int pt = 0, taken = 0, pxsl = 0, pslot = 0, issued = 0;
+  uint32_t epar = 1u;
+  unsigned int claim = 0u;
+  auto advance = [&]() {
+    if (++pxsl == p.slabs) pxsl = 0;
+    if (++pslot == stages) {
+      pslot = 0;
+      epar ^= 1u;
+    }
+    ++issued;
+  };
   if (producer) {
-    // weights do not depend on the previous kernel: the first ring of stages
-    // (no empty wait needed) streams while that kernel may still be running
-    for (int it = 0; it < first; ++it) {
-      const Tile tl = tile_of(p, cta + (it / p.slabs) * cps);
-      issue_stage<G>(p, smem, ring_a + it * p.stage, bar_full + 8 * it, tl, sl0 + it % p.slabs);
+    // weights do not depend on the previous kernel: the stages of the fixed
+    // tiles that fit the ring stream while that kernel may still be running
+    while (issued < stages) {
+      if (pxsl == 0) {
+        const int t = cta + taken * cps;
+        if (taken >= p.static_tiles || t >= p.tiles) break;
+        pt = t;
+        ++taken;
+      }
+      if (lane == 0) stage_tile[pslot] = pt;
+      issue_stage<G>(p, smem, ring_a + pslot * p.stage, bar_full + 8 * pslot, tile_of(p, pt),
+                     sl0 + pxsl);
+      advance();
     }
   }
   // x may be produced by the previous kernel: wait for it to complete
@@ -1026,25 +1060,47 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
   stage_x<F, NT, XBF>(p, smem, kseg * p.kpad);
   __syncthreads();
   if (producer) {
-    // ring position, empty-barrier parity and (tile, slab) of stage `first`,
-    // advanced by counting (no division per stage)
-    int slot = 0, xsl = first % p.slabs, tn = first / p.slabs;
-    uint32_t parity = 0;
-    for (int it = first; it < total; ++it) {
-      if (!mbar_wait_warp(bar_empty + 8 * slot, parity)) return;
+    const int dyn0 = p.static_tiles * cps;   // first claimed tile index
+    bool pending = false;
+    for (;;) {
+      if (pxsl == 0) {
+        int t = cta + taken * cps;
+        if (taken >= p.static_tiles || t >= p.tiles) {
+          if (!pending && lane == 0) claim = atomicAdd(&g_sched[kseg], 1u);
+          t = dyn0 + static_cast<int>(__shfl_sync(0xFFFFFFFFu, claim, 0));
+          pending = false;
+        }
+        ++taken;
+        if (t >= p.tiles) {
+          // nothing left: tell the consumers through the next slot, and let
+          // the segment's last producer re-arm its counters
+          if (issued >= stages && !mbar_wait_warp(bar_empty + 8 * pslot, epar)) return;
+          if (lane == 0) {
+            stage_tile[pslot] = -1;
+            if (atomicAdd(&g_sched[kMaxSegs + kseg], 1u) == static_cast<unsigned>(cps - 1)) {
+              g_sched[kseg] = 0u;
+              g_sched[kMaxSegs + kseg] = 0u;
+            }
+          }
+          if (!p.tma || lane == 0) mbar_arrive(bar_full + 8 * pslot);
+          return;
+        }
+        pt = t;
+      }
+      // the claim for the next tile goes out with the current tile's last
+      // stage, so its latency hides behind the next empty wait
+      if (pxsl == p.slabs - 1 && !pending &&
+          (taken >= p.static_tiles || cta + taken * cps >= p.tiles)) {
+        if (lane == 0) claim = atomicAdd(&g_sched[kseg], 1u);
+        pending = true;
+      }
+      if (issued >= stages && !mbar_wait_warp(bar_empty + 8 * pslot, epar)) return;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      const Tile tl = tile_of(p, cta + tn * cps);
-      issue_stage<G>(p, smem, ring_a + slot * p.stage, bar_full + 8 * slot, tl, sl0 + xsl);
-      if (++xsl == p.slabs) {
-        xsl = 0;
-        ++tn;
-      }
-      if (++slot == stages) {
-        slot = 0;
-        parity ^= 1u;
-      }
+      if (lane == 0) stage_tile[pslot] = pt;
+      issue_stage<G>(p, smem, ring_a + pslot * p.stage, bar_full + 8 * pslot, tile_of(p, pt),
+                     sl0 + pxsl);
+      advance();
     }
-    return;
   }
   // consumers
   constexpr int kCW = G::kCW;
@@ -1058,21 +1114,22 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
   float2 acc[RT][NT];
   Tile tl{};
   int t = 0;
-  // slab within the segment, tile count, ring slot and full-barrier parity,
-  // advanced by counting (no division per stage)
-  int xsl = 0, tn = 0, slot = 0;
+  // slab within the segment, ring slot and full-barrier parity, advanced by
+  // counting (no division per stage)
+  int xsl = 0, slot = 0;
   uint32_t parity = 0;
-  for (int it = 0; it < total; ++it) {
+  for (;;) {
     const int sl = sl0 + xsl;       // slab within the row
+    if (!mbar_wait_warp(bar_full + 8 * slot, parity)) return;
     if (xsl == 0) {
-      t = cta + tn * cps;
+      t = stage_tile[slot];
+      if (t < 0) return;
       tl = tile_of(p, t);
 #pragma unroll
       for (int r = 0; r < RT; ++r)
 #pragma unroll
         for (int k = 0; k < NT; ++k) acc[r][k] = make_float2(0.0f, 0.0f);
     }
-    if (!mbar_wait_warp(bar_full + 8 * slot, parity)) return;
     const uint32_t st = ring_a + slot * p.stage;
     if (sl * G::kSlabSB + sbl < p.nsb) {
       // rows of this half-warp inside the tile (the same for all its lanes)
@@ -1170,10 +1227,7 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
         }
       }
     }
-    if (++xsl == p.slabs) {
-      xsl = 0;
-      ++tn;
-    }
+    if (++xsl == p.slabs) xsl = 0;
     if (++slot == stages) {
       slot = 0;
       parity ^= 1u;
@@ -1911,6 +1965,10 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   int stages = static_cast<int>((pl.budget - p.x_bytes) / ss.bytes);
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < pl.stages) stages = pl.stages;
+  // fixed tiles per CTA: enough to fill the ring before the previous kernel
+  // has finished (claims wait for it); every further tile is claimed
+  p.static_tiles = (stages + p.slabs - 1) / p.slabs;
+  if (ksplit > kMaxSegs) return false;
   const size_t smem = p.x_bytes + static_cast<size_t>(stages) * ss.bytes;
   static size_t configured = 0;   // dynamic shared memory above 48 KB is opt-in
   if (smem > configured) {
@@ -2053,6 +2111,7 @@ bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   p.part = nullptr;
   p.arrivals = nullptr;
   p.tma = tma ? 1 : 0;
+  p.static_tiles = 0;   // the verify kernel keeps its fixed tile order
   p.slot = full.slot;
   p.pslot = full.pslot;
   p.pbase = full.pbase;
@@ -2313,6 +2372,10 @@ bool read_wait_timeouts(unsigned int* count, cudaStream_t s) {
       return false;
     Scratch& sc = scratch_of_device();
     if (sc.base != nullptr && cudaMemsetAsync(sc.base, 0, sc.bytes, s) != cudaSuccess) return false;
+    static const unsigned int zeros[2 * kMaxSegs] = {};
+    if (cudaMemcpyToSymbolAsync(g_sched, zeros, sizeof(zeros), 0, cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+      return false;
   }
   return cudaStreamSynchronize(s) == cudaSuccess;
 }
