@@ -50,7 +50,7 @@ __device__ unsigned int g_wait_timeouts = 0;
 // + j] the producers that found none left; the last of those re-arms both, so
 // they are zero between launches.  Launches touch them only after
 // griddepcontrol.wait, i.e. after the previous kernel on the stream is done.
-constexpr int kMaxSegs = 16;
+constexpr int kMaxSegs = 32;
 __device__ unsigned int g_sched[2 * kMaxSegs];
 
 namespace {
@@ -609,6 +609,116 @@ __device__ __forceinline__ void issue_stage(const Params& p, uint8_t* smem, uint
   mbar_arrive_tx(full, tx);   // every producer lane arrives (count 32)
 }
 
+// ------------------------------------------------------------- producer
+//
+// The producer warp's stage sequence: the slabs of the CTA's tiles in order.
+// Its tiles are the fixed ones cta + i * cps (i < static_tiles), then tiles
+// claimed from the K segment's counter (one claim ahead, sent with the
+// current tile's last stage so its latency hides behind the next empty
+// wait).  stage_tile[slot] tells the consumers the tile of a slot; -1 ends
+// their loop.  Claims are made only after griddepcontrol.wait (the previous
+// kernel may still be using the counters before it).
+struct Ring {
+  int pt = 0;        // tile of the stage being issued
+  int taken = 0;     // tiles taken so far
+  int xsl = 0;       // slab within the segment
+  int slot = 0;      // ring slot
+  int issued = 0;    // stages issued
+  uint32_t epar = 1u;   // parity of the empty wait (waited from the second lap on)
+  unsigned int claim = 0u;
+  bool pending = false;
+  __device__ __forceinline__ void advance(int slabs, int stages) {
+    if (++xsl == slabs) xsl = 0;
+    if (++slot == stages) {
+      slot = 0;
+      epar ^= 1u;
+    }
+    ++issued;
+  }
+};
+
+// Before griddepcontrol.wait: the stages of the fixed tiles that fit the ring.
+template <class G>
+__device__ __forceinline__ void produce_prefill(const Params& p, uint8_t* smem, uint32_t ring_a,
+                                                uint32_t bar_full, int* stage_tile, int stages,
+                                                int cta, int cps, int sl0, Ring& r) {
+  const int lane = threadIdx.x & 31;
+  while (r.issued < stages) {
+    if (r.xsl == 0) {
+      const int t = cta + r.taken * cps;
+      if (r.taken >= p.static_tiles || t >= p.tiles) break;
+      r.pt = t;
+      ++r.taken;
+    }
+    if (lane == 0) stage_tile[r.slot] = r.pt;
+    issue_stage<G>(p, smem, ring_a + r.slot * p.stage, bar_full + 8 * r.slot, tile_of(p, r.pt),
+                   sl0 + r.xsl);
+    r.advance(p.slabs, stages);
+  }
+}
+
+// After griddepcontrol.wait: every further stage, then the end marker.
+template <class G>
+__device__ __forceinline__ void produce_rest(const Params& p, uint8_t* smem, uint32_t ring_a,
+                                             uint32_t bar_full, uint32_t bar_empty,
+                                             int* stage_tile, int stages, int cta, int cps,
+                                             int kseg, int sl0, Ring& r) {
+  const int lane = threadIdx.x & 31;
+  const int dyn0 = p.static_tiles * cps;   // first claimed tile index
+  for (;;) {
+    if (r.xsl == 0) {
+      int t = cta + r.taken * cps;
+      if (r.taken >= p.static_tiles || t >= p.tiles) {
+        if (!r.pending && lane == 0) r.claim = atomicAdd(&g_sched[kseg], 1u);
+        t = dyn0 + static_cast<int>(__shfl_sync(0xFFFFFFFFu, r.claim, 0));
+        r.pending = false;
+      }
+      ++r.taken;
+      if (t >= p.tiles) {
+        // nothing left: tell the consumers through the next slot, and let
+        // the segment's last producer re-arm its counters
+        if (r.issued >= stages && !mbar_wait_warp(bar_empty + 8 * r.slot, r.epar)) return;
+        if (lane == 0) {
+          stage_tile[r.slot] = -1;
+          if (atomicAdd(&g_sched[kMaxSegs + kseg], 1u) == static_cast<unsigned>(cps - 1)) {
+            g_sched[kseg] = 0u;
+            g_sched[kMaxSegs + kseg] = 0u;
+          }
+        }
+        if (!p.tma || lane == 0) mbar_arrive(bar_full + 8 * r.slot);
+        return;
+      }
+      r.pt = t;
+    }
+    if (r.xsl == p.slabs - 1 && !r.pending &&
+        (r.taken >= p.static_tiles || cta + r.taken * cps >= p.tiles)) {
+      if (lane == 0) r.claim = atomicAdd(&g_sched[kseg], 1u);
+      r.pending = true;
+    }
+    if (r.issued >= stages && !mbar_wait_warp(bar_empty + 8 * r.slot, r.epar)) return;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (lane == 0) stage_tile[r.slot] = r.pt;
+    issue_stage<G>(p, smem, ring_a + r.slot * p.stage, bar_full + 8 * r.slot, tile_of(p, r.pt),
+                   sl0 + r.xsl);
+    r.advance(p.slabs, stages);
+  }
+}
+
+// The sum of a value's split-K partial sums (ksplit <= 16 segments, seg_stride
+// floats apart), added in segment order 0..ksplit-1; the loads are issued
+// together rather than one L2 round trip after another.
+constexpr int kMaxSplitSum = 16;
+__device__ __forceinline__ float sum_segments(const float* part, int64_t seg_stride, int ksplit) {
+  float pv[kMaxSplitSum];
+#pragma unroll
+  for (int j = 0; j < kMaxSplitSum; ++j) pv[j] = j < ksplit ? __ldcg(part + j * seg_stride) : 0.0f;
+  float v = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kMaxSplitSum; ++j)
+    if (j < ksplit) v += pv[j];
+  return v;
+}
+
 // ------------------------------------------------------------- consumers
 
 template <int NW>
@@ -1025,82 +1135,16 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
   // and the split-K scratch only after its own griddepcontrol.wait, i.e.
   // after this grid has completed.
   asm volatile("griddepcontrol.launch_dependents;");
-  // Producer state: tile of the stage being issued, tiles taken, slab within
-  // the segment, ring slot, stages issued, parity of the empty wait (waited
-  // from the second lap of the ring on) and the claim made ahead.
-  int pt = 0, taken = 0, pxsl = 0, pslot = 0, issued = 0;
-  uint32_t epar = 1u;
-  unsigned int claim = 0u;
-  auto advance = [&]() {
-    if (++pxsl == p.slabs) pxsl = 0;
-    if (++pslot == stages) {
-      pslot = 0;
-      epar ^= 1u;
-    }
-    ++issued;
-  };
-  if (producer) {
-    // weights do not depend on the previous kernel: the stages of the fixed
-    // tiles that fit the ring stream while that kernel may still be running
-    while (issued < stages) {
-      if (pxsl == 0) {
-        const int t = cta + taken * cps;
-        if (taken >= p.static_tiles || t >= p.tiles) break;
-        pt = t;
-        ++taken;
-      }
-      if (lane == 0) stage_tile[pslot] = pt;
-      issue_stage<G>(p, smem, ring_a + pslot * p.stage, bar_full + 8 * pslot, tile_of(p, pt),
-                     sl0 + pxsl);
-      advance();
-    }
-  }
+  Ring ring;
+  if (producer) produce_prefill<G>(p, smem, ring_a, bar_full, stage_tile, stages, cta, cps, sl0, ring);
   // x may be produced by the previous kernel: wait for it to complete
   asm volatile("griddepcontrol.wait;" ::: "memory");
   stage_x<F, NT, XBF>(p, smem, kseg * p.kpad);
   __syncthreads();
   if (producer) {
-    const int dyn0 = p.static_tiles * cps;   // first claimed tile index
-    bool pending = false;
-    for (;;) {
-      if (pxsl == 0) {
-        int t = cta + taken * cps;
-        if (taken >= p.static_tiles || t >= p.tiles) {
-          if (!pending && lane == 0) claim = atomicAdd(&g_sched[kseg], 1u);
-          t = dyn0 + static_cast<int>(__shfl_sync(0xFFFFFFFFu, claim, 0));
-          pending = false;
-        }
-        ++taken;
-        if (t >= p.tiles) {
-          // nothing left: tell the consumers through the next slot, and let
-          // the segment's last producer re-arm its counters
-          if (issued >= stages && !mbar_wait_warp(bar_empty + 8 * pslot, epar)) return;
-          if (lane == 0) {
-            stage_tile[pslot] = -1;
-            if (atomicAdd(&g_sched[kMaxSegs + kseg], 1u) == static_cast<unsigned>(cps - 1)) {
-              g_sched[kseg] = 0u;
-              g_sched[kMaxSegs + kseg] = 0u;
-            }
-          }
-          if (!p.tma || lane == 0) mbar_arrive(bar_full + 8 * pslot);
-          return;
-        }
-        pt = t;
-      }
-      // the claim for the next tile goes out with the current tile's last
-      // stage, so its latency hides behind the next empty wait
-      if (pxsl == p.slabs - 1 && !pending &&
-          (taken >= p.static_tiles || cta + taken * cps >= p.tiles)) {
-        if (lane == 0) claim = atomicAdd(&g_sched[kseg], 1u);
-        pending = true;
-      }
-      if (issued >= stages && !mbar_wait_warp(bar_empty + 8 * pslot, epar)) return;
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      if (lane == 0) stage_tile[pslot] = pt;
-      issue_stage<G>(p, smem, ring_a + pslot * p.stage, bar_full + 8 * pslot, tile_of(p, pt),
-                     sl0 + pxsl);
-      advance();
-    }
+    produce_rest<G>(p, smem, ring_a, bar_full, bar_empty, stage_tile, stages, cta, cps, kseg, sl0,
+                    ring);
+    return;
   }
   // consumers
   constexpr int kCW = G::kCW;
@@ -1209,19 +1253,11 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
         asm volatile("bar.sync 1, %0;" ::"r"(WC * 32) : "memory");
         if (last_flag) {
           __threadfence();
-          if (ul == 0) {
-#pragma unroll
-            for (int r = 0; r < RT; ++r) {
-              const int row = hw + 2 * WC * r;
-              if (row < tl.rcnt) {
-#pragma unroll
-                for (int k = 0; k < NT; ++k) {
-                  float v = 0.0f;
-                  for (int j = 0; j < p.ksplit; ++j) v += __ldcg(part + j * seg_stride + row * NT + k);
-                  if (k < p.nt) y[static_cast<int64_t>(k) * N + tl.row0 + row] = v;
-                }
-              }
-            }
+          // every consumer thread takes (row, token) values of the tile
+          for (int e = static_cast<int>(threadIdx.x); e < tl.rcnt * NT; e += WC * 32) {
+            const int row = e / NT, k = e % NT;
+            const float v = sum_segments(part + e, seg_stride, p.ksplit);
+            if (k < p.nt) y[static_cast<int64_t>(k) * N + tl.row0 + row] = v;
           }
           if (threadIdx.x == 0) p.arrivals[t] = 0u;
         }
@@ -1709,11 +1745,9 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC <= 4 ? 2 : 1)
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const int tok = 8 * nb + 2 * t + e;
-                if (row < tl.rcnt && tok < p.nt) {
-                  float v = 0.0f;
-                  for (int j = 0; j < p.ksplit; ++j) v += __ldcg(part + j * seg_stride + row * NTP + tok);
-                  y[static_cast<int64_t>(tok) * N + tl.row0 + row] = v;
-                }
+                if (row < tl.rcnt && tok < p.nt)
+                  y[static_cast<int64_t>(tok) * N + tl.row0 + row] =
+                      sum_segments(part + row * NTP + tok, seg_stride, p.ksplit);
               }
             }
           if (threadIdx.x == 0) p.arrivals[tix] = 0u;
@@ -1724,6 +1758,375 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC <= 4 ? 2 : 1)
       xsl = 0;
       ++tn;
     }
+    if (++slot == stages) {
+      slot = 0;
+      parity ^= 1u;
+    }
+  }
+}
+
+// ===================================================== single-token tensor-core kernel
+//
+// n_tok = 1 on large Q4_K / Q4_G128 matrices.  The products run on the tensor cores as
+// mma.sync m16n8k16 (bf16 operands, fp32 accumulation), and the eight
+// columns of the n8 operand carry eight SUB-BLOCKS of the one token instead
+// of eight tokens.  The k slots of an mma are assigned per lane: slots (2t,
+// 2t+1) of lane t (t = lane & 3) hold weights of sub-block lo(t), slots
+// (2t+8, 2t+9) weights of sub-block hi(t), and B holds x at those slots in
+// column lo(t) / hi(t) and zero in the other columns.  After the 16 mmas of
+// a super-block, D[row][n] is the dot product of sub-block n alone, the
+// quantity one scale multiplies:
+//   y_row += s1[n] D[row][n] + s2[n] Sx[n]
+// A = bf16(128 + q) (one LOP3 per two weights: (w & 0x000F000F) | 0x43004300
+// is exact), s1 = d sc, s2 = -(128 s1 + dmin m), Sx[n] the sum of x over
+// sub-block n, staged once per launch.  Lane t takes chunk t of the
+// super-block (sub-block 2t: low nibbles -> slots 2t.., sub-block 2t+1: high
+// nibbles -> slots 2t+8..); word m of the chunk gives mma 2m (bytes 0, 2) and
+// 2m+1 (bytes 1, 3).  Per weight: half a LOP3 plus the shifts that bring the
+// next byte's nibbles down; per sub-block and row: one scale pair.  (Q5_K and
+// Q6_K would need their fields assembled first, which costs more integer
+// work than their CUDA-core path; they stay on gemv_stream.)
+// The column-n lane of each slot pair loads the x entries of sub-block n in
+// that order; the other lanes read a zero block.  Two accumulator chains
+// (bytes 0, 2 / bytes 1, 3) keep consecutive mmas independent.
+//
+// One CTA per SM: kWC consumer warps (a warp owns 16 rows of a 16 kWC-row
+// tile), a producer warp (the ring of one-super-block stages, tile claiming:
+// as in gemv_stream) and, when K is split, a reducer warp.  At the end of a
+// (tile, K segment) unit the consumers leave the unit's row sums in one of two
+// shared buffers and go on; the reducer warp publishes them to the split-K
+// scratch, counts the arrival and, for the last segment of the tile, adds the
+// segments in order 0..ksplit-1 and writes y.  So the device-wide fence and
+// atomic of the reduction never stall the consumers.
+
+template <int F, int WC_>
+struct TGeo {
+  static constexpr int kF = F;
+  static constexpr int kWC = WC_;
+  static constexpr int kThreads = (WC_ + 2) * 32;   // + producer + reducer
+  static constexpr int kRows = 16 * WC_;
+  static_assert(kRows <= 256, "a tile is one tensor-copy box (at most 256 rows)");
+  static constexpr int kSlabSB = 1;
+  static constexpr int kSlabK = 256;
+  static constexpr int kBB = block_bytes(F);
+  static constexpr int kSub = 32;   // weights per sub-block
+  static_assert(F == kQ4K || F == kG128, "Q4_K and Q4_G128 only");
+  static constexpr int kQBytes = (F == kG128) ? 128 * kSlabSB : kBB * kSlabSB;
+  static constexpr int kPBytes = (F == kG128) ? 8 * kSlabSB : 0;
+  static constexpr int round16(int b) { return (b + 15) / 16 * 16; }
+  // row pitch an odd multiple of 16 bytes: the 8 rows a warp reads at once
+  // start in 8 different 16-byte bank groups
+  static constexpr int odd16(int b) { return (b / 16) % 2 ? b : b + 16; }
+  static constexpr int kSlotTma = odd16(round16(kQBytes + (kQBytes % 16 ? 15 : 0)));
+  static constexpr int kPSlotTma = (F == kG128) ? round16(kPBytes + (kPBytes % 16 ? 15 : 0)) : 0;
+  static constexpr int kSlotBulk = odd16(round16(kQBytes + 16));
+  static constexpr int kPSlotBulk = (F == kG128) ? round16(kPBytes + 16) : 0;
+};
+
+// Shared layout before the ring: the staged x of the K segment (kpad values
+// as bf16, each group of four positions (a, b, c, d) stored as (a, c, b, d),
+// so that 32-bit entry i of a sub-block holds positions 4 (i >> 1) + (i & 1)
+// and that + 2), then Sx (the fp32 sum of x over every sub-block), then 64
+// zero bytes, then the reducer's two row-sum buffers of `rows` floats.
+__host__ __device__ constexpr uint32_t tc_x_only(int kpad, int sub) {
+  return (2u * static_cast<uint32_t>(kpad) + 4u * static_cast<uint32_t>(kpad / sub) + 64u + 15u) &
+         ~15u;
+}
+__host__ __device__ constexpr uint32_t tc_x_bytes(int kpad, int sub, int rows) {
+  return (tc_x_only(kpad, sub) + 8u * static_cast<uint32_t>(rows) + 127u) & ~127u;
+}
+
+template <int S>
+__device__ void stage_x_tc(const Params& p, uint32_t xsh, int kbase) {
+  const int nch = p.kpad / 8;   // 16-byte chunks (a multiple of 32)
+  const uint32_t xsum = xsh + 2u * static_cast<uint32_t>(p.kpad);
+  const int lane = threadIdx.x & 31;
+  for (int base = static_cast<int>(threadIdx.x) & ~31; base < nch;
+       base += static_cast<int>(blockDim.x)) {
+    const int c = base + lane;
+    const int k = kbase + 8 * c;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (k < p.K) v = ldg_nc_v4(p.x + k);
+    sts128u(xsh + 16u * c, make_uint4(prmt(v.x, v.y, 0x5410u), prmt(v.x, v.y, 0x7632u),
+                                      prmt(v.z, v.w, 0x5410u), prmt(v.z, v.w, 0x7632u)));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float sum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      sum += __uint_as_float(w[j] << 16) + __uint_as_float(w[j] & 0xFFFF0000u);
+#pragma unroll
+    for (int m = 1; m < S / 8; m <<= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, m);
+    if ((c & (S / 8 - 1)) == 0) {
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(xsum + 4u * (c / (S / 8))), "f"(sum) : "memory");
+    }
+  }
+  if (threadIdx.x < 4)
+    sts128u(xsum + 4u * static_cast<uint32_t>(p.kpad / S) + 16u * threadIdx.x, make_uint4(0, 0, 0, 0));
+}
+
+// y += s1 D + s2 Sx for rows g (h = 0) and g+8 (h = 1), columns (2t, 2t+1)
+__device__ __forceinline__ void tc_epilogue(float2 (&acc)[2], const float (&d)[2][4], float2 s1g,
+                                            float2 s2g, float2 s1h, float2 s2h, float2 sx) {
+  acc[0] = __ffma2_rn(s1g, make_float2(d[0][0] + d[1][0], d[0][1] + d[1][1]), acc[0]);
+  acc[0] = __ffma2_rn(s2g, sx, acc[0]);
+  acc[1] = __ffma2_rn(s1h, make_float2(d[0][2] + d[1][2], d[0][3] + d[1][3]), acc[1]);
+  acc[1] = __ffma2_rn(s2h, sx, acc[1]);
+}
+
+// (s1, s2) of sub-blocks (2t, 2t+1) of one row: Q4_K from the record's
+// header, Q4_G128 from its param plane.
+template <class G>
+__device__ __forceinline__ void tc_scales_q4(const Params& p, const Tile& tl, int sl, uint32_t st,
+                                             int row, int s, const ScaleSel& ss, int t,
+                                             float2& s1, float2& s2) {
+  constexpr int F = G::kF;
+  if constexpr (F == kG128) {
+    const uint32_t po =
+        (static_cast<uint32_t>(tl.row0 + row) * ((8u * p.nsb) & 15u) + sl * G::kPBytes) & 15u;
+    const uint2 pr = lds64(st + p.pbase + row * p.pslot + po + 8 * s);
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
+    const int grp = t >> 1;
+    const float a = dd.x * static_cast<float>((pr.y >> (8 * grp)) & 0xFF);
+    const float b = -(128.0f * a + dd.y * static_cast<float>((pr.y >> (16 + 8 * grp)) & 0xFF));
+    s1 = make_float2(a, a);
+    s2 = make_float2(b, b);
+  } else {
+    const uint4 hdr = lds128(st + row * p.slot + G::kBB * s);
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
+    uint32_t scp, mnp;
+    scale_pair6(ss, hdr.y, hdr.z, hdr.w, scp, mnp);
+    s1 = make_float2(dd.x * static_cast<float>(scp & 0xFF), dd.x * static_cast<float>(scp >> 8));
+    s2 = make_float2(-(128.0f * s1.x + dd.y * static_cast<float>(mnp & 0xFF)),
+                     -(128.0f * s1.y + dd.y * static_cast<float>(mnp >> 8)));
+  }
+}
+
+// One stage for this warp's 16 rows (rbase .. rbase + 15): Q4_K, Q4_G128.
+template <class G>
+__device__ __forceinline__ void tc_stage_q4(const Params& p, const Tile& tl, int sl, int xsl,
+                                            uint32_t st, int rbase, uint32_t xsh,
+                                            const ScaleSel& ss, float2 (&acc)[2]) {
+  constexpr int F = G::kF;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t magic = 0x43004300u;
+  const uint32_t mask = 0x000F000Fu;
+  const uint32_t xsum = xsh + 2u * static_cast<uint32_t>(p.kpad);
+  const uint32_t zero = xsum + 4u * static_cast<uint32_t>(p.kpad / 32);
+  const bool act_lo = g == 2 * t, act_hi = g == 2 * t + 1;   // column g of the B operand
+#pragma unroll
+  for (int s = 0; s < G::kSlabSB; ++s) {
+    if (sl * G::kSlabSB + s >= p.nsb) break;
+    const int sbx = xsl * G::kSlabSB + s;   // super-block of the staged segment
+    const uint32_t xlo = act_lo ? xsh + 64u * (8 * sbx + 2 * t) : zero;
+    const uint32_t xhi = act_hi ? xsh + 64u * (8 * sbx + 2 * t + 1) : zero;
+    uint32_t qa[2];   // rows g, g+8: the chunk's qs bytes
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t rs = st + (rbase + g + 8 * h) * p.slot;
+      qa[h] = (F == kG128) ? rs + 128 * s + 32 * t : rs + G::kBB * s + 16 + 32 * t;
+    }
+    float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int hv = 0; hv < 2; ++hv) {   // words 4 hv .. 4 hv + 3 of the chunk
+      const uint4 w0 = lds128(qa[0] + 16 * hv), w8 = lds128(qa[1] + 16 * hv);
+      const uint4 bl0 = lds128(xlo + 32 * hv), bl1 = lds128(xlo + 32 * hv + 16);
+      const uint4 bh0 = lds128(xhi + 32 * hv), bh1 = lds128(xhi + 32 * hv + 16);
+      const uint32_t W[2][4] = {{w0.x, w0.y, w0.z, w0.w}, {w8.x, w8.y, w8.z, w8.w}};
+      const uint32_t BL[8] = {bl0.x, bl0.y, bl0.z, bl0.w, bl1.x, bl1.y, bl1.z, bl1.w};
+      const uint32_t BH[8] = {bh0.x, bh0.y, bh0.z, bh0.w, bh1.x, bh1.y, bh1.z, bh1.w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        // nibbles at bits 0.. of every byte: low (sub-block 2t), high (2t+1)
+        const uint32_t lo[2] = {W[0][m], W[1][m]};
+        const uint32_t hi[2] = {W[0][m] >> 4, W[1][m] >> 4};
+        mma_bf16(d[0], lop_mask_or(lo[0], mask, magic), lop_mask_or(lo[1], mask, magic),
+                 lop_mask_or(hi[0], mask, magic), lop_mask_or(hi[1], mask, magic), BL[2 * m],
+                 BH[2 * m]);
+        mma_bf16(d[1], lop_mask_or(lo[0] >> 8, mask, magic), lop_mask_or(lo[1] >> 8, mask, magic),
+                 lop_mask_or(hi[0] >> 8, mask, magic), lop_mask_or(hi[1] >> 8, mask, magic),
+                 BL[2 * m + 1], BH[2 * m + 1]);
+      }
+    }
+    float2 s1g, s2g, s1h, s2h;
+    tc_scales_q4<G>(p, tl, sl, st, rbase + g, s, ss, t, s1g, s2g);
+    tc_scales_q4<G>(p, tl, sl, st, rbase + g + 8, s, ss, t, s1h, s2h);
+    const float2 sx = lds_f2(xsum + 4u * (8 * sbx + 2 * t));
+    tc_epilogue(acc, d, s1g, s2g, s1h, s2h, sx);
+  }
+}
+
+constexpr int kTcMaxRows = 256;   // largest tile of the single-token tensor-core kernel
+
+// The reducer warp: for every unit the consumers finish (in order), publish
+// its row sums to the split-K scratch, count the arrival, and for the tile's
+// last segment add segments 0..ksplit-1 in order and write y.
+__device__ __forceinline__ void tc_reduce(const Params& p, uint32_t psum, uint32_t part_full,
+                                          uint32_t part_empty, const int* part_tile, int kseg) {
+  const int lane = threadIdx.x & 31;
+  const int64_t seg_stride = static_cast<int64_t>(p.tiles) * p.tile_rows;
+  for (int u = 0;; ++u) {
+    const int b = u & 1;
+    if (!mbar_wait_warp(part_full + 8 * b, static_cast<uint32_t>(u >> 1) & 1u)) return;
+    const int tix = part_tile[b];
+    if (tix < 0) return;
+    const Tile tl = tile_of(p, tix);
+    float* part = p.part + static_cast<int64_t>(tix) * p.tile_rows;
+    const uint32_t buf = psum + 4u * static_cast<uint32_t>(b * p.tile_rows);
+    for (int row = lane; row < tl.rcnt; row += 32) {
+      float v;
+      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(buf + 4u * row));
+      __stcg(part + kseg * seg_stride + row, v);
+    }
+    // every lane's stores are visible device-wide before the arrival
+    __threadfence();
+    __syncwarp();
+    unsigned last = 0;
+    if (lane == 0)
+      last = atomicAdd(p.arrivals + tix, 1u) == static_cast<unsigned>(p.ksplit - 1) ? 1u : 0u;
+    last = __shfl_sync(0xFFFFFFFFu, last, 0);
+    if (lane == 0) mbar_arrive(part_empty + 8 * b);   // the buffer may be refilled
+    if (last) {
+      __threadfence();
+      // rows lane + 32 i: the loads of one segment are independent, so the
+      // segments stream back to back (each row still adds them in order)
+      float* y = pick(p.g.y, tl.mi);
+      constexpr int kR = kTcMaxRows / 32;
+      float a[kR];
+#pragma unroll
+      for (int i = 0; i < kR; ++i) a[i] = 0.0f;
+      for (int j = 0; j < p.ksplit; ++j) {
+        const float* pj = part + j * seg_stride + lane;
+#pragma unroll
+        for (int i = 0; i < kR; ++i)
+          if (lane + 32 * i < tl.rcnt) a[i] += __ldcg(pj + 32 * i);
+      }
+#pragma unroll
+      for (int i = 0; i < kR; ++i)
+        if (lane + 32 * i < tl.rcnt) y[tl.row0 + lane + 32 * i] = a[i];
+      if (lane == 0) p.arrivals[tix] = 0u;
+    }
+  }
+}
+
+template <int F, int WC>
+__global__ void __launch_bounds__((WC + 2) * 32, WC <= 8 ? 2 : 1)
+    gemv_tc1(const __grid_constant__ Params p, int stages) {
+  using G = TGeo<F, WC>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 4];
+  __shared__ int stage_tile[kMaxStages];
+  __shared__ int part_tile[2];
+  const uint32_t bar_full = smem_addr(&bars[0]);
+  const uint32_t bar_empty = smem_addr(&bars[kMaxStages]);
+  const uint32_t part_full = smem_addr(&bars[2 * kMaxStages]);    // [2]: consumers -> reducer
+  const uint32_t part_empty = smem_addr(&bars[2 * kMaxStages + 2]);   // [2]: reducer -> consumers
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t xsh = smem_addr(smem);
+  const uint32_t psum = xsh + tc_x_only(p.kpad, G::kSub);   // the two row-sum buffers
+  const uint32_t ring_a = xsh + p.x_bytes;
+  const int kseg = static_cast<int>(blockIdx.x) % p.ksplit;
+  const int cta = static_cast<int>(blockIdx.x) / p.ksplit;
+  const int cps = static_cast<int>(gridDim.x) / p.ksplit;
+  const int sl0 = kseg * p.slabs;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(bar_full + 8 * s, p.tma ? 1 : 32);
+      mbar_init(bar_empty + 8 * s, WC);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(part_full + 8 * b, WC);
+      mbar_init(part_empty + 8 * b, 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const bool producer = warp == WC, reducer = warp == WC + 1;
+  asm volatile("griddepcontrol.launch_dependents;");
+  Ring ring;
+  if (producer) produce_prefill<G>(p, smem, ring_a, bar_full, stage_tile, stages, cta, cps, sl0, ring);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  stage_x_tc<G::kSub>(p, xsh, kseg * p.kpad);
+  __syncthreads();
+  if (producer) {
+    produce_rest<G>(p, smem, ring_a, bar_full, bar_empty, stage_tile, stages, cta, cps, kseg, sl0,
+                    ring);
+    return;
+  }
+  if (reducer) {
+    if (p.ksplit > 1) tc_reduce(p, psum, part_full, part_empty, part_tile, kseg);
+    return;
+  }
+  const int g = lane >> 2, t = lane & 3;
+  const int rbase = 16 * warp;
+  const ScaleSel ss = scale_sel(t);
+  float2 acc[2];
+  Tile tl{};
+  int tix = 0, unit = 0;
+  int xsl = 0, slot = 0;
+  uint32_t parity = 0;
+  // hand unit `unit` (tile tix, or -1: no more) to the reducer through
+  // buffer unit & 1, once the reducer has drained that buffer's previous use
+  auto hand_over = [&](const float (&v)[2]) -> bool {
+    const int b = unit & 1;
+    if (unit >= 2 && !mbar_wait_warp(part_empty + 8 * b, static_cast<uint32_t>((unit >> 1) - 1) & 1u))
+      return false;
+    if (tix >= 0 && t == 0) {
+      const uint32_t buf = psum + 4u * static_cast<uint32_t>(b * p.tile_rows);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(buf + 4u * (rbase + g + 8 * h)), "f"(v[h])
+                     : "memory");
+    }
+    if (warp == 0 && lane == 0) part_tile[b] = tix;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(part_full + 8 * b);
+    ++unit;
+    return true;
+  };
+  for (;;) {
+    const int sl = sl0 + xsl;
+    if (!mbar_wait_warp(bar_full + 8 * slot, parity)) return;
+    if (xsl == 0) {
+      tix = stage_tile[slot];
+      if (tix < 0) {
+        if (p.ksplit > 1) {
+          const float none[2] = {0.0f, 0.0f};
+          hand_over(none);
+        }
+        return;
+      }
+      tl = tile_of(p, tix);
+      acc[0] = acc[1] = make_float2(0.0f, 0.0f);
+    }
+    const uint32_t st = ring_a + slot * p.stage;
+    if (rbase < tl.rcnt) tc_stage_q4<G>(p, tl, sl, xsl, st, rbase, xsh, ss, acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+    if (xsl == p.slabs - 1) {
+      // rows g, g+8: add the column pairs, then the four lanes of the row
+      float v[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float a = acc[h].x + acc[h].y;
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, 1);
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, 2);
+        v[h] = a;
+      }
+      if (p.ksplit == 1) {
+        float* y = pick(p.g.y, tl.mi);
+        if (t == 0) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int row = rbase + g + 8 * h;
+            if (row < tl.rcnt) y[tl.row0 + row] = v[h];
+          }
+        }
+      } else if (!hand_over(v)) {
+        return;
+      }
+    }
+    if (++xsl == p.slabs) xsl = 0;
     if (++slot == stages) {
       slot = 0;
       parity ^= 1u;
@@ -2259,6 +2662,153 @@ bool launch_verify(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cuda
                : launch_mma<F, 2, 8>(g, x, K, n_tok, s, src, st);
 }
 
+// The single-token tensor-core kernel: tiles of 16 WC rows (two CTAs per SM
+// up to eight consumer warps, else one), K split into the fewest segments
+// that give every CTA about kTcUnits (tile, segment) units to claim (finer
+// units shorten the tail; each segment's x is staged once per CTA), keeping
+// at least kTcMinStages stages per unit (each unit ends with one split-K
+// hand-over).  Rows whose stride is off the 16-byte grid (no tensor copies)
+// stay on gemv_stream: one-super-block stages would take one bulk copy per
+// row and super-block.
+constexpr int kTcUnits = 6;
+constexpr int kTcMinStages = 4;
+
+template <int F, int WC>
+bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
+                ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
+  using G = TGeo<F, WC>;
+  const DevInfo& di = dev_info();
+  const bool tma = tma_possible<G>(K);
+  if (!tma) return false;
+  const int per_sm = WC <= 8 ? 2 : 1;
+  Params p;
+  p.g = g;
+  p.x = x;
+  p.K = K;
+  p.nsb = K / 256;
+  p.nt = 1;
+  p.part = nullptr;
+  p.arrivals = nullptr;
+  p.tma = tma ? 1 : 0;
+  const int slabs_row = (p.nsb + G::kSlabSB - 1) / G::kSlabSB;
+  const StageShape ss = stage_shape<G>(tma);
+  p.slot = ss.slot;
+  p.pslot = ss.pslot;
+  p.pbase = ss.pbase;
+  p.stage = ss.bytes;
+  p.tile_rows = G::kRows;
+  p.tiles = 0;
+  for (int i = 0; i < kMaxGroup; ++i) {
+    if (i < g.count) p.tiles += (g.N[i] + G::kRows - 1) / G::kRows;
+    p.tile_end[i] = p.tiles;
+  }
+  size_t budget = di.smem_sm / per_sm > di.smem_reserved + kStaticSmem
+                      ? di.smem_sm / per_sm - di.smem_reserved - kStaticSmem
+                      : 0;
+  if (budget > di.smem_optin - kStaticSmem) budget = di.smem_optin - kStaticSmem;
+  int ksplit = 0;
+  for (int ks = 1; ks <= kMaxSegs && ks <= slabs_row; ++ks) {
+    if (slabs_row % ks != 0) continue;
+    if (ks > 1 && slabs_row / ks < kTcMinStages) break;
+    if (tc_x_bytes(slabs_row / ks * G::kSlabK, G::kSub, G::kRows) + 2 * ss.bytes > budget) continue;
+    ksplit = ks;
+    if (static_cast<int64_t>(p.tiles) * ks >= static_cast<int64_t>(kTcUnits) * per_sm * di.sms)
+      break;
+  }
+  if (ksplit == 0) return false;
+  for (;; ksplit = 1) {
+    p.ksplit = ksplit;
+    p.slabs = slabs_row / ksplit;
+    p.kpad = p.slabs * G::kSlabK;
+    p.x_bytes = tc_x_bytes(p.kpad, G::kSub, G::kRows);
+    if (p.x_bytes + 2 * ss.bytes > budget) return false;
+    if (ksplit == 1) break;
+    const size_t part_bytes = static_cast<size_t>(ksplit) * p.tiles * p.tile_rows * sizeof(float);
+    if (src == ScratchSrc::kDevice) {
+      if (p.tiles > kMaxTiles) continue;
+      uint8_t* base = static_cast<uint8_t*>(scratch_get(kCounterBytes + part_bytes, s));
+      if (base == nullptr) continue;   // no scratch (e.g. during capture): unsplit
+      p.arrivals = reinterpret_cast<unsigned int*>(base);
+      p.part = reinterpret_cast<float*>(base + kCounterBytes);
+    } else {
+      if (p.tiles > kNoAllocMaxTiles ||
+          kNoAllocCounterBytes + part_bytes > kNoAllocScratchBytes) {
+        st->too_large = true;
+        return false;
+      }
+      if (cudaMemsetAsync(st->base, 0, static_cast<size_t>(p.tiles) * sizeof(unsigned int), s) !=
+          cudaSuccess)
+        return false;
+      p.arrivals = reinterpret_cast<unsigned int*>(st->base);
+      p.part = reinterpret_cast<float*>(st->base + kNoAllocCounterBytes);
+    }
+    break;
+  }
+  int stages = static_cast<int>((budget - p.x_bytes) / ss.bytes);
+  if (stages > kMaxStages) stages = kMaxStages;
+  int cps = per_sm * di.sms / p.ksplit;
+  if (cps > p.tiles) cps = p.tiles;
+  if (cps < 1) cps = 1;
+  p.static_tiles = (stages + p.slabs - 1) / p.slabs;
+  const size_t smem = p.x_bytes + static_cast<size_t>(stages) * ss.bytes;
+  static size_t configured = 0;
+  if (smem > configured) {
+    if (cudaFuncSetAttribute(gemv_tc1<F, WC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return false;
+    }
+    configured = smem;
+  }
+  p.tx = 0;
+  if (tma) {
+    for (int i = 0; i < g.count; ++i) {
+      const int64_t n = g.N[i];
+      bool ok;
+      if constexpr (F == kG128) {
+        ok = encode_plane(&p.tm[i][0], g.W[i], 128 * static_cast<uint64_t>(p.nsb), n, ss.slot,
+                          G::kRows) &&
+             encode_plane(&p.tm[i][1], g.W[i] + n * p.nsb * 128, 8 * static_cast<uint64_t>(p.nsb), n,
+                          ss.pslot, G::kRows);
+      } else {
+        ok = encode_plane(&p.tm[i][0], g.W[i], static_cast<uint64_t>(p.nsb) * G::kBB, n, ss.slot,
+                          G::kRows);
+      }
+      if (!ok) return false;
+    }
+    p.tx = static_cast<uint32_t>(G::kRows) * (ss.slot + ss.pslot);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cps * p.ksplit));
+  cfg.blockDim = dim3(G::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_tc1<F, WC>, p, stages) == cudaSuccess;
+}
+
+// Single-token launches that take the tensor-core kernel: Q4_K and Q4_G128
+// matrices of at least 32 M weights (the MLP matrices of a decoder layer).
+// Q5_K and Q6_K stay on gemv_stream: assembling their 5- and 6-bit fields
+// costs the A operand more integer instructions than the CUDA-core path
+// spends per weight, and the integer pipe is what bounds both kernels.
+bool tc1_eligible(int fmt, const GemvGroup& g, int K, int n_tok) {
+  if (n_tok != 1 || (fmt != kQ4K && fmt != kG128)) return false;
+  int64_t rows = 0;
+  for (int i = 0; i < g.count; ++i) rows += g.N[i];
+  return rows * K >= (int64_t{1} << 25);
+}
+
+template <int F>
+bool launch_tc1_fmt(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
+                    ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
+  return launch_tc1<F, 16>(g, x, K, s, src, st);   // 16 consumer warps, one CTA per SM
+}
+
 }  // namespace
 
 bool launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
@@ -2272,6 +2822,10 @@ bool launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_
       case kG128: return launch_verify<kG128>(g, x, K, n_tok, s);
     }
     return false;
+  }
+  if (tc1_eligible(fmt, g, K, n_tok)) {
+    const bool ok = fmt == kQ4K ? launch_tc1_fmt<kQ4K>(g, x, K, s) : launch_tc1_fmt<kG128>(g, x, K, s);
+    if (ok) return true;
   }
   const int nt = n_tok <= 1 ? 1 : (n_tok <= 2 ? 2 : 4);
 #define KQ_CASE(F)                                                  \
@@ -2337,6 +2891,12 @@ NoAllocResult launch_stream_noalloc(int fmt, const GemvGroup& g, const uint16_t*
     }
     if (st.too_large) return NoAllocResult::kTooLarge;
     return ok ? NoAllocResult::kLaunched : NoAllocResult::kNotServed;
+  }
+  if (tc1_eligible(fmt, g, K, n_tok)) {
+    ok = fmt == kQ4K ? launch_tc1_fmt<kQ4K>(g, x, K, s, ScratchSrc::kStatic, &st)
+                     : launch_tc1_fmt<kG128>(g, x, K, s, ScratchSrc::kStatic, &st);
+    if (st.too_large) return NoAllocResult::kTooLarge;
+    if (ok) return NoAllocResult::kLaunched;
   }
   const int nt = n_tok <= 1 ? 1 : (n_tok <= 2 ? 2 : 4);
 #define KQ_CASE(F)                                                                          \

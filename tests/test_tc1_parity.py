@@ -1,0 +1,130 @@
+"""GPU parity of single-token launches on large matrices (n_tok = 1, at least
+32 M weights).  Q4_K and Q4_G128 run on the tensor cores with the sub-blocks
+of the one token as the columns of the mma's n8 operand; Q5_K and Q6_K on the
+streaming CUDA-core kernel.
+
+Every row is checked against the fp64 oracle (|y - y_ref| <= 1e-3 sum|w^ x| +
+1e-5).  The shapes cover: ragged last tiles; an odd super-block count; Q6_K
+and Q4_G128 rows whose stride is off the 16-byte grid (per-row bulk copies;
+the tensor-core kernel declines those and the streaming kernel serves them);
+long rows split into many K segments (split-K hand-over to the reducer warp);
+rows on the 16-byte grid (2-D tensor copies); random block bytes (every scale
+and field value); a grouped launch whose tiles straddle the two matrices; and
+repeated launches (tiles are claimed at run time, the result must not vary).
+"""
+import numpy as np
+import pytest
+
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+CANARY = 1234.5678
+FMTS = [0, 1, 2, 3]
+FMT_IDS = ["Q4_K", "Q5_K", "Q6_K", "G128"]
+
+# (N, K): ragged tiles + odd K/256 (per-row copies for Q6_K and G128);
+# long rows with few tiles (many K segments); rows on the 16-byte grid
+CASES = [(8300, 4352), (1100, 32768), (20000, 2048)]
+
+
+@pytest.fixture(scope="module")
+def kq():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from quant_weight_gemv_dequant_b300 import build
+    build.build()
+    import quant_weight_gemv_dequant_b300 as k
+    k.lib()
+    return k
+
+
+_W = {}
+
+
+def _weights_f32(N, K):
+    if (N, K) not in _W:
+        _W[(N, K)] = wl.weights_f32(wl.derive_seed(700, N, K), N, K)
+    return _W[(N, K)]
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _dev_x(x_u16):
+    return _dev(x_u16.view(np.int16)).view(torch.bfloat16)
+
+
+def _gemv(kq, fmt, Wb, x, N, K):
+    pad = 64
+    ybuf = torch.full((N + 2 * pad,), CANARY, dtype=torch.float32, device="cuda")
+    kq.kq_gemv(fmt, _dev(Wb), _dev_x(x), ybuf[pad:pad + N], N, K, 1)
+    kq.kq_device_status()
+    out = ybuf.cpu().numpy()
+    assert np.all(out[:pad] == np.float32(CANARY)) and np.all(out[pad + N:] == np.float32(CANARY))
+    return out[pad:pad + N].reshape(1, N)
+
+
+def _assert_parity(y, yref, A, what):
+    tol = 1e-3 * A + 1e-5
+    err = np.abs(y.astype(np.float64) - yref)
+    bad = ~(err <= tol)
+    if bad.any():
+        i = np.unravel_index(np.argmax(np.where(bad, err / tol, 0)), err.shape)
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; worst at {i}: "
+                             f"y={y[i]!r} ref={yref[i]!r} tol={tol[i]!r}")
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=FMT_IDS)
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}x{c[1]}")
+def test_single_token_large_matches_oracle(kq, oracle, fmt, case):
+    N, K = case
+    Wb = oracle.quantize(fmt, _weights_f32(N, K), N, K)
+    x = wl.activations_bf16(wl.derive_seed(701, fmt, N), 1, K, heavy=True)
+    yref, A = oracle.gemv(fmt, Wb, N, K, x)
+    _assert_parity(_gemv(kq, fmt, Wb, x, N, K), yref, A, f"fmt={fmt} {N}x{K}")
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=FMT_IDS)
+def test_single_token_large_random_blocks(kq, oracle, fmt):
+    N, K = 8300, 4352
+    Wb = wl.random_block_bytes(wl.derive_seed(702, fmt), fmt, N * K // 256)
+    x = wl.activations_bf16(wl.derive_seed(703, fmt), 1, K)
+    yref, A = oracle.gemv(fmt, Wb, N, K, x)
+    _assert_parity(_gemv(kq, fmt, Wb, x, N, K), yref, A, f"random fmt={fmt}")
+
+
+@pytest.mark.parametrize("fmt", [0, 2], ids=["Q4_K", "Q6_K"])
+def test_single_token_grouped_launch(kq, oracle, fmt):
+    # two matrices in one launch (gate / up style); 9000 and 7001 rows: the
+    # tiles of the first end mid-tile, the second has a ragged tail
+    K = 2304
+    Ns = [9000, 7001]
+    x = wl.activations_bf16(wl.derive_seed(704, fmt), 1, K, heavy=True)
+    Ws, ys, refs = [], [], []
+    for j, N in enumerate(Ns):
+        Wb = oracle.quantize(fmt, wl.weights_f32(wl.derive_seed(705, fmt, j), N, K), N, K)
+        refs.append(oracle.gemv(fmt, Wb, N, K, x))
+        Ws.append(_dev(Wb))
+        ys.append(torch.full((1, N), CANARY, dtype=torch.float32, device="cuda"))
+    kq.kq_gemv_multi(fmt, Ws, ys, Ns, _dev_x(x), K, 1)
+    kq.kq_device_status()
+    for j, (yref, A) in enumerate(refs):
+        _assert_parity(ys[j].cpu().numpy(), yref, A, f"matrix {j}")
+
+
+def test_single_token_repeated_launches_agree(kq, oracle):
+    # the tile order differs run to run (tiles are claimed at run time); the
+    # result must not: every tile's sum is formed in a fixed order
+    N, K = 1100, 32768
+    Wb = oracle.quantize(2, _weights_f32(N, K), N, K)
+    x = wl.activations_bf16(wl.derive_seed(706), 1, K, heavy=True)
+    W, xd = _dev(Wb), _dev_x(x)
+    y0 = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    kq.kq_gemv(2, W, xd, y0, N, K, 1)
+    for _ in range(5):
+        y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+        kq.kq_gemv(2, W, xd, y, N, K, 1)
+        assert torch.equal(y, y0)
+    kq.kq_device_status()

@@ -36,7 +36,7 @@ def _dev(a):
 
 # (format, N_out, K, n_tok): split-K cases (long rows, several K segments),
 # an unsplit case and an n_tok > 4 case (served without scratch)
-CASES = [(2, 600, 32768, 1), (0, 300, 32768, 2), (1, 96, 5120, 3), (0, 4096, 4096, 1),
+CASES = [(2, 600, 32768, 1), (0, 300, 32768, 2), (1, 96, 5120, 3), (0, 4096, 4096, 1), (0, 1100, 32768, 1),
          (3, 64, 1024, 8)]
 
 
