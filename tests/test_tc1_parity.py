@@ -114,17 +114,18 @@ def test_single_token_grouped_launch(kq, oracle, fmt):
         _assert_parity(ys[j].cpu().numpy(), yref, A, f"matrix {j}")
 
 
-def test_single_token_repeated_launches_agree(kq, oracle):
+@pytest.mark.parametrize("fmt", [0, 2], ids=["Q4_K", "Q6_K"])
+def test_single_token_repeated_launches_agree(kq, oracle, fmt):
     # the tile order differs run to run (tiles are claimed at run time); the
     # result must not: every tile's sum is formed in a fixed order
     N, K = 1100, 32768
-    Wb = oracle.quantize(2, _weights_f32(N, K), N, K)
+    Wb = oracle.quantize(fmt, _weights_f32(N, K), N, K)
     x = wl.activations_bf16(wl.derive_seed(706), 1, K, heavy=True)
     W, xd = _dev(Wb), _dev_x(x)
     y0 = torch.empty((1, N), dtype=torch.float32, device="cuda")
-    kq.kq_gemv(2, W, xd, y0, N, K, 1)
+    kq.kq_gemv(fmt, W, xd, y0, N, K, 1)
     for _ in range(5):
         y = torch.empty((1, N), dtype=torch.float32, device="cuda")
-        kq.kq_gemv(2, W, xd, y, N, K, 1)
+        kq.kq_gemv(fmt, W, xd, y, N, K, 1)
         assert torch.equal(y, y0)
     kq.kq_device_status()
