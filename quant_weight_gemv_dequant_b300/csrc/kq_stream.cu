@@ -1799,12 +1799,12 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC <= 4 ? 2 : 1)
 // segments in order 0..ksplit-1 and writes y.  So the device-wide fence and
 // atomic of the reduction never stall the consumers.
 
-template <int F, int WC_>
+template <int F, int WC_, int RTW = 1>
 struct TGeo {
   static constexpr int kF = F;
   static constexpr int kWC = WC_;
   static constexpr int kThreads = (WC_ + 2) * 32;   // + producer + reducer
-  static constexpr int kRows = 16 * WC_;
+  static constexpr int kRows = 16 * WC_ * RTW;        // a warp owns RTW 16-row tiles
   static_assert(kRows <= 256, "a tile is one tensor-copy box (at most 256 rows)");
   static constexpr int kSlabSB = 1;
   static constexpr int kSlabK = 256;
@@ -1956,27 +1956,28 @@ __device__ __forceinline__ void tc_stage_q4(const Params& p, const Tile& tl, int
   }
 }
 
-constexpr int kTcMaxRows = 256;   // largest tile of the single-token tensor-core kernel
-
 // The reducer warp: for every unit the consumers finish (in order), publish
-// its row sums to the split-K scratch, count the arrival, and for the tile's
-// last segment add segments 0..ksplit-1 in order and write y.
+// its sums (tile_rows x NTP values, row-major) to the split-K scratch, count
+// the arrival, and for the tile's last segment add segments 0..ksplit-1 in
+// order and write y (token k of row r to y[k][row0 + r], k < n_tok).
+template <int NTP>
 __device__ __forceinline__ void tc_reduce(const Params& p, uint32_t psum, uint32_t part_full,
                                           uint32_t part_empty, const int* part_tile, int kseg) {
   const int lane = threadIdx.x & 31;
-  const int64_t seg_stride = static_cast<int64_t>(p.tiles) * p.tile_rows;
+  const int64_t seg_stride = static_cast<int64_t>(p.tiles) * p.tile_rows * NTP;
   for (int u = 0;; ++u) {
     const int b = u & 1;
     if (!mbar_wait_warp(part_full + 8 * b, static_cast<uint32_t>(u >> 1) & 1u)) return;
     const int tix = part_tile[b];
     if (tix < 0) return;
     const Tile tl = tile_of(p, tix);
-    float* part = p.part + static_cast<int64_t>(tix) * p.tile_rows;
-    const uint32_t buf = psum + 4u * static_cast<uint32_t>(b * p.tile_rows);
-    for (int row = lane; row < tl.rcnt; row += 32) {
+    const int n = tl.rcnt * NTP;
+    float* part = p.part + static_cast<int64_t>(tix) * p.tile_rows * NTP;
+    const uint32_t buf = psum + 4u * static_cast<uint32_t>(b * p.tile_rows * NTP);
+    for (int e = lane; e < n; e += 32) {
       float v;
-      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(buf + 4u * row));
-      __stcg(part + kseg * seg_stride + row, v);
+      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(buf + 4u * e));
+      __stcg(part + kseg * seg_stride + e, v);
     }
     // every lane's stores are visible device-wide before the arrival
     __threadfence();
@@ -1988,22 +1989,28 @@ __device__ __forceinline__ void tc_reduce(const Params& p, uint32_t psum, uint32
     if (lane == 0) mbar_arrive(part_empty + 8 * b);   // the buffer may be refilled
     if (last) {
       __threadfence();
-      // rows lane + 32 i: the loads of one segment are independent, so the
-      // segments stream back to back (each row still adds them in order)
+      // values e0 + lane + 32 i: the loads of one segment are independent, so
+      // the segments stream back to back (each value still adds them in order)
       float* y = pick(p.g.y, tl.mi);
-      constexpr int kR = kTcMaxRows / 32;
-      float a[kR];
+      const int64_t N = pick(p.g.N, tl.mi);
+      constexpr int kR = 8;
+      for (int e0 = 0; e0 < n; e0 += 32 * kR) {
+        float a[kR];
 #pragma unroll
-      for (int i = 0; i < kR; ++i) a[i] = 0.0f;
-      for (int j = 0; j < p.ksplit; ++j) {
-        const float* pj = part + j * seg_stride + lane;
+        for (int i = 0; i < kR; ++i) a[i] = 0.0f;
+        for (int j = 0; j < p.ksplit; ++j) {
+          const float* pj = part + j * seg_stride + e0 + lane;
 #pragma unroll
-        for (int i = 0; i < kR; ++i)
-          if (lane + 32 * i < tl.rcnt) a[i] += __ldcg(pj + 32 * i);
+          for (int i = 0; i < kR; ++i)
+            if (e0 + lane + 32 * i < n) a[i] += __ldcg(pj + 32 * i);
+        }
+#pragma unroll
+        for (int i = 0; i < kR; ++i) {
+          const int e = e0 + lane + 32 * i;
+          const int row = e / NTP, k = e % NTP;
+          if (e < n && k < p.nt) y[static_cast<int64_t>(k) * N + tl.row0 + row] = a[i];
+        }
       }
-#pragma unroll
-      for (int i = 0; i < kR; ++i)
-        if (lane + 32 * i < tl.rcnt) y[tl.row0 + lane + 32 * i] = a[i];
       if (lane == 0) p.arrivals[tix] = 0u;
     }
   }
@@ -2054,7 +2061,7 @@ __global__ void __launch_bounds__((WC + 2) * 32, WC <= 8 ? 2 : 1)
     return;
   }
   if (reducer) {
-    if (p.ksplit > 1) tc_reduce(p, psum, part_full, part_empty, part_tile, kseg);
+    if (p.ksplit > 1) tc_reduce<1>(p, psum, part_full, part_empty, part_tile, kseg);
     return;
   }
   const int g = lane >> 2, t = lane & 3;
@@ -2123,6 +2130,339 @@ __global__ void __launch_bounds__((WC + 2) * 32, WC <= 8 ? 2 : 1)
           }
         }
       } else if (!hand_over(v)) {
+        return;
+      }
+    }
+    if (++xsl == p.slabs) xsl = 0;
+    if (++slot == stages) {
+      slot = 0;
+      parity ^= 1u;
+    }
+  }
+}
+
+// ============================================= multi-token tensor-core kernel
+//
+// n_tok 5..16 on large Q4_K / Q4_G128 matrices (the speculative-verify
+// widths), on the skeleton of gemv_tc1 (one CTA per SM, one-super-block
+// stages, tile claiming, reducer warp).  Columns of the n8 operand are tokens
+// (NB blocks of eight); a warp owns two 16-row mma tiles, so every B fragment
+// loaded from shared memory feeds two A fragments.  One mma covers 16
+// positions of one sub-block: lane t takes bytes 8t .. 8t+7 of a chunk, and
+// word m of them gives slots (2t, 2t+1) <- bytes (0, 2) and (2t+8, 2t+9) <-
+// bytes (1, 3): the low nibbles for the chunk's first sub-block, the high
+// nibbles (one more shift) for its second.  Two mmas per sub-block, token
+// block and row tile, then
+//   y[tok] += s1 D + s2 Sx[tok]
+// per (row, sub-block), with s1, s2 from a per-warp table built once per
+// super-block (each lane decodes the four chunks of one row) and Sx staged
+// with x.  The staged x: token rows of kpad bf16 values, each group of four
+// positions (a, b, c, d) stored as (a, c, b, d) so that one 8-byte load gives
+// a lane both B registers of an mma; row tok starts at tok (2 kpad + 128) +
+// 8 ((tok & 1) + 8 ((tok >> 1) & 1)), which puts the 16 lanes of a half-warp
+// load (4 tokens x 4 lanes) in 16 different 8-byte bank slots.
+
+constexpr int kTcvRT = 2;                     // 16-row mma tiles per warp
+constexpr uint32_t kTcvTabPitch = 144;        // 8 float4 + 16 bytes: the 8 g of a read in distinct banks
+constexpr uint32_t kTcvTabWarp = kTcvRT * 8 * kTcvTabPitch;
+
+__host__ __device__ constexpr uint32_t tcv_xstride(int kpad) { return 2u * kpad + 128u; }
+__host__ __device__ constexpr uint32_t tcv_row(int tok, int kpad) {
+  return tok * tcv_xstride(kpad) + 8u * ((tok & 1) + 8 * ((tok >> 1) & 1));
+}
+// shared layout before the ring: x rows | Sx [kpad/32][8 NB] | WC scale
+// tables | two hand-over buffers of rows x 8 NB floats
+__host__ __device__ constexpr uint32_t tcv_sx(int kpad, int nb) {
+  return tcv_xstride(kpad) * 8u * nb;
+}
+__host__ __device__ constexpr uint32_t tcv_tab(int kpad, int nb) {
+  return tcv_sx(kpad, nb) + 4u * (kpad / 32) * 8u * nb;
+}
+__host__ __device__ constexpr uint32_t tcv_psum(int kpad, int nb, int wc) {
+  return tcv_tab(kpad, nb) + wc * kTcvTabWarp;
+}
+__host__ __device__ constexpr uint32_t tcv_x_bytes(int kpad, int nb, int wc, int rows) {
+  return (tcv_psum(kpad, nb, wc) + 2u * rows * 8u * nb * 4u + 127u) & ~127u;
+}
+
+template <int NB>
+__device__ void stage_x_tcv(const Params& p, uint32_t xsh, int kbase) {
+  constexpr int NTP = 8 * NB;
+  const int per_tok = p.kpad / 8;   // 16-byte chunks per token (a multiple of 32)
+  const uint32_t sxa = xsh + tcv_sx(p.kpad, NB);
+  const int lane = threadIdx.x & 31;
+  for (int base = static_cast<int>(threadIdx.x) & ~31; base < NTP * per_tok;
+       base += static_cast<int>(blockDim.x)) {
+    const int q = base + lane;
+    const int tok = q / per_tok, c = q % per_tok;
+    const int k = kbase + 8 * c;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (tok < p.nt && k < p.K) v = ldg_nc_v4(p.x + static_cast<int64_t>(tok) * p.K + k);
+    // rows start on 8-byte boundaries: two 8-byte stores
+    const uint32_t a = xsh + tcv_row(tok, p.kpad) + 16u * c;
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(prmt(v.x, v.y, 0x5410u)),
+                 "r"(prmt(v.x, v.y, 0x7632u))
+                 : "memory");
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a + 8u), "r"(prmt(v.z, v.w, 0x5410u)),
+                 "r"(prmt(v.z, v.w, 0x7632u))
+                 : "memory");
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float sum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      sum += __uint_as_float(w[j] << 16) + __uint_as_float(w[j] & 0xFFFF0000u);
+    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+    if ((c & 3) == 0) {
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(sxa + 4u * ((c >> 2) * NTP + tok)), "f"(sum)
+                   : "memory");
+    }
+  }
+}
+
+__device__ __forceinline__ void sts_f2(uint32_t a, float x, float y) {
+  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
+}
+
+// This warp's scale table for one super-block.  Entry (rt, g, j), a float4 at
+// tab + (rt 8 + g) pitch + 16 j: (s1, s2) of row 16 rt + g and of row 16 rt +
+// g + 8, sub-block j.  Lane l decodes the four chunks of row l of the warp.
+template <class G>
+__device__ __forceinline__ void tcv_scale_table(const Params& p, const Tile& tl, int sl,
+                                                uint32_t st, int rbase, int s, uint32_t tab) {
+  constexpr int F = G::kF;
+  const int lane = threadIdx.x & 31;
+  const int row = rbase + lane;
+  const uint32_t te = tab + ((lane >> 4) * 8 + (lane & 7)) * kTcvTabPitch + 8u * ((lane >> 3) & 1);
+  if constexpr (F == kG128) {
+    const uint32_t po =
+        (static_cast<uint32_t>(tl.row0 + row) * ((8u * p.nsb) & 15u) + sl * G::kPBytes) & 15u;
+    const uint2 pr = lds64(st + p.pbase + row * p.pslot + po + 8 * s);
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp) {
+      const float a = dd.x * static_cast<float>((pr.y >> (8 * grp)) & 0xFF);
+      const float b = -(128.0f * a + dd.y * static_cast<float>((pr.y >> (16 + 8 * grp)) & 0xFF));
+#pragma unroll
+      for (int j = 4 * grp; j < 4 * grp + 4; ++j) sts_f2(te + 16 * j, a, b);
+    }
+  } else {
+    const uint4 hdr = lds128(st + row * p.slot + G::kBB * s);
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t scp, mnp;
+      scale_pair6(scale_sel(c), hdr.y, hdr.z, hdr.w, scp, mnp);
+      const float a0 = dd.x * static_cast<float>(scp & 0xFF);
+      const float a1 = dd.x * static_cast<float>(scp >> 8);
+      sts_f2(te + 32 * c, a0, -(128.0f * a0 + dd.y * static_cast<float>(mnp & 0xFF)));
+      sts_f2(te + 32 * c + 16, a1, -(128.0f * a1 + dd.y * static_cast<float>(mnp >> 8)));
+    }
+  }
+}
+
+// One stage for this warp's rows rbase .. rbase + 32, NB blocks of eight tokens.
+template <class G, int NB>
+__device__ __forceinline__ void tcv_stage_q4(const Params& p, const Tile& tl, int sl, int xsl,
+                                             uint32_t st, int rbase, uint32_t xsh, uint32_t tab,
+                                             float2 (&acc)[NB][kTcvRT][2]) {
+  constexpr int F = G::kF;
+  constexpr int NTP = 8 * NB;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t magic = 0x43004300u, mask = 0x000F000Fu;
+  const uint32_t sxa = xsh + tcv_sx(p.kpad, NB);
+  const int nrt = tl.rcnt - rbase > 16 ? 2 : 1;   // live row tiles of this warp
+#pragma unroll
+  for (int s = 0; s < G::kSlabSB; ++s) {
+    if (sl * G::kSlabSB + s >= p.nsb) break;
+    const int sbx = xsl * G::kSlabSB + s;
+    tcv_scale_table<G>(p, tl, sl, st, rbase, s, tab);
+    __syncwarp();
+    uint32_t qa[kTcvRT][2];
+#pragma unroll
+    for (int rt = 0; rt < kTcvRT; ++rt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t rs = st + (rbase + 16 * rt + g + 8 * h) * p.slot;
+        qa[rt][h] = (F == kG128) ? rs + 128 * s + 8 * t : rs + G::kBB * s + 16 + 8 * t;
+      }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      // A registers [tile][row h][word m]: low nibbles of bytes (0, 2), (1,
+      // 3); high nibbles of bytes (0, 2), (1, 3)
+      uint32_t l02[kTcvRT][2][2], l13[kTcvRT][2][2], h02[kTcvRT][2][2], h13[kTcvRT][2][2];
+#pragma unroll
+      for (int rt = 0; rt < kTcvRT; ++rt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint2 wv = (rt < nrt) ? lds64(qa[rt][h] + 32 * c) : make_uint2(0, 0);
+          const uint32_t W[2] = {wv.x, wv.y};
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            l02[rt][h][m] = lop_mask_or(W[m], mask, magic);
+            l13[rt][h][m] = lop_mask_or(W[m] >> 8, mask, magic);
+            h02[rt][h][m] = lop_mask_or(W[m] >> 4, mask, magic);
+            h13[rt][h][m] = lop_mask_or(W[m] >> 12, mask, magic);
+          }
+        }
+      const int jlo = 8 * sbx + 2 * c;   // sub-block of the segment (low nibbles)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const uint32_t xr = xsh + tcv_row(8 * nb + g, p.kpad) + 2u * (256 * sbx + 64 * c + 8 * t);
+        float dl[kTcvRT][4] = {}, dh[kTcvRT][4] = {};
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const uint2 bl = lds64(xr + 8 * m);
+          const uint2 bh = lds64(xr + 64 + 8 * m);
+#pragma unroll
+          for (int rt = 0; rt < kTcvRT; ++rt) {
+            mma_bf16(dl[rt], l02[rt][0][m], l02[rt][1][m], l13[rt][0][m], l13[rt][1][m], bl.x, bl.y);
+            mma_bf16(dh[rt], h02[rt][0][m], h02[rt][1][m], h13[rt][0][m], h13[rt][1][m], bh.x, bh.y);
+          }
+        }
+        const float2 sxl = lds_f2(sxa + 4u * (jlo * NTP + 8 * nb + 2 * t));
+        const float2 sxh = lds_f2(sxa + 4u * ((jlo + 1) * NTP + 8 * nb + 2 * t));
+#pragma unroll
+        for (int rt = 0; rt < kTcvRT; ++rt) {
+          const uint32_t te = tab + (rt * 8 + g) * kTcvTabPitch + 32u * c;
+          const float4 el = lds_f4(te), eh = lds_f4(te + 16);   // (s1, s2) of rows g, g + 8
+          float2& a0 = acc[nb][rt][0];
+          float2& a1 = acc[nb][rt][1];
+          a0 = __ffma2_rn(make_float2(el.x, el.x), make_float2(dl[rt][0], dl[rt][1]), a0);
+          a0 = __ffma2_rn(make_float2(el.y, el.y), sxl, a0);
+          a0 = __ffma2_rn(make_float2(eh.x, eh.x), make_float2(dh[rt][0], dh[rt][1]), a0);
+          a0 = __ffma2_rn(make_float2(eh.y, eh.y), sxh, a0);
+          a1 = __ffma2_rn(make_float2(el.z, el.z), make_float2(dl[rt][2], dl[rt][3]), a1);
+          a1 = __ffma2_rn(make_float2(el.w, el.w), sxl, a1);
+          a1 = __ffma2_rn(make_float2(eh.z, eh.z), make_float2(dh[rt][2], dh[rt][3]), a1);
+          a1 = __ffma2_rn(make_float2(eh.w, eh.w), sxh, a1);
+        }
+      }
+    }
+    __syncwarp();   // the table is rebuilt for the next super-block
+  }
+}
+
+template <int F, int WC, int NB>
+__global__ void __launch_bounds__((WC + 2) * 32, 1)
+    gemv_tcv(const __grid_constant__ Params p, int stages) {
+  using G = TGeo<F, WC, kTcvRT>;
+  constexpr int NTP = 8 * NB;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 4];
+  __shared__ int stage_tile[kMaxStages];
+  __shared__ int part_tile[2];
+  const uint32_t bar_full = smem_addr(&bars[0]);
+  const uint32_t bar_empty = smem_addr(&bars[kMaxStages]);
+  const uint32_t part_full = smem_addr(&bars[2 * kMaxStages]);
+  const uint32_t part_empty = smem_addr(&bars[2 * kMaxStages + 2]);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t xsh = smem_addr(smem);
+  const uint32_t tab = xsh + tcv_tab(p.kpad, NB) + warp * kTcvTabWarp;
+  const uint32_t psum = xsh + tcv_psum(p.kpad, NB, WC);
+  const uint32_t ring_a = xsh + p.x_bytes;
+  const int kseg = static_cast<int>(blockIdx.x) % p.ksplit;
+  const int cta = static_cast<int>(blockIdx.x) / p.ksplit;
+  const int cps = static_cast<int>(gridDim.x) / p.ksplit;
+  const int sl0 = kseg * p.slabs;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(bar_full + 8 * s, p.tma ? 1 : 32);
+      mbar_init(bar_empty + 8 * s, WC);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(part_full + 8 * b, WC);
+      mbar_init(part_empty + 8 * b, 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const bool producer = warp == WC, reducer = warp == WC + 1;
+  asm volatile("griddepcontrol.launch_dependents;");
+  Ring ring;
+  if (producer) produce_prefill<G>(p, smem, ring_a, bar_full, stage_tile, stages, cta, cps, sl0, ring);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  stage_x_tcv<NB>(p, xsh, kseg * p.kpad);
+  __syncthreads();
+  if (producer) {
+    produce_rest<G>(p, smem, ring_a, bar_full, bar_empty, stage_tile, stages, cta, cps, kseg, sl0,
+                    ring);
+    return;
+  }
+  if (reducer) {
+    if (p.ksplit > 1) tc_reduce<NTP>(p, psum, part_full, part_empty, part_tile, kseg);
+    return;
+  }
+  const int g = lane >> 2, t = lane & 3;
+  const int rbase = 16 * kTcvRT * warp;
+  float2 acc[NB][kTcvRT][2];
+  Tile tl{};
+  int tix = 0, unit = 0;
+  int xsl = 0, slot = 0;
+  uint32_t parity = 0;
+  // hand unit `unit` (tile tix, or -1: no more) to the reducer through
+  // buffer unit & 1, once the reducer has drained that buffer's previous use
+  auto hand_over = [&](bool data) -> bool {
+    const int b = unit & 1;
+    if (unit >= 2 && !mbar_wait_warp(part_empty + 8 * b, static_cast<uint32_t>((unit >> 1) - 1) & 1u))
+      return false;
+    if (data) {
+      const uint32_t buf = psum + 4u * static_cast<uint32_t>(b * p.tile_rows * NTP);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int rt = 0; rt < kTcvRT; ++rt)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t a = buf + 4u * ((rbase + 16 * rt + g + 8 * h) * NTP + 8 * nb + 2 * t);
+            sts_f2(a, acc[nb][rt][h].x, acc[nb][rt][h].y);
+          }
+    }
+    if (warp == 0 && lane == 0) part_tile[b] = data ? tix : -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(part_full + 8 * b);
+    ++unit;
+    return true;
+  };
+  for (;;) {
+    const int sl = sl0 + xsl;
+    if (!mbar_wait_warp(bar_full + 8 * slot, parity)) return;
+    if (xsl == 0) {
+      tix = stage_tile[slot];
+      if (tix < 0) {
+        if (p.ksplit > 1) hand_over(false);
+        return;
+      }
+      tl = tile_of(p, tix);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int rt = 0; rt < kTcvRT; ++rt) acc[nb][rt][0] = acc[nb][rt][1] = make_float2(0.0f, 0.0f);
+    }
+    const uint32_t st = ring_a + slot * p.stage;
+    if (rbase < tl.rcnt) tcv_stage_q4<G, NB>(p, tl, sl, xsl, st, rbase, xsh, tab, acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+    if (xsl == p.slabs - 1) {
+      if (p.ksplit == 1) {
+        float* y = pick(p.g.y, tl.mi);
+        const int64_t N = pick(p.g.N, tl.mi);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int rt = 0; rt < kTcvRT; ++rt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int row = rbase + 16 * rt + g + 8 * h;
+              const int tok = 8 * nb + 2 * t;
+              if (row < tl.rcnt) {
+                if (tok < p.nt) y[static_cast<int64_t>(tok) * N + tl.row0 + row] = acc[nb][rt][h].x;
+                if (tok + 1 < p.nt)
+                  y[static_cast<int64_t>(tok + 1) * N + tl.row0 + row] = acc[nb][rt][h].y;
+              }
+            }
+      } else if (!hand_over(true)) {
         return;
       }
     }
@@ -2791,6 +3131,141 @@ bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
   return cudaLaunchKernelEx(&cfg, gemv_tc1<F, WC>, p, stages) == cudaSuccess;
 }
 
+// The multi-token tensor-core kernel (n_tok 5..16, NB = 1 or 2 blocks of
+// eight tokens): one CTA per SM; K segments chosen as for gemv_tc1.
+template <int F, int WC, int NB>
+bool launch_tcv(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
+                ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
+  using G = TGeo<F, WC, kTcvRT>;
+  constexpr int NTP = 8 * NB;
+  const DevInfo& di = dev_info();
+  const bool tma = tma_possible<G>(K);
+  if (!tma) return false;
+  Params p;
+  p.g = g;
+  p.x = x;
+  p.K = K;
+  p.nsb = K / 256;
+  p.nt = n_tok;
+  p.part = nullptr;
+  p.arrivals = nullptr;
+  p.tma = 1;
+  const int slabs_row = (p.nsb + G::kSlabSB - 1) / G::kSlabSB;
+  const StageShape ss = stage_shape<G>(true);
+  p.slot = ss.slot;
+  p.pslot = ss.pslot;
+  p.pbase = ss.pbase;
+  p.stage = ss.bytes;
+  p.tile_rows = G::kRows;
+  p.tiles = 0;
+  for (int i = 0; i < kMaxGroup; ++i) {
+    if (i < g.count) p.tiles += (g.N[i] + G::kRows - 1) / G::kRows;
+    p.tile_end[i] = p.tiles;
+  }
+  size_t budget = di.smem_sm > di.smem_reserved + kStaticSmem
+                      ? di.smem_sm - di.smem_reserved - kStaticSmem
+                      : 0;
+  if (budget > di.smem_optin - kStaticSmem) budget = di.smem_optin - kStaticSmem;
+  auto xb = [&](int kpad) { return static_cast<size_t>(tcv_x_bytes(kpad, NB, WC, G::kRows)); };
+  // the fewest K segments whose x fits: a split-K hand-over carries 8 NB
+  // values per row, which costs more than the coarser tile balance
+  int ksplit = 0;
+  for (int ks = 1; ks <= kMaxSegs && ks <= slabs_row; ++ks) {
+    if (slabs_row % ks != 0) continue;
+    if (xb(slabs_row / ks * G::kSlabK) + 2 * ss.bytes > budget) continue;
+    ksplit = ks;
+    break;
+  }
+  if (ksplit == 0) return false;
+  for (;; ksplit = 1) {
+    p.ksplit = ksplit;
+    p.slabs = slabs_row / ksplit;
+    p.kpad = p.slabs * G::kSlabK;
+    p.x_bytes = static_cast<uint32_t>(xb(p.kpad));
+    if (p.x_bytes + 2 * ss.bytes > budget) return false;
+    if (ksplit == 1) break;
+    const size_t part_bytes =
+        static_cast<size_t>(ksplit) * p.tiles * p.tile_rows * NTP * sizeof(float);
+    if (src == ScratchSrc::kDevice) {
+      if (p.tiles > kMaxTiles) continue;
+      uint8_t* base = static_cast<uint8_t*>(scratch_get(kCounterBytes + part_bytes, s));
+      if (base == nullptr) continue;   // no scratch (e.g. during capture): unsplit
+      p.arrivals = reinterpret_cast<unsigned int*>(base);
+      p.part = reinterpret_cast<float*>(base + kCounterBytes);
+    } else {
+      if (p.tiles > kNoAllocMaxTiles ||
+          kNoAllocCounterBytes + part_bytes > kNoAllocScratchBytes) {
+        st->too_large = true;
+        return false;
+      }
+      if (cudaMemsetAsync(st->base, 0, static_cast<size_t>(p.tiles) * sizeof(unsigned int), s) !=
+          cudaSuccess)
+        return false;
+      p.arrivals = reinterpret_cast<unsigned int*>(st->base);
+      p.part = reinterpret_cast<float*>(st->base + kNoAllocCounterBytes);
+    }
+    break;
+  }
+  int stages = static_cast<int>((budget - p.x_bytes) / ss.bytes);
+  if (stages > kMaxStages) stages = kMaxStages;
+  int cps = di.sms / p.ksplit;
+  if (cps > p.tiles) cps = p.tiles;
+  if (cps < 1) cps = 1;
+  p.static_tiles = (stages + p.slabs - 1) / p.slabs;
+  const size_t smem = p.x_bytes + static_cast<size_t>(stages) * ss.bytes;
+  static size_t configured = 0;
+  if (smem > configured) {
+    if (cudaFuncSetAttribute(gemv_tcv<F, WC, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return false;
+    }
+    configured = smem;
+  }
+  for (int i = 0; i < g.count; ++i) {
+    const int64_t n = g.N[i];
+    bool ok;
+    if constexpr (F == kG128) {
+      ok = encode_plane(&p.tm[i][0], g.W[i], 128 * static_cast<uint64_t>(p.nsb), n, ss.slot,
+                        G::kRows) &&
+           encode_plane(&p.tm[i][1], g.W[i] + n * p.nsb * 128, 8 * static_cast<uint64_t>(p.nsb), n,
+                        ss.pslot, G::kRows);
+    } else {
+      ok = encode_plane(&p.tm[i][0], g.W[i], static_cast<uint64_t>(p.nsb) * G::kBB, n, ss.slot,
+                        G::kRows);
+    }
+    if (!ok) return false;
+  }
+  p.tx = static_cast<uint32_t>(G::kRows) * (ss.slot + ss.pslot);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cps * p.ksplit));
+  cfg.blockDim = dim3(G::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_tcv<F, WC, NB>, p, stages) == cudaSuccess;
+}
+
+// Verify-width (n_tok 5..16) launches that take the multi-token tensor-core
+// kernel: Q4_K and Q4_G128 matrices of at least 32 M weights.
+bool tcv_eligible(int fmt, const GemvGroup& g, int K, int n_tok) {
+  if (n_tok < 5 || n_tok > 16 || (fmt != kQ4K && fmt != kG128)) return false;
+  int64_t rows = 0;
+  for (int i = 0; i < g.count; ++i) rows += g.N[i];
+  return rows * K >= (int64_t{1} << 25);
+}
+
+template <int F>
+bool launch_tcv_fmt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
+                    ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
+  return n_tok <= 8 ? launch_tcv<F, 8, 1>(g, x, K, n_tok, s, src, st)
+                    : launch_tcv<F, 8, 2>(g, x, K, n_tok, s, src, st);
+}
+
 // Single-token launches that take the tensor-core kernel: Q4_K and Q4_G128
 // matrices of at least 32 M weights (the MLP matrices of a decoder layer).
 // Q5_K and Q6_K stay on gemv_stream: assembling their 5- and 6-bit fields
@@ -2814,6 +3289,11 @@ bool launch_tc1_fmt(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s
 bool launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
                    cudaStream_t s) {
   if (n_tok > 16) return false;
+  if (tcv_eligible(fmt, g, K, n_tok)) {
+    const bool ok = fmt == kQ4K ? launch_tcv_fmt<kQ4K>(g, x, K, n_tok, s)
+                                : launch_tcv_fmt<kG128>(g, x, K, n_tok, s);
+    if (ok) return true;
+  }
   if (n_tok > 4) {
     switch (fmt) {
       case kQ4K: return launch_verify<kQ4K>(g, x, K, n_tok, s);
@@ -2881,6 +3361,12 @@ NoAllocResult launch_stream_noalloc(int fmt, const GemvGroup& g, const uint16_t*
   StaticScratch st{static_cast<uint8_t*>(noalloc_scratch_address()), false};
   if (st.base == nullptr) return NoAllocResult::kFailed;
   bool ok = false;
+  if (tcv_eligible(fmt, g, K, n_tok)) {
+    ok = fmt == kQ4K ? launch_tcv_fmt<kQ4K>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st)
+                     : launch_tcv_fmt<kG128>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st);
+    if (st.too_large) return NoAllocResult::kTooLarge;
+    if (ok) return NoAllocResult::kLaunched;
+  }
   if (n_tok > 4) {
     switch (fmt) {
       case kQ4K: ok = launch_verify<kQ4K>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st); break;

@@ -1,7 +1,9 @@
-"""GPU parity of single-token launches on large matrices (n_tok = 1, at least
-32 M weights).  Q4_K and Q4_G128 run on the tensor cores with the sub-blocks
-of the one token as the columns of the mma's n8 operand; Q5_K and Q6_K on the
-streaming CUDA-core kernel.
+"""GPU parity of launches on large matrices (at least 32 M weights) at one
+token and at the verify widths.  At n_tok = 1, Q4_K and Q4_G128 run on the
+tensor cores with the sub-blocks of the one token as the columns of the mma's
+n8 operand (gemv_tc1); Q5_K and Q6_K on the streaming CUDA-core kernel.  At
+n_tok 5..16, Q4_K and Q4_G128 run on the one-CTA-per-SM tensor-core kernel
+with tokens as columns (gemv_tcv); Q5_K and Q6_K on gemv_mma.
 
 Every row is checked against the fp64 oracle (|y - y_ref| <= 1e-3 sum|w^ x| +
 1e-5).  The shapes cover: ragged last tiles; an odd super-block count; Q6_K
@@ -64,6 +66,17 @@ def _gemv(kq, fmt, Wb, x, N, K):
     out = ybuf.cpu().numpy()
     assert np.all(out[:pad] == np.float32(CANARY)) and np.all(out[pad + N:] == np.float32(CANARY))
     return out[pad:pad + N].reshape(1, N)
+
+
+def _gemv_t(kq, fmt, Wb, x, N, K):
+    T = x.shape[0]
+    pad = 64
+    ybuf = torch.full((T * N + 2 * pad,), CANARY, dtype=torch.float32, device="cuda")
+    kq.kq_gemv(fmt, _dev(Wb), _dev_x(x), ybuf[pad:pad + T * N], N, K, T)
+    kq.kq_device_status()
+    out = ybuf.cpu().numpy()
+    assert np.all(out[:pad] == np.float32(CANARY)) and np.all(out[pad + T * N:] == np.float32(CANARY))
+    return out[pad:pad + T * N].reshape(T, N)
 
 
 def _assert_parity(y, yref, A, what):
@@ -129,3 +142,39 @@ def test_single_token_repeated_launches_agree(kq, oracle, fmt):
         kq.kq_gemv(fmt, W, xd, y, N, K, 1)
         assert torch.equal(y, y0)
     kq.kq_device_status()
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=FMT_IDS)
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}x{c[1]}")
+def test_verify_widths_large_match_oracle(kq, oracle, fmt, case):
+    N, K = case
+    Wb = oracle.quantize(fmt, _weights_f32(N, K), N, K)
+    x = wl.activations_bf16(wl.derive_seed(707, fmt, N), 16, K, heavy=True)
+    yref, A = oracle.gemv(fmt, Wb, N, K, x)
+    for T in (5, 8, 11, 16):
+        _assert_parity(_gemv_t(kq, fmt, Wb, x[:T], N, K), yref[:T], A[:T], f"fmt={fmt} {N}x{K} n_tok={T}")
+
+
+@pytest.mark.parametrize("fmt", [0, 3], ids=["Q4_K", "G128"])
+def test_verify_width_random_blocks(kq, oracle, fmt):
+    N, K = 20000, 2048
+    Wb = wl.random_block_bytes(wl.derive_seed(708, fmt), fmt, N * K // 256)
+    x = wl.activations_bf16(wl.derive_seed(709, fmt), 8, K)
+    yref, A = oracle.gemv(fmt, Wb, N, K, x)
+    _assert_parity(_gemv_t(kq, fmt, Wb, x, N, K), yref, A, f"random fmt={fmt}")
+
+
+def test_verify_width_grouped_launch(kq, oracle):
+    K, T = 2304, 8
+    Ns = [9000, 7001]
+    x = wl.activations_bf16(wl.derive_seed(710), T, K, heavy=True)
+    Ws, ys, refs = [], [], []
+    for j, N in enumerate(Ns):
+        Wb = oracle.quantize(0, wl.weights_f32(wl.derive_seed(711, j), N, K), N, K)
+        refs.append(oracle.gemv(0, Wb, N, K, x))
+        Ws.append(_dev(Wb))
+        ys.append(torch.full((T, N), CANARY, dtype=torch.float32, device="cuda"))
+    kq.kq_gemv_multi(0, Ws, ys, Ns, _dev_x(x), K, T)
+    kq.kq_device_status()
+    for j, (yref, A) in enumerate(refs):
+        _assert_parity(ys[j].cpu().numpy(), yref, A, f"matrix {j}")
