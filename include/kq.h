@@ -114,9 +114,13 @@ size_t kq_matrix_bytes(kq_format f, int64_t N_out, int64_t K);
  * scratch buffer of the current device, allocated by the library on first
  * need (never while the stream is being captured; a capture then runs the
  * unsplit configuration) and grown by allocating a larger one; buffers are
- * never freed, so CUDA graphs captured earlier stay valid.  The buffer is
- * shared by all calls on a device: calls that overlap on the GPU (different
- * streams, no ordering between them) race on it. */
+ * never freed, so CUDA graphs captured earlier stay valid.  Row tiles are
+ * handed to CTAs at run time from per-K-segment counters that live in the
+ * library (zero between launches; every launch re-arms them before it ends).
+ * The scratch buffer and the counters are shared by all calls on a device:
+ * calls that overlap on the GPU (different streams, no ordering between
+ * them) race on them.  Results do not depend on which CTA takes which tile:
+ * every sum is formed in a fixed order. */
 kq_status kq_gemv(kq_format f, const void* W_blocks, const void* x_bf16,
                   float* y, int64_t N_out, int64_t K, int n_tok,
                   kq_stream_t stream);
@@ -144,7 +148,8 @@ kq_status kq_gemv(kq_format f, const void* W_blocks, const void* x_bf16,
  *   Sharing: every call uses the same array, which keeps the previous
  *   call's contents; each call clears the counters it needs (a
  *   stream-ordered memset).  Calls that overlap on the GPU (different
- *   streams, no ordering between them) race on the array. */
+ *   streams, no ordering between them) race on the array and on the tile
+ *   counters (as for kq_gemv). */
 kq_status kq_gemv_noalloc(kq_format f, const void* W_blocks, const void* x_bf16, float* y,
                           int64_t N_out, int64_t K, int n_tok, kq_stream_t stream);
 
@@ -225,7 +230,8 @@ kq_status kq_merge_g128(const void* q4k_host, int64_t N_out, int64_t K,
  * and a wait that runs out makes the kernel stop early and count the event
  * in a device word instead of hanging.  This call synchronises `stream`,
  * reads and clears that count, and returns KQ_ERR_TIMEOUT if it was non-zero
- * (the outputs of the kernels since the previous call are then not valid),
+ * (the outputs of the kernels since the previous call are then not valid;
+ * the split-K and tile counters a stopped kernel left behind are re-armed),
  * KQ_ERR_CUDA if the read failed, KQ_OK otherwise.  Not for use inside
  * stream capture. */
 kq_status kq_device_status(kq_stream_t stream);
