@@ -2553,6 +2553,12 @@ struct Plan {
   size_t budget = 0;   // dynamic shared memory one CTA may use at per_sm CTAs per SM
 };
 
+// CTAs per SM the streaming kernel's launch bounds allow
+template <int WC>
+constexpr int stream_max_per_sm() {
+  return WC == 8 ? 2 : 3;
+}
+
 template <int F, int NT, int RT, int WC, bool XBF>
 Plan make_plan(int K, int ksplit, bool tma) {
   using G = Geo<F, NT, RT, WC>;
@@ -2565,7 +2571,7 @@ Plan make_plan(int K, int ksplit, bool tma) {
                     static_cast<size_t>(NT) * (kpad / G::kPart) * 4;
   pl.x_bytes = static_cast<uint32_t>((xb + 127) & ~size_t{127});
   const DevInfo& di = dev_info();
-  for (int per_sm = 3; per_sm >= 1; --per_sm) {
+  for (int per_sm = stream_max_per_sm<WC>(); per_sm >= 1; --per_sm) {
     // dynamic shared memory of one CTA when per_sm CTAs share an SM
     size_t budget = di.smem_sm / per_sm;
     budget = budget > di.smem_reserved + kStaticSmem ? budget - di.smem_reserved - kStaticSmem : 0;
@@ -2781,26 +2787,27 @@ bool launch_rt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStre
                ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
   using G = Geo<F, NT, RT, WC>;
   // K segments: the fewest (a power of two dividing the slabs of a row, at
-  // most 16) that reach three CTAs per SM, else the fewest that reach the
-  // most CTAs per SM.  x is staged as bf16 only when its fp32 copy would not
-  // fit at all.
+  // most 16) that reach the kernel's most CTAs per SM, else the fewest that
+  // reach the most CTAs per SM.
   const int slabs_row = (K / 256 + G::kSlabSB - 1) / G::kSlabSB;
   const bool tma = tma_possible<G>(K);
   int best_ks = 0, best_sm = 0;
   bool best_bf = false;
-  for (int ks = 1; ks <= 16 && slabs_row % ks == 0; ks *= 2) {
-    Plan pl = make_plan<F, NT, RT, WC, false>(K, ks, tma);
-    bool bf = false;
-    if (pl.per_sm == 0) {
-      pl = make_plan<F, NT, RT, WC, true>(K, ks, tma);
-      bf = true;
+  // fp32 x first (no conversion in the consumers); bf16 x only where it
+  // admits more CTAs per SM than any fp32 plan (e.g. the LM head's per-row
+  // copies, whose stages with fp32 x leave room for two CTAs only)
+  constexpr int kMaxPer = stream_max_per_sm<WC>();
+  for (int bf = 0; bf < 2 && best_sm < kMaxPer; ++bf) {
+    for (int ks = 1; ks <= 16 && slabs_row % ks == 0; ks *= 2) {
+      const Plan pl = bf ? make_plan<F, NT, RT, WC, true>(K, ks, tma)
+                         : make_plan<F, NT, RT, WC, false>(K, ks, tma);
+      if (pl.per_sm > best_sm) {
+        best_sm = pl.per_sm;
+        best_ks = ks;
+        best_bf = bf != 0;
+      }
+      if (best_sm == kMaxPer) break;
     }
-    if (pl.per_sm > best_sm) {
-      best_sm = pl.per_sm;
-      best_ks = ks;
-      best_bf = bf;
-    }
-    if (best_sm == 3) break;
   }
   if (best_ks == 0) return false;
   for (int ks = best_ks;; ks = 1) {
