@@ -2994,14 +2994,16 @@ bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
 }
 
 // Consumer warps per CTA: 8 (one CTA per SM) for launches of 64 M weights
-// or more; 4 (two CTAs per SM, 64-row tiles) for smaller ones such as the
-// attention projections, where more, smaller tiles fill the GPU better.
+// or more whose rows take 2-D tensor copies; 4 (two CTAs per SM, 64-row
+// tiles) for smaller ones such as the attention projections, where more,
+// smaller tiles fill the GPU better, and for rows off the 16-byte grid (the
+// LM head), where two producer warps per SM issue the per-row copies.
 template <int F>
 bool launch_verify(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
                    ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
   int64_t rows = 0;
   for (int i = 0; i < g.count; ++i) rows += g.N[i];
-  const bool small = rows * K < (int64_t{64} << 20);
+  const bool small = rows * K < (int64_t{64} << 20) || !tma_possible<MGeo<F, 8>>(K);
   if (n_tok <= 8)
     return small ? launch_mma<F, 1, 4>(g, x, K, n_tok, s, src, st)
                  : launch_mma<F, 1, 8>(g, x, K, n_tok, s, src, st);
