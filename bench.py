@@ -104,6 +104,21 @@ def replica_throughput(dist, bytes_this_rank: float, seconds_this_rank: float):
     return total / t_max / 1e9, t_max, total
 
 
+NOMINAL_HBM_GBS = 7700.0   # B300 HBM3e, nominal (context only; the roofline uses the measured peak)
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (Linux /proc/cpuinfo), for the oracle baseline."""
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -358,6 +373,7 @@ def run_reference(args):
         "config": {"workload": WORKLOAD, "n_tok": args.n_tok, "layers": args.layers,
                    "weight_bytes_per_step": step_bytes},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "cpu_model": cpu_model(), "host_cpus": os.cpu_count(),
                          "sample": f"2 sampled rows of each of the 7 matrices of 8 layers and of the LM head, "
                                    f"cycled for ~1 s of single-threaded fp64 oracle per step; {tot_b} packed "
                                    f"bytes total; ms_per_step extrapolates to the full 19.1 GB step"},
@@ -451,6 +467,7 @@ def run_kq(args):
     if rank == 0 and not args.no_extra:
         gbs, el, nb = oracle_sample_rate(oracle_samples(oracle_pools(), 8, args.n_tok), 12.0)
         cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "cpu_model": cpu_model(), "host_cpus": os.cpu_count(),
                "sample": f"single-threaded fp64 oracle on 2 sampled rows of each of the 7 matrices of 8 "
                          f"layers and of the LM head, cycled for {el:.1f} s ({nb} packed bytes)"}
 
@@ -467,6 +484,7 @@ def run_kq(args):
                        "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}"},
             "us_per_step": t_max * 1e6, "tok_per_s": args.n_tok / t_max * world,
             "pct_of_hbm_peak": 100 * value / world / hbm,
+            "pct_of_nominal_hbm": 100 * value / world / NOMINAL_HBM_GBS,
             "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": hbm,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
                          "traffic": profiled_traffic(kname), "bytes_per_launch": kbytes,
