@@ -334,3 +334,36 @@ def test_graph_survives_scratch_growth(kq, oracle, pools):
     sub = wl.tiled_rows(pools[fmt], fmt, sb, Nb, K, rows)
     yref, A = oracle.gemv(fmt, sub, len(rows), K, xb)
     assert_parity(yb.cpu().numpy()[:, rows], yref, A, "large split-K request")
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3], ids=["Q4_K", "Q5_K", "Q6_K", "G128"])
+def test_degenerate_rows_and_tokens(kq, oracle, fmt):
+    """Degenerate cases of the method through every kernel: rows that are all
+    zero (d = dmin = 0), constant (one sub-block value, the scale term zero),
+    a million times smaller than the rest, a single spike, and rows whose
+    sub-blocks alternate between zero and constant; a token of all-zero x
+    among heavy-tailed ones.  8300 x 4352 (36 M weights) takes the
+    tensor-core kernels for Q4_K / Q4_G128 at n_tok 1 and 8, the streaming
+    kernel at 2, gemv_mma for Q5_K / Q6_K at 8."""
+    N, K = 8300, 4352
+    w = wl.weights_f32(wl.derive_seed(120, fmt), N, K)
+    w[0] = 0.0
+    w[1] = 0.5
+    w[2] = -0.125
+    w[3] *= 1e-6
+    w[4] = 0.0
+    w[4, 1234] = 3.0
+    for j in range(0, K, 64):
+        w[5, j:j + 32] = 0.0
+        w[5, j + 32:j + 64] = 0.03
+    w[N - 1] = 0.0
+    Wb = oracle.quantize(fmt, w, N, K)
+    x = wl.activations_bf16(wl.derive_seed(121, fmt), 8, K, heavy=True)
+    x[1] = 0
+    yref, A = oracle.gemv(fmt, Wb, N, K, x)
+    for T in (1, 2, 8):
+        y = gpu_gemv(kq, fmt, Wb, x[:T], N, K)
+        assert_parity(y, yref[:T], A[:T], f"fmt={fmt} n_tok={T}")
+        assert np.all(y[:, 0] == 0.0) and np.all(y[:, N - 1] == 0.0)   # zero rows give exact zeros
+        if T > 1:
+            assert np.all(y[1] == 0.0)                                  # so does a zero token
