@@ -2144,8 +2144,9 @@ __global__ void __launch_bounds__((WC + 2) * 32, WC <= 8 ? 2 : 1)
 // ============================================= multi-token tensor-core kernel
 //
 // n_tok 5..16 on large Q4_K / Q4_G128 matrices (the speculative-verify
-// widths), on the skeleton of gemv_tc1 (one CTA per SM, one-super-block
-// stages, tile claiming, reducer warp).  Columns of the n8 operand are tokens
+// widths), on the skeleton of gemv_tc1 (one-super-block stages, tile
+// claiming, reducer warp; two 4-warp CTAs per SM up to eight tokens, one
+// 8-warp CTA beyond).  Columns of the n8 operand are tokens
 // (NB blocks of eight); a warp owns two 16-row mma tiles, so every B fragment
 // loaded from shared memory feeds two A fragments.  One mma covers 16
 // positions of one sub-block: lane t takes bytes 8t .. 8t+7 of a chunk, and
@@ -2345,7 +2346,7 @@ __device__ __forceinline__ void tcv_stage_q4(const Params& p, const Tile& tl, in
 }
 
 template <int F, int WC, int NB>
-__global__ void __launch_bounds__((WC + 2) * 32, 1)
+__global__ void __launch_bounds__((WC + 2) * 32, WC <= 4 ? 2 : 1)
     gemv_tcv(const __grid_constant__ Params p, int stages) {
   using G = TGeo<F, WC, kTcvRT>;
   constexpr int NTP = 8 * NB;
@@ -3141,7 +3142,7 @@ bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
 }
 
 // The multi-token tensor-core kernel (n_tok 5..16, NB = 1 or 2 blocks of
-// eight tokens): one CTA per SM; K segments chosen as for gemv_tc1.
+// eight tokens).  K segments: the fewest whose x fits with two ring stages.
 template <int F, int WC, int NB>
 bool launch_tcv(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
                 ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
@@ -3171,8 +3172,9 @@ bool launch_tcv(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
     if (i < g.count) p.tiles += (g.N[i] + G::kRows - 1) / G::kRows;
     p.tile_end[i] = p.tiles;
   }
-  size_t budget = di.smem_sm > di.smem_reserved + kStaticSmem
-                      ? di.smem_sm - di.smem_reserved - kStaticSmem
+  const int per_sm = WC <= 4 ? 2 : 1;   // CTAs per SM (the launch bounds' minimum)
+  size_t budget = di.smem_sm / per_sm > di.smem_reserved + kStaticSmem
+                      ? di.smem_sm / per_sm - di.smem_reserved - kStaticSmem
                       : 0;
   if (budget > di.smem_optin - kStaticSmem) budget = di.smem_optin - kStaticSmem;
   auto xb = [&](int kpad) { return static_cast<size_t>(tcv_x_bytes(kpad, NB, WC, G::kRows)); };
@@ -3217,7 +3219,7 @@ bool launch_tcv(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   }
   int stages = static_cast<int>((budget - p.x_bytes) / ss.bytes);
   if (stages > kMaxStages) stages = kMaxStages;
-  int cps = di.sms / p.ksplit;
+  int cps = per_sm * di.sms / p.ksplit;
   if (cps > p.tiles) cps = p.tiles;
   if (cps < 1) cps = 1;
   p.static_tiles = (stages + p.slabs - 1) / p.slabs;
@@ -3271,7 +3273,10 @@ bool tcv_eligible(int fmt, const GemvGroup& g, int K, int n_tok) {
 template <int F>
 bool launch_tcv_fmt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
                     ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
-  return n_tok <= 8 ? launch_tcv<F, 8, 1>(g, x, K, n_tok, s, src, st)
+  // up to eight tokens: two CTAs of four consumer warps per SM (each with
+  // half the x, so the SM keeps twice the weight stages in flight); 9..16
+  // tokens: one CTA of eight consumer warps per SM
+  return n_tok <= 8 ? launch_tcv<F, 4, 1>(g, x, K, n_tok, s, src, st)
                     : launch_tcv<F, 8, 2>(g, x, K, n_tok, s, src, st);
 }
 
