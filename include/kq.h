@@ -91,7 +91,7 @@ typedef enum {
   KQ_ERR_NOT_MERGEABLE = 4, /* kq_merge_g128: sub-blocks differ in (sc, m) */
   KQ_ERR_RANGE = 5,         /* kq_quantize: a scale exceeds fp16 range     */
   KQ_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed        */
-  KQ_ERR_UNSUPPORTED = 7,   /* valid request this build cannot serve       */
+  KQ_ERR_UNSUPPORTED = 7,   /* valid request the library cannot serve     */
   KQ_ERR_TIMEOUT = 8,       /* a kernel's bounded wait ran out (see below) */
   KQ_ERR_TOO_LARGE = 9      /* kq_gemv_noalloc: beyond its fixed scratch    */
 } kq_status;
