@@ -8,7 +8,7 @@
  * runs GGUF Q4_K/Q5_K/Q6_K weights directly as packed integer GEMV kernels and
  * that adjacent sub-blocks with the same scale/min are merged, when lossless,
  * into groups of up to 128.  The SGLang day-0 post on Muse Glimmer (paragraph
- * on the GGUF checkpoints) names the "Q4KM format with a group size of 128".
+ * on the GGUF checkpoints) names a Q4_K_M checkpoint with 128-weight groups.
  * The Core AI model card for Muse-Glimmer-30B (first table and the sentence
  * under it) shows decode streaming every weight once per token (23.7 tok/s x
  * 17.9 GB = 424 GB/s), i.e. the product y = W x is weight-bandwidth bound.
@@ -50,17 +50,25 @@
  *     w^ = d*sc_g*q - dmin*m_g
  *
  * Conventions for every entry point.
- *   - The caller owns all memory.  No entry point allocates device memory.
+ *   - The caller owns its inputs and outputs.  The library allocates device
+ *     memory in exactly one place: kq_gemv (and kq_gemv_multi, kq_layer_step,
+ *     which use it) grows a per-device split-K scratch buffer with cudaMalloc
+ *     on the first long-row request that needs more than it holds (never
+ *     while the stream is being captured; that request then runs a
+ *     configuration without the buffer).  kq_gemv_noalloc never allocates.
  *   - Device pointers: W_blocks must be 16-byte aligned; x is bf16
  *     [n_tok][K] with contiguous rows (x must be 16-byte aligned and K a
  *     multiple of 256); y is fp32 [n_tok][N_out] and is overwritten.
  *   - Requirements: K % 256 == 0, K > 0, N_out > 0, 1 <= n_tok <= 16.  A
  *     violation returns a status before anything is launched.
- *   - Calls on a stream are asynchronous, never synchronise, and may be
- *     captured into a CUDA graph.
+ *   - Calls on a stream are asynchronous and never synchronise (except
+ *     kq_device_status); a CUDA graph may capture them once the same shape
+ *     has run outside capture.
  *   - A CUDA launch failure returns KQ_ERR_CUDA.  Nothing throws or exits
  *     across this ABI.  NaN/Inf inputs give unspecified (but in-bounds)
  *     results.
+ *   - Every declaration below carries a "Source:" line: the page passage
+ *     that defines the operation, or a statement that the pages define none.
  */
 #ifndef KQ_H
 #define KQ_H
@@ -97,19 +105,27 @@ typedef enum {
 } kq_status;
 
 /* Bytes of one 256-weight super-block: 144 / 176 / 210 / 136.  0 for a bad
- * format. */
+ * format.
+ * Source: the pages define no sizes; these are the GGUF record sizes of the
+ * formats the daily.dev summary names (answer on exporting GGUF
+ * checkpoints), whose bytes per weight match the Core AI card's 17.9 GB file
+ * (first table), plus this library's 136-byte merged group-128 record. */
 size_t kq_block_bytes(kq_format f);
 
 /* Bytes of an N_out x K matrix in format f (N_out*K/256 super-blocks; for
- * KQ_Q4_G128 both planes).  0 if the shape is invalid. */
+ * KQ_Q4_G128 both planes).  0 if the shape is invalid.
+ * Source: none in the pages; N_out*K/256 times kq_block_bytes. */
 size_t kq_matrix_bytes(kq_format f, int64_t N_out, int64_t K);
 
 /* y[t][n] = sum_k w^[n][k] x[t][k] for t < n_tok, n < N_out.
  *   W_blocks : device, the N_out x K matrix in format f, 16-B aligned
  *   x_bf16   : device, bf16 [n_tok][K], 16-B aligned
  *   y        : device, fp32 [n_tok][N_out], overwritten
- * Accumulates in fp32.  Source: the daily.dev ExecuTorch summary, answer on
- * exporting GGUF checkpoints (Q4_K/Q5_K/Q6_K GEMV; group-128 merge).
+ * Accumulates in fp32.
+ * Source: the daily.dev ExecuTorch summary, answer on exporting GGUF
+ * checkpoints (Q4_K/Q5_K/Q6_K GEMV; group-128 merge); the Core AI card's
+ * n-gram speculation paragraph and the PTE card ("Adjustments per variant")
+ * for the verify widths n_tok <= 16.
  * Long rows are split over several CTAs whose partial sums go to a split-K
  * scratch buffer of the current device, allocated by the library on first
  * need (never while the stream is being captured; a capture then runs the
@@ -125,23 +141,27 @@ kq_status kq_gemv(kq_format f, const void* W_blocks, const void* x_bf16,
                   float* y, int64_t N_out, int64_t K, int n_tok,
                   kq_stream_t stream);
 
-/* kq_gemv for callers that must not allocate device memory.  The reference
- * pages have no counterpart: this entry point exists for users of this
- * library.  Some callers cannot call cudaMalloc at the moment they compute:
- * code running while a stream is being captured into a CUDA graph, engines
- * that hand out all device memory from their own pool and forbid driver
- * allocations after start-up, and latency-critical loops that cannot afford
- * an allocation's implicit device synchronisation.  kq_gemv may allocate a
- * split-K scratch buffer on its first long-row call; this variant never
- * allocates and keeps that scratch in a fixed 2 MiB array compiled into the
- * library, which every GPU that loads the library holds until the process
- * exits.
+/* kq_gemv for callers that must not allocate device memory.
+ * Source: none -- the pages have no counterpart; this entry point exists
+ * for users of this library.  Some callers cannot call cudaMalloc at the
+ * moment they compute: code running while a stream is being captured into a
+ * CUDA graph, engines that hand out all device memory from their own pool
+ * and forbid driver allocations after start-up, and latency-critical loops
+ * that cannot afford an allocation's implicit device synchronisation.
+ * kq_gemv may allocate a split-K scratch buffer on its first long-row call;
+ * this variant never allocates (no cudaMalloc, cudaFree or allocating
+ * library call on any path) and keeps that scratch in a fixed 2 MiB array
+ * compiled into the library, which every GPU that loads the library holds
+ * until the process exits.
  *   Same arguments, requirements and result as kq_gemv (within the same
- *   tolerance; the same kernels run).
- *   Limits: a request whose split-K scratch would exceed the array (more
- *   than 16384 row tiles, or more partial sums than fit in 2 MiB - 64 KiB;
- *   roughly N_out * n_tok * segments > 500000) returns KQ_ERR_TOO_LARGE and
- *   launches nothing.
+ *   tolerance).  The kernels are kq_gemv's; where the fastest configuration
+ *   would need more split-K sums than the array holds, a configuration with
+ *   fewer K segments, or the next kernel kq_gemv would try, runs instead.
+ *   Limits: a request that the streaming and tensor-core kernels can serve
+ *   only with more than 16384 row tiles or more partial sums than fit in
+ *   2 MiB - 64 KiB (roughly N_out * n_tok * K-segments > 500000, e.g. rows
+ *   of 32768 weights at 4 tokens and 200000 outputs) returns
+ *   KQ_ERR_TOO_LARGE and launches nothing.
  *   Set-up: the first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current and caches it; make
  *   that first call before any stream capture.
@@ -154,11 +174,12 @@ kq_status kq_gemv_noalloc(kq_format f, const void* W_blocks, const void* x_bf16,
                           int64_t N_out, int64_t K, int n_tok, kq_stream_t stream);
 
 /* Several matrices of one format and one K that read the same activations,
- * computed in ONE launch: y_i = w^_i x for i < count (1 <= count <= 4).  The
- * Core AI card for Muse-Glimmer-30B ("The architecture, and what the port had
- * to do about it") folds q, k, v and the sigmoid attention gate, which all
- * read the pre-attention hidden state, into one qkvg projection; the SwiGLU
- * gate and up projections share their input the same way.
+ * computed in ONE launch: y_i = w^_i x for i < count (1 <= count <= 4).
+ * Source: the Core AI card for Muse-Glimmer-30B ("The architecture, and what
+ * the port had to do about it") folds q, k, v and the sigmoid attention
+ * gate, which all read the pre-attention hidden state, into one qkvg
+ * projection; the SwiGLU gate and up projections share their input the same
+ * way.
  *   W[i]     : device, N_out[i] x K matrix in format f, 16-B aligned
  *   y[i]     : device, fp32 [n_tok][N_out[i]], overwritten
  *   x_bf16   : device, bf16 [n_tok][K], 16-B aligned
@@ -167,9 +188,10 @@ kq_status kq_gemv_multi(kq_format f, int count, const void* const* W, float* con
                         const int64_t* N_out, const void* x_bf16, int64_t K, int n_tok,
                         kq_stream_t stream);
 
-/* One decoder layer's seven projections.  The Muse-Glimmer-30B Core AI card
- * ("The architecture, and what the port had to do about it") and the SGLang
- * day-0 post (architecture paragraph) describe GQA attention (q, k, v read the
+/* One decoder layer's seven projections.
+ * Source: the Muse-Glimmer-30B Core AI card ("The architecture, and what
+ * the port had to do about it") and the SGLang day-0 post (architecture
+ * paragraph) describe GQA attention (q, k, v read the
  * same hidden state; o reads the attention output) and a SwiGLU FFN (gate, up
  * read the same hidden state; down reads their product).  kq_layer_step runs
  * q/k/v as one launch on x_attn, then o on x_o, gate/up as one launch on
@@ -195,19 +217,27 @@ typedef struct {
 
 /* Requirements: q.K == k.K == v.K, gate.K == up.K, gate.N_out == up.N_out,
  * plus each matrix's own requirements.  Returns the first failing status;
- * on a validation failure nothing is launched. */
+ * on a validation failure nothing is launched.
+ * Source: the layer structure of the Core AI card's architecture section
+ * (see the layer types above); the product of each launch as kq_gemv. */
 kq_status kq_layer_step(const kq_layer* L, const kq_layer_io* io, int n_tok,
                         kq_stream_t stream);
 
 /* W_out[n][k] = w^[n][k] as fp32 (device, [N_out][K]).  Every w^ of these
  * formats is computed with at most one rounding (at the subtraction of the
  * min term), so the result is bit-exact: the fp32 round-to-nearest-even of
- * the exact value. */
+ * the exact value.
+ * Source: the dequantisation formulas of the GGUF K-quant layouts that the
+ * daily.dev summary names (answer on exporting GGUF checkpoints), written out
+ * above: w^ = d*sc*q - dmin*m (Q4_K, Q5_K, Q4_G128), d*sc*(q-32) (Q6_K). */
 kq_status kq_dequantize(kq_format f, const void* W_blocks, float* W_out,
                         int64_t N_out, int64_t K, kq_stream_t stream);
 
 /* Host-side quantiser for test and benchmark data (runs on the CPU, not on
- * the hot path).  W_host: fp32 [N_out][K]; blocks_host receives
+ * the hot path).
+ * Source: none -- the pages define no quantiser; this is this library's
+ * rounding quantiser (round to nearest, scales rounded outward), the reading
+ * chosen for test data.  W_host: fp32 [N_out][K]; blocks_host receives
  * kq_matrix_bytes(f, N_out, K) bytes.  Rounds q to nearest (ties to even)
  * and rounds d, dmin up to fp16 so every group's range is covered, which
  * bounds |w - w^| by half a quantisation step.  Q4_G128 takes its statistics
@@ -219,13 +249,17 @@ kq_status kq_quantize(kq_format f, const float* W_host, int64_t N_out,
  * Succeeds only if, in every super-block, sub-blocks 0..3 share one (sc, m)
  * and sub-blocks 4..7 share one (sc, m); otherwise returns
  * KQ_ERR_NOT_MERGEABLE and leaves g128_host unspecified.  The merged matrix
- * dequantises to bit-identical weights.  Source: the daily.dev ExecuTorch
- * summary (merge "when lossless" up to 128) and the SGLang post ("Q4KM ...
- * group size of 128"). */
+ * dequantises to bit-identical weights.
+ * Source: the daily.dev ExecuTorch summary, answer on exporting GGUF
+ * checkpoints (neighbouring sub-blocks that share scale and min are merged,
+ * where nothing is lost, into groups of up to 128 weights) and the SGLang
+ * day-0 post, GGUF paragraph (a Q4_K_M checkpoint with 128-weight groups). */
 kq_status kq_merge_g128(const void* q4k_host, int64_t N_out, int64_t K,
                         void* g128_host);
 
-/* Device-side health check.  The streaming kernels hand data between warps
+/* Device-side health check.
+ * Source: none in the pages; failure detection of this library's kernels.
+ * The streaming kernels hand data between warps
  * through shared-memory barriers; every wait is bounded (about two seconds),
  * and a wait that runs out makes the kernel stop early and count the event
  * in a device word instead of hanging.  This call synchronises `stream`,
@@ -236,7 +270,19 @@ kq_status kq_merge_g128(const void* q4k_host, int64_t N_out, int64_t K,
  * stream capture. */
 kq_status kq_device_status(kq_stream_t stream);
 
-/* Static string for a status code. */
+/* Test hook for the failure path above.  Launches one warp on `stream` that
+ * waits on a shared-memory barrier nothing completes, with the bounded wait
+ * shortened to about wait_us microseconds (1 <= wait_us <= 1000000): the wait
+ * runs out, the event is counted like any other timeout, and the kernel
+ * returns.  The next kq_device_status on that stream returns KQ_ERR_TIMEOUT
+ * (and re-arms the library's counters); later launches are unaffected.
+ * Nothing faults and nothing hangs.  Returns KQ_ERR_ARG for wait_us out of
+ * range, KQ_ERR_CUDA if the launch failed.
+ * Source: none in the pages; tests this library's failure detection. */
+kq_status kq_test_wait_timeout(unsigned int wait_us, kq_stream_t stream);
+
+/* Static string for a status code.
+ * Source: none in the pages. */
 const char* kq_status_str(kq_status s);
 
 #ifdef __cplusplus

@@ -11,7 +11,7 @@ Sources (see the header of ``kq_oracle.c`` for the per-function passages):
 the daily.dev summary "Fast on-device agentic AI with Muse Glimmer on
 ExecuTorch" (answer on exporting GGUF checkpoints: Q4_K/Q5_K/Q6_K GEMV and the
 lossless merge into groups of up to 128) and the SGLang day-0 post (GGUF
-paragraph: "Q4KM ... group size of 128").
+paragraph: a Q4_K_M checkpoint with 128-weight groups).
 
 Parity unpinned: GGUF bit-placement compatibility with real checkpoint files.
 """

@@ -18,7 +18,7 @@
  *    repeated, in this file's own words, at each decoder below.
  *  - The group-128 merged layout: the same page says adjacent sub-blocks with
  *    identical scale/min are merged into groups of up to 128 when lossless;
- *    the SGLang day-0 post names a "Q4KM format with a group size of 128".
+ *    the SGLang day-0 post names a Q4_K_M checkpoint with 128-weight groups.
  *    Reading taken: one (sc, m) per 128 weights, planar storage.
  *  - The product: y[t][n] = sum_k w^[n][k] x[t][k], in k order, in fp64,
  *    with bf16 x widened exactly, and A[t][n] = sum_k |w^[n][k] x[t][k]|,

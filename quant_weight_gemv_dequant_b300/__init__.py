@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
         L.kq_merge_g128.argtypes = [P, I64, I64, P]
         L.kq_device_status.argtypes = [P]
         L.kq_device_status.restype = I
+        L.kq_test_wait_timeout.argtypes = [ctypes.c_uint, P]
+        L.kq_test_wait_timeout.restype = I
         L.kq_status_str.argtypes = [I]
         L.kq_status_str.restype = ctypes.c_char_p
         for name in ("kq_gemv", "kq_gemv_multi", "kq_gemv_noalloc", "kq_layer_step", "kq_dequantize", "kq_quantize", "kq_merge_g128"):
@@ -115,6 +117,13 @@ def kq_device_status(stream=None, check=True) -> int:
     return _check(st, "kq_device_status") if check else st
 
 
+def kq_test_wait_timeout(wait_us: int, stream=None, check=True) -> int:
+    """Launch one warp whose bounded wait (about wait_us) runs out; the next
+    kq_device_status reports KQ_ERR_TIMEOUT.  For testing the failure path."""
+    st = lib().kq_test_wait_timeout(wait_us, _stream(stream))
+    return _check(st, "kq_test_wait_timeout") if check else st
+
+
 def kq_block_bytes(fmt: int) -> int:
     return lib().kq_block_bytes(fmt)
 
@@ -130,7 +139,8 @@ def kq_gemv(fmt, W, x, y, N_out, K, n_tok, stream=None, check=True) -> int:
 
 
 def kq_gemv_noalloc(fmt, W, x, y, N_out, K, n_tok, stream=None, check=True) -> int:
-    """kq_gemv that never allocates device memory (fixed 2 MiB scratch)."""
+    """kq_gemv that never allocates device memory (fixed 2 MiB scratch);
+    KQ_ERR_TOO_LARGE for requests beyond that array."""
     st = lib().kq_gemv_noalloc(fmt, _addr(W), _addr(x), _addr(y), N_out, K, n_tok,
                                _stream(stream))
     return _check(st, "kq_gemv_noalloc") if check else st

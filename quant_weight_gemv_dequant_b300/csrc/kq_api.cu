@@ -36,6 +36,16 @@ kq_status launch_status() {
   return cudaPeekAtLastError() == cudaSuccess ? KQ_OK : KQ_ERR_CUDA;
 }
 
+kq_status status_of(kq::StreamResult r) {
+  switch (r) {
+    case kq::StreamResult::kLaunched: return launch_status();
+    case kq::StreamResult::kTooLarge: return KQ_ERR_TOO_LARGE;
+    case kq::StreamResult::kFailed: return KQ_ERR_CUDA;
+    case kq::StreamResult::kNotServed: break;
+  }
+  return KQ_ERR_UNSUPPORTED;
+}
+
 }  // namespace
 
 extern "C" {
@@ -51,10 +61,8 @@ kq_status kq_gemv(kq_format f, const void* W_blocks, const void* x_bf16, float* 
   g.W[0] = static_cast<const uint8_t*>(W_blocks);
   g.y[0] = y;
   g.N[0] = static_cast<int>(N_out);
-  if (!kq::launch_gemv(f, g, static_cast<const uint16_t*>(x_bf16), static_cast<int>(K), n_tok,
-                       reinterpret_cast<cudaStream_t>(stream)))
-    return KQ_ERR_UNSUPPORTED;
-  return launch_status();
+  return status_of(kq::launch_gemv(f, g, static_cast<const uint16_t*>(x_bf16), static_cast<int>(K),
+                                   n_tok, reinterpret_cast<cudaStream_t>(stream), false));
 }
 
 kq_status kq_gemv_noalloc(kq_format f, const void* W_blocks, const void* x_bf16, float* y,
@@ -68,23 +76,8 @@ kq_status kq_gemv_noalloc(kq_format f, const void* W_blocks, const void* x_bf16,
   g.W[0] = static_cast<const uint8_t*>(W_blocks);
   g.y[0] = y;
   g.N[0] = static_cast<int>(N_out);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  switch (kq::launch_stream_noalloc(f, g, static_cast<const uint16_t*>(x_bf16),
-                                    static_cast<int>(K), n_tok, s)) {
-    case kq::NoAllocResult::kLaunched:
-      return launch_status();
-    case kq::NoAllocResult::kTooLarge:
-      return KQ_ERR_TOO_LARGE;
-    case kq::NoAllocResult::kFailed:
-      return KQ_ERR_CUDA;
-    case kq::NoAllocResult::kNotServed:
-      break;
-  }
-  // requests the streaming kernel does not serve need no scratch
-  if (!kq::launch_gemv(f, g, static_cast<const uint16_t*>(x_bf16), static_cast<int>(K), n_tok,
-                       s))
-    return KQ_ERR_UNSUPPORTED;
-  return launch_status();
+  return status_of(kq::launch_gemv(f, g, static_cast<const uint16_t*>(x_bf16), static_cast<int>(K),
+                                   n_tok, reinterpret_cast<cudaStream_t>(stream), true));
 }
 
 kq_status kq_gemv_multi(kq_format f, int count, const void* const* W, float* const* y,
@@ -103,10 +96,8 @@ kq_status kq_gemv_multi(kq_format f, int count, const void* const* W, float* con
     g.N[i] = static_cast<int>(N_out[i]);
   }
   g.count = count;
-  if (!kq::launch_gemv(f, g, static_cast<const uint16_t*>(x_bf16), static_cast<int>(K), n_tok,
-                       reinterpret_cast<cudaStream_t>(stream)))
-    return KQ_ERR_UNSUPPORTED;
-  return launch_status();
+  return status_of(kq::launch_gemv(f, g, static_cast<const uint16_t*>(x_bf16), static_cast<int>(K),
+                                   n_tok, reinterpret_cast<cudaStream_t>(stream), false));
 }
 
 kq_status kq_layer_step(const kq_layer* L, const kq_layer_io* io, int n_tok, kq_stream_t stream) {
@@ -145,10 +136,9 @@ kq_status kq_layer_step(const kq_layer* L, const kq_layer_io* io, int n_tok, kq_
         ++g.count;
         done[b] = true;
       }
-      if (!kq::launch_gemv(lead->format, g, static_cast<const uint16_t*>(xs[pending[a]]),
-                           static_cast<int>(lead->K), n_tok, s))
-        return KQ_ERR_UNSUPPORTED;
-      kq_status st = launch_status();
+      const kq_status st =
+          status_of(kq::launch_gemv(lead->format, g, static_cast<const uint16_t*>(xs[pending[a]]),
+                                    static_cast<int>(lead->K), n_tok, s, false));
       if (st != KQ_OK) return st;
     }
   }
@@ -164,6 +154,12 @@ kq_status kq_dequantize(kq_format f, const void* W_blocks, float* W_out, int64_t
   kq::launch_dequant(f, static_cast<const uint8_t*>(W_blocks), W_out, static_cast<int>(N_out),
                      static_cast<int>(K), reinterpret_cast<cudaStream_t>(stream));
   return launch_status();
+}
+
+kq_status kq_test_wait_timeout(unsigned int wait_us, kq_stream_t stream) {
+  if (wait_us < 1 || wait_us > 1000000) return KQ_ERR_ARG;
+  return kq::launch_wait_timeout_probe(wait_us, reinterpret_cast<cudaStream_t>(stream)) ? KQ_OK
+                                                                                       : KQ_ERR_CUDA;
 }
 
 kq_status kq_device_status(kq_stream_t stream) {

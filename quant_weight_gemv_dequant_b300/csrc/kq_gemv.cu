@@ -238,33 +238,20 @@ void launch_f(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStrea
 
 }  // namespace
 
-bool launch_gemv(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
-                 cudaStream_t s) {
-  // the streaming kernels serve n_tok <= 4 (CUDA cores, while x fits in
-  // shared memory) and 5..16 (tensor cores).  If the tensor-core kernel does
-  // not serve a request, its tokens run as consecutive CUDA-core launches of
-  // up to 4 tokens each (x and y rows of a token are contiguous, so a chunk
-  // is an offset view); anything else takes the warp-per-row kernel below
-  if (launch_stream(fmt, g, x, K, n_tok, s)) return true;
-  if (n_tok > 4) {
-    bool ok = true;
-    for (int t0 = 0; t0 < n_tok && ok; t0 += 4) {
-      const int nt = n_tok - t0 < 4 ? n_tok - t0 : 4;
-      GemvGroup gc = g;
-      for (int i = 0; i < g.count; ++i) gc.y[i] = g.y[i] + static_cast<int64_t>(t0) * g.N[i];
-      ok = launch_stream(fmt, gc, x + static_cast<int64_t>(t0) * K, K, nt, s);
-    }
-    if (ok) return true;
-    // a chunk could not be served (nothing launched for it): recompute all
-    // tokens with the kernel below, which overwrites every output
-  }
+StreamResult launch_gemv(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
+                         cudaStream_t s, bool noalloc) {
+  const StreamResult r = launch_stream(fmt, g, x, K, n_tok, s, noalloc);
+  if (r != StreamResult::kNotServed) return r;
+  // a shape the streaming kernels decline (x too large for shared memory
+  // even in bf16): the warp-per-row kernel, which overwrites every output
   switch (fmt) {
-    case kQ4K: launch_f<kQ4K>(g, x, K, n_tok, s); return true;
-    case kQ5K: launch_f<kQ5K>(g, x, K, n_tok, s); return true;
-    case kQ6K: launch_f<kQ6K>(g, x, K, n_tok, s); return true;
-    case kG128: launch_f<kG128>(g, x, K, n_tok, s); return true;
+    case kQ4K: launch_f<kQ4K>(g, x, K, n_tok, s); break;
+    case kQ5K: launch_f<kQ5K>(g, x, K, n_tok, s); break;
+    case kQ6K: launch_f<kQ6K>(g, x, K, n_tok, s); break;
+    case kG128: launch_f<kG128>(g, x, K, n_tok, s); break;
+    default: return StreamResult::kNotServed;
   }
-  return false;
+  return StreamResult::kLaunched;
 }
 
 void launch_dequant(int fmt, const uint8_t* W, float* out, int N, int K, cudaStream_t s) {

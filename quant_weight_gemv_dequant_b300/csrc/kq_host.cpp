@@ -18,8 +18,8 @@
 //
 // Merge: the daily.dev ExecuTorch summary (answer on exporting GGUF
 // checkpoints) merges adjacent sub-blocks with identical scale/min into
-// groups of up to 128 when lossless; the SGLang day-0 post names the "Q4KM
-// format with a group size of 128".
+// groups of up to 128 when lossless; the SGLang day-0 post names a Q4_K_M
+// checkpoint with 128-weight groups.
 #include <cmath>
 #include <cstdint>
 #include <cstring>

@@ -18,22 +18,28 @@ struct GemvGroup {
   int N[kMaxGroup];
 };
 
-// Returns false if the format / n_tok combination has no kernel.
-bool launch_gemv(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
-                 cudaStream_t stream);
+// Outcome of a launch request.  kNotServed: no configuration of the
+// streaming / tensor-core kernels serves it (nothing was launched);
+// kTooLarge: only configurations whose split-K sums exceed the fixed scratch
+// array of the no-allocation path would serve it; kFailed: a CUDA call failed.
+enum class StreamResult { kLaunched, kNotServed, kTooLarge, kFailed };
 
-// The streaming kernels: n_tok <= 4 on the CUDA cores, 5..16 on the tensor
-// cores; false if they do not serve the request.
-bool launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
-                   cudaStream_t stream);
+// The streaming and tensor-core kernels: n_tok 1 on the CUDA cores or (large
+// Q4_K / Q4_G128) the tensor cores, 2..16 on the tensor cores, else the
+// CUDA-core kernel in chunks of up to four tokens.  noalloc: split-K partial
+// sums go to the library's fixed device array instead of the per-device
+// buffer that grows with cudaMalloc.
+StreamResult launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
+                           cudaStream_t stream, bool noalloc);
 
-// kq_gemv_noalloc: the streaming kernels with their split-K scratch in a
-// fixed device array (no allocation).  kNotServed: no configuration of these
-// kernels serves the request; the caller may use a kernel that needs no
-// scratch.
-enum class NoAllocResult { kLaunched, kNotServed, kTooLarge, kFailed };
-NoAllocResult launch_stream_noalloc(int fmt, const GemvGroup& g, const uint16_t* x, int K,
-                                    int n_tok, cudaStream_t stream);
+// launch_stream, then, for requests it does not serve, the warp-per-row
+// kernel (which needs no scratch and serves every valid request).
+StreamResult launch_gemv(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
+                         cudaStream_t stream, bool noalloc);
+
+// One warp whose bounded wait (limit ~wait_us) runs out on a barrier that
+// nothing completes; the event is counted like any other timeout.
+bool launch_wait_timeout_probe(unsigned int wait_us, cudaStream_t stream);
 
 // Number of bounded waits that timed out since the last call (then cleared).
 bool read_wait_timeouts(unsigned int* count, cudaStream_t stream);

@@ -36,6 +36,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 #include <type_traits>
 
 #include "kq_decode.cuh"
@@ -90,15 +91,16 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 
 // Bounded, warp-uniform wait (every lane of the warp calls it): true once
 // the phase with this parity has completed for all lanes; false, with a
-// recorded timeout, if that takes longer than kWaitCycles.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
+// recorded timeout, if that takes longer than `limit` cycles.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               long long limit = kWaitCycles) {
   long long t0 = 0;
   for (int i = 0;; ++i) {
     const bool done = mbar_try(bar, parity);
     if (__all_sync(0xFFFFFFFFu, done)) return true;
     if (i == 0) {
       t0 = clock64();
-    } else if (__shfl_sync(0xFFFFFFFFu, (clock64() - t0 > kWaitCycles) ? 1 : 0, 0)) {
+    } else if (__shfl_sync(0xFFFFFFFFu, (clock64() - t0 > limit) ? 1 : 0, 0)) {
       if ((threadIdx.x & 31) == 0) atomicAdd(&g_wait_timeouts, 1u);
       return false;
     }
@@ -185,6 +187,13 @@ __device__ __forceinline__ uint32_t lop_mask_or(uint32_t w, uint32_t mask, uint3
   uint32_t d;
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(w), "r"(mask), "r"(magic));
   return d;   // (w & mask) | magic
+}
+// (a - b) on two bf16 halves.  Used as bf16(c + q) - bf16(c) = bf16(q): both
+// operands and the difference are small integers, so the result is exact.
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 __device__ __forceinline__ uint32_t bitsel(uint32_t a, uint32_t b, uint32_t m) {
   uint32_t d;
@@ -763,6 +772,14 @@ __device__ __forceinline__ float2 cvt_pair(uint32_t a, uint32_t b, uint32_t magi
   return r;
 }
 constexpr uint64_t kNegMagic2 = 0xCB000000CB000000ull;   // (-2^23, -2^23)
+// Q6_K: -(2^23 + 32 2^s) for the field shifts s = 0, 8, 16, so that
+// (2^23 + q 2^s) - (2^23 + 32 2^s) = (q - 32) 2^s exactly (both terms are
+// integers in [2^23, 2^24)): the signed weight without a separate -32 sum x
+// correction.  Halves: (s, s) for 0, 8, 16, and (0, 16) for the permuted byte.
+constexpr uint64_t kNegQ6s0 = 0xCB000020CB000020ull;
+constexpr uint64_t kNegQ6s8 = 0xCB002000CB002000ull;
+constexpr uint64_t kNegQ6s16 = 0xCB200000CB200000ull;
+constexpr uint64_t kNegQ6s0s16 = 0xCB200000CB000020ull;
 
 // The same on 64-bit register pairs: a .b64 operand of the packed f32x2
 // instructions is one aligned register pair by construction, so the hot loop
@@ -985,8 +1002,9 @@ __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl
 // holds t0 (low nibble) and t2 (high), ql[64h + 32 + l0 + l] holds t1 and t3,
 // qh[32h + l0 + l] the two high bits of each.  Each byte column gives the
 // pairs (t0, t2), (t1, t3), accumulated with packed fmas against the staged x
-// pairs; the scales apply as the pairs (d sc_t0, d sc_t2), (d sc_t1, d sc_t3)
-// and q - 32 as ds (S - 32 sx).  Records start on 2-byte boundaries: words
+// pairs; every 6-bit field converts straight to the signed (q - 32) 2^s (no
+// offset to remove afterwards), and the scales apply as the pairs (d sc_t0,
+// d sc_t2), (d sc_t1, d sc_t3).  Records start on 2-byte boundaries: words
 // are read aligned and shifted.  Word-outer order, as in stage_q4: one
 // word's x is live at a time and the scales are decoded after the products.
 template <int NT, int RT, int WC, int NR, bool XBF>
@@ -997,7 +1015,6 @@ __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl
   using L = XLayout<kQ6K, NT, XBF>;
   constexpr int kCW = G::kCW, QW = kCW / 16;   // words per t-run of the unit: 4, 2, 1
   const uint32_t magic = kMagic;
-  const uint64_t neg = kNegMagic2;
   const int h = un / (G::kUnitsPerSB / 2);
   const int u2 = un % (G::kUnitsPerSB / 2);
   const int l0 = u2 * (kCW / 4);
@@ -1045,15 +1062,16 @@ __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl
       const uint32_t q3 = bitsel(B[r][j] >> 4, H[r][j] >> 2, M);
       const uint32_t p02 = prmt(q0, q2, 0x0703u);   // byte 3 of q0 -> byte 0, of q2 -> byte 2
       const uint32_t p13 = prmt(q1, q3, 0x0703u);
+      // signed (q - 32) 2^s, exact (kNegQ6*)
       float2 c02[4], c13[4];
-      c02[0] = cvt_pair<0x3Fu, 0x3Fu>(q0, q2, magic, neg);
-      c02[1] = cvt_pair<0x3F00u, 0x3F00u>(q0, q2, magic, neg);
-      c02[2] = cvt_pair<0x3F0000u, 0x3F0000u>(q0, q2, magic, neg);
-      c02[3] = cvt_pair<0x3Fu, 0x3F0000u>(p02, p02, magic, neg);
-      c13[0] = cvt_pair<0x3Fu, 0x3Fu>(q1, q3, magic, neg);
-      c13[1] = cvt_pair<0x3F00u, 0x3F00u>(q1, q3, magic, neg);
-      c13[2] = cvt_pair<0x3F0000u, 0x3F0000u>(q1, q3, magic, neg);
-      c13[3] = cvt_pair<0x3Fu, 0x3F0000u>(p13, p13, magic, neg);
+      c02[0] = cvt_pair<0x3Fu, 0x3Fu>(q0, q2, magic, kNegQ6s0);
+      c02[1] = cvt_pair<0x3F00u, 0x3F00u>(q0, q2, magic, kNegQ6s8);
+      c02[2] = cvt_pair<0x3F0000u, 0x3F0000u>(q0, q2, magic, kNegQ6s16);
+      c02[3] = cvt_pair<0x3Fu, 0x3F0000u>(p02, p02, magic, kNegQ6s0s16);
+      c13[0] = cvt_pair<0x3Fu, 0x3Fu>(q1, q3, magic, kNegQ6s0);
+      c13[1] = cvt_pair<0x3F00u, 0x3F00u>(q1, q3, magic, kNegQ6s8);
+      c13[2] = cvt_pair<0x3F0000u, 0x3F0000u>(q1, q3, magic, kNegQ6s16);
+      c13[3] = cvt_pair<0x3Fu, 0x3F0000u>(p13, p13, magic, kNegQ6s0s16);
 #pragma unroll
       for (int k = 0; k < NT; ++k)
 #pragma unroll
@@ -1063,18 +1081,6 @@ __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl
         }
     }
   }
-  // sums of x over the unit's four t-runs, then the scales and q - 32
-  const uint32_t sxa = xs + static_cast<uint32_t>(L::bytes(static_cast<size_t>(NT) * p.kpad));
-  const int parts = p.kpad / G::kPart;
-  float2 sx02[NT], sx13[NT];
-#pragma unroll
-  for (int k = 0; k < NT; ++k) {
-    const float4 s4 =
-        lds_f4(sxa + 4 * (k * parts + (kb / 128) * (128 / G::kPart) + 4 * (l0 / G::kPart)));
-    sx02[k] = make_float2(s4.x, s4.y);
-    sx13[k] = make_float2(s4.z, s4.w);
-  }
-  const float2 m32 = make_float2(-32.0f, -32.0f);
   // scales of the unit's sub-blocks: t0 byte su, t1 su+2 (of S[0]), t2 su,
   // t3 su+2 (of S[1]); sign-extended with a byte permute
   const uint32_t sel0 = su | ((8 | su) << 4) | ((8 | su) << 8) | ((8 | su) << 12);
@@ -1091,8 +1097,8 @@ __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl
                                     d * static_cast<float>(static_cast<int>(prmt(S[1], 0, sel2))));
 #pragma unroll
     for (int k = 0; k < NT; ++k) {
-      acc[r][k] = __ffma2_rn(ds02, __ffma2_rn(m32, sx02[k], a02[r][k]), acc[r][k]);
-      acc[r][k] = __ffma2_rn(ds13, __ffma2_rn(m32, sx13[k], a13[r][k]), acc[r][k]);
+      acc[r][k] = __ffma2_rn(ds02, a02[r][k], acc[r][k]);
+      acc[r][k] = __ffma2_rn(ds13, a13[r][k], acc[r][k]);
     }
   }
 }
@@ -1275,15 +1281,18 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
 //
 // n_tok 5..16 (speculative verify): the products run on the tensor cores as
 // mma.sync m16n8k16 (bf16 operands, fp32 accumulators).  A = weights: a warp
-// owns 16 rows of a tile; each qs byte's nibble becomes one bf16 value
-// 128 + q (one LOP3 builds two: (w & 0x000F000F) | 0x43004300), exact.  B = x,
+// owns 16 rows of a tile; each qs byte's nibble becomes the exact bf16 value
+// q (one LOP3 builds two bf16 128 + q: (w & 0x000F000F) | 0x43004300, and one
+// bf16 subtraction of (128, 128) leaves (q, q); Q6_K subtracts 160 and gets
+// q - 32).  No offset is left in the products, so a record whose weights are
+// zero contributes exactly zero whatever its scales.  B = x,
 // eight tokens per mma (two mmas per A fragment for 9..16 tokens): the CTA's
 // K segment of x is staged once as bf16 in shared memory, one row per token
 // padded by 64 bytes so that the eight tokens of a fragment load hit
-// different banks.  Per sub-block the accumulator holds D = 128 Sx + sum q x, and a
-// second mma against an all-ones A gives Sx, so
-//   y += s1 D + s2 Sx,  s1 = d sc,  s2 = -(128 s1 + dmin m)       (Q4 family)
-//   y += s1 (D - 160 Sx), s1 = d sc                               (Q6_K: q - 32)
+// different banks.  Per sub-block the accumulator holds D = sum q x, and (Q4
+// family) a second mma against an all-ones A gives Sx for the min term, so
+//   y += s1 D + s2 Sx,  s1 = d sc,  s2 = -dmin m                  (Q4 family)
+//   y += s1 D,          s1 = d sc,  D = sum (q - 32) x            (Q6_K)
 // s1, s2 per (row, sub-block) are decoded once per stage into a per-warp
 // shared table.  The weight ring, tiling, split-K and bounded waits are those
 // of gemv_stream.
@@ -1351,13 +1360,17 @@ constexpr uint32_t kBf16Magic2 = 0x43004300u;   // bf16 (128, 128)
 __device__ __forceinline__ uint32_t sext_sel(uint32_t b) { return b | ((8u | b) * 0x1110u); }
 constexpr uint32_t kBf16One2 = 0x3F803F80u;     // bf16 (1, 1)
 
-// bf16 pairs (128 + q) of the fields under mask M in bytes (0, 1) and in
-// bytes (2, 3) of v: the two bytes of a pair are moved to the two halves
-// with a byte permute, so a pair is two consecutive positions.
+constexpr uint32_t kBf16Q6Zero2 = 0x43204320u;  // bf16 (160, 160) = 128 + the Q6_K zero point 32
+
+// Exact bf16 pairs of the fields under mask M in bytes (0, 1) and in bytes
+// (2, 3) of v: the two bytes of a pair are moved to the two halves with a
+// byte permute (a pair is two consecutive positions), one LOP3 makes the
+// bf16 (128 + field), and one bf16 subtraction of `off` leaves field + 128 -
+// off exactly: the field itself (off = 128) or Q6_K's q - 32 (off = 160).
 template <uint32_t M>
-__device__ __forceinline__ void bf16_pairs(uint32_t v, uint32_t& p01, uint32_t& p23) {
-  p01 = lop_or<M>(prmt(v, 0, 0x4140u), kBf16Magic2);
-  p23 = lop_or<M>(prmt(v, 0, 0x4342u), kBf16Magic2);
+__device__ __forceinline__ void bf16_pairs(uint32_t v, uint32_t off, uint32_t& p01, uint32_t& p23) {
+  p01 = bf16x2_sub(lop_or<M>(prmt(v, 0, 0x4140u), kBf16Magic2), off);
+  p23 = bf16x2_sub(lop_or<M>(prmt(v, 0, 0x4342u), kBf16Magic2), off);
 }
 
 // The per-warp scale table of one stage: lane -> (row = lane & 15, super-block
@@ -1393,7 +1406,7 @@ __device__ __forceinline__ void build_scale_table(const Params& p, const Tile& t
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
       const float s1 = dd.x * static_cast<float>((pr.y >> (8 * g)) & 0xFF);
-      const float s2 = -(128.0f * s1 + dd.y * static_cast<float>((pr.y >> (16 + 8 * g)) & 0xFF));
+      const float s2 = -(dd.y * static_cast<float>((pr.y >> (16 + 8 * g)) & 0xFF));
       const float4 e = make_float4(s1, s1, s2, s2);
 #pragma unroll
       for (int c = 2 * g; c < 2 * g + 2; ++c) {
@@ -1410,8 +1423,8 @@ __device__ __forceinline__ void build_scale_table(const Params& p, const Tile& t
       scale_pair6(scale_sel(c), hdr.y, hdr.z, hdr.w, scp, mnp);
       const float s1l = dd.x * static_cast<float>(scp & 0xFF);
       const float s1h = dd.x * static_cast<float>(scp >> 8);
-      const float s2l = -(128.0f * s1l + dd.y * static_cast<float>(mnp & 0xFF));
-      const float s2h = -(128.0f * s1h + dd.y * static_cast<float>(mnp >> 8));
+      const float s2l = -(dd.y * static_cast<float>(mnp & 0xFF));
+      const float s2h = -(dd.y * static_cast<float>(mnp >> 8));
       sts128(trow + ((s * 4 + c) * 2) * 16, make_float4(s1l, s1l, s2l, s2l));
       sts128(trow + ((s * 4 + c) * 2 + 1) * 16, make_float4(s1h, s1h, s2h, s2h));
     }
@@ -1477,11 +1490,11 @@ __device__ __forceinline__ void mma_stage_q4(const Params& p, const Tile& tl, in
             const int rlo = (2 * c + 28) & 31, rhi = (2 * c + 29) & 31;
             const uint32_t lo5 = bitsel(wd[i], __funnelshift_r(hq[i], hq[i], rlo), 0x0F0F0F0Fu);
             const uint32_t hi5 = bitsel(wd[i] >> 4, __funnelshift_r(hq[i], hq[i], rhi), 0x0F0F0F0Fu);
-            bf16_pairs<0x001F001Fu>(lo5, a[h][i][0], a[h][i][1]);
-            bf16_pairs<0x001F001Fu>(hi5, a[h][i][2], a[h][i][3]);
+            bf16_pairs<0x001F001Fu>(lo5, kBf16Magic2, a[h][i][0], a[h][i][1]);
+            bf16_pairs<0x001F001Fu>(hi5, kBf16Magic2, a[h][i][2], a[h][i][3]);
           } else {
-            bf16_pairs<0x000F000Fu>(wd[i], a[h][i][0], a[h][i][1]);
-            bf16_pairs<0x000F000Fu>(wd[i] >> 4, a[h][i][2], a[h][i][3]);
+            bf16_pairs<0x000F000Fu>(wd[i], kBf16Magic2, a[h][i][0], a[h][i][1]);
+            bf16_pairs<0x000F000Fu>(wd[i] >> 4, kBf16Magic2, a[h][i][2], a[h][i][3]);
           }
         }
       }
@@ -1522,8 +1535,6 @@ __device__ __forceinline__ void mma_stage_q6(const Params& p, const Tile& tl, in
                                              uint32_t xstride, float2 (&acc)[NB][2]) {
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const uint32_t ones = kBf16One2;
-  const float2 m160 = make_float2(-160.0f, -160.0f);
   uint32_t rec[2];
 #pragma unroll
   for (int s = 0; s < G::kSlabSB; ++s) {
@@ -1553,10 +1564,10 @@ __device__ __forceinline__ void mma_stage_q6(const Params& p, const Tile& tl, in
           const uint32_t q2 = bitsel(A[0] >> 4, H[0], M4);
           const uint32_t q1 = bitsel(B[0], H[0] << 2, M4);
           const uint32_t q3 = bitsel(B[0] >> 4, H[0] >> 2, M4);
-          bf16_pairs<0x003F003Fu>(q0, a[h][0][0], a[h][0][1]);
-          bf16_pairs<0x003F003Fu>(q1, a[h][1][0], a[h][1][1]);
-          bf16_pairs<0x003F003Fu>(q2, a[h][2][0], a[h][2][1]);
-          bf16_pairs<0x003F003Fu>(q3, a[h][3][0], a[h][3][1]);
+          bf16_pairs<0x003F003Fu>(q0, kBf16Q6Zero2, a[h][0][0], a[h][0][1]);
+          bf16_pairs<0x003F003Fu>(q1, kBf16Q6Zero2, a[h][1][0], a[h][1][1]);
+          bf16_pairs<0x003F003Fu>(q2, kBf16Q6Zero2, a[h][2][0], a[h][2][1]);
+          bf16_pairs<0x003F003Fu>(q3, kBf16Q6Zero2, a[h][3][0], a[h][3][1]);
         }
 #pragma unroll
         for (int tr = 0; tr < 4; ++tr) {
@@ -1570,14 +1581,10 @@ __device__ __forceinline__ void mma_stage_q6(const Params& p, const Tile& tl, in
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
             const uint2 b = lds64(xb + nb * 8 * xstride);
-            float d[4] = {0.f, 0.f, 0.f, 0.f}, sx[4] = {0.f, 0.f, 0.f, 0.f};
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
             mma_bf16(d, a[0][tr][0], a[1][tr][0], a[0][tr][1], a[1][tr][1], b.x, b.y);
-            mma_bf16(sx, ones, ones, ones, ones, b.x, b.y);
-            const float2 x01 = make_float2(sx[0], sx[1]);
-            const float2 tg = __ffma2_rn(m160, x01, make_float2(d[0], d[1]));
-            const float2 tg8 = __ffma2_rn(m160, x01, make_float2(d[2], d[3]));
-            acc[nb][0] = __ffma2_rn(s1, tg, acc[nb][0]);
-            acc[nb][1] = __ffma2_rn(s18, tg8, acc[nb][1]);
+            acc[nb][0] = __ffma2_rn(s1, make_float2(d[0], d[1]), acc[nb][0]);
+            acc[nb][1] = __ffma2_rn(s18, make_float2(d[2], d[3]), acc[nb][1]);
           }
         }
       }
@@ -1777,13 +1784,16 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC <= 4 ? 2 : 1)
 // a super-block, D[row][n] is the dot product of sub-block n alone, the
 // quantity one scale multiplies:
 //   y_row += s1[n] D[row][n] + s2[n] Sx[n]
-// A = bf16(128 + q) (one LOP3 per two weights: (w & 0x000F000F) | 0x43004300
-// is exact), s1 = d sc, s2 = -(128 s1 + dmin m), Sx[n] the sum of x over
-// sub-block n, staged once per launch.  Lane t takes chunk t of the
+// A = bf16(q), exact: one LOP3 per two weights builds bf16 (128 + q, 128 +
+// q) as (w & 0x000F000F) | 0x43004300 and one bf16 subtraction of (128, 128)
+// leaves (q, q), so no offset term remains in D (a record of zero weights
+// gives D = 0 whatever its scales); s1 = d sc, s2 = -dmin m, Sx[n] the sum of
+// x over sub-block n, staged once per launch.  Lane t takes chunk t of the
 // super-block (sub-block 2t: low nibbles -> slots 2t.., sub-block 2t+1: high
 // nibbles -> slots 2t+8..); word m of the chunk gives mma 2m (bytes 0, 2) and
-// 2m+1 (bytes 1, 3).  Per weight: half a LOP3 plus the shifts that bring the
-// next byte's nibbles down; per sub-block and row: one scale pair.  (Q5_K and
+// 2m+1 (bytes 1, 3).  Per weight: half a LOP3, half a bf16 subtraction (on
+// the FMA pipe) plus the shifts that bring the next byte's nibbles down; per
+// sub-block and row: one scale pair.  (Q5_K and
 // Q6_K would need their fields assembled first, which costs more integer
 // work than their CUDA-core path; they stay on gemv_stream.)
 // The column-n lane of each slot pair loads the x entries of sub-block n in
@@ -1824,44 +1834,136 @@ struct TGeo {
 };
 
 // Shared layout before the ring: the staged x of the K segment (kpad values
-// as bf16, each group of four positions (a, b, c, d) stored as (a, c, b, d),
+// as fp16, each group of four positions (a, b, c, d) stored as (a, c, b, d),
 // so that 32-bit entry i of a sub-block holds positions 4 (i >> 1) + (i & 1)
-// and that + 2), then Sx (the fp32 sum of x over every sub-block), then 64
-// zero bytes, then the reducer's two row-sum buffers of `rows` floats.
+// and that + 2), then Sx (the fp32 sum of x over every sub-block), then the
+// column scale of every sub-block (see stage_x_tc_raw), then 64 zero bytes,
+// then the reducer's two row-sum buffers of `rows` floats.
 __host__ __device__ constexpr uint32_t tc_x_only(int kpad, int sub) {
-  return (2u * static_cast<uint32_t>(kpad) + 4u * static_cast<uint32_t>(kpad / sub) + 64u + 15u) &
+  return (2u * static_cast<uint32_t>(kpad) + 8u * static_cast<uint32_t>(kpad / sub) + 64u + 15u) &
          ~15u;
 }
 __host__ __device__ constexpr uint32_t tc_x_bytes(int kpad, int sub, int rows) {
   return (tc_x_only(kpad, sub) + 8u * static_cast<uint32_t>(rows) + 127u) & ~127u;
 }
 
+// x of a K segment for the tensor-core product (fp16 operands), with the
+// sum of x over every sub-block (fp32, for the min term).  The products need
+// x exactly; bf16 x is exact in fp16 within fp16's exponent range, so every
+// sub-block is scaled by a power of two 2^-f chosen from its own largest |x|
+// (which lands in [2^14, 2^15)): then every value of the sub-block within a
+// factor 2^31 of its largest converts exactly (fp16 subnormals reach 2^-24),
+// and smaller ones round (contributing less than 2^-38 of the largest |x|
+// each).  The sub-block's column scale, stored beside Sx, undoes 2^-f: 2^f
+// for an even sub-block (low nibbles, A = q) and 2^(f-4) for an odd one
+// (high nibbles, A = 16 q).  bf16 subnormal x (below 2^-126) is not kept.
 template <int S>
-__device__ void stage_x_tc(const Params& p, uint32_t xsh, int kbase) {
-  const int nch = p.kpad / 8;   // 16-byte chunks (a multiple of 32)
-  const uint32_t xsum = xsh + 2u * static_cast<uint32_t>(p.kpad);
+__device__ void stage_x_tc_raw(const uint16_t* x, int K, int kpad, uint32_t xsh, int kbase) {
+  static_assert(S == 32, "one sub-block is four lanes of eight positions");
+  const int nch = kpad / 8;   // 16-byte chunks (a multiple of 32)
+  const uint32_t xsum = xsh + 2u * static_cast<uint32_t>(kpad);
+  const uint32_t xscl = xsum + 4u * static_cast<uint32_t>(kpad / S);
   const int lane = threadIdx.x & 31;
   for (int base = static_cast<int>(threadIdx.x) & ~31; base < nch;
        base += static_cast<int>(blockDim.x)) {
     const int c = base + lane;
     const int k = kbase + 8 * c;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (k < p.K) v = ldg_nc_v4(p.x + k);
-    sts128u(xsh + 16u * c, make_uint4(prmt(v.x, v.y, 0x5410u), prmt(v.x, v.y, 0x7632u),
-                                      prmt(v.z, v.w, 0x5410u), prmt(v.z, v.w, 0x7632u)));
+    if (k < K) v = ldg_nc_v4(x + k);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float sum = 0.0f;
+    float f[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      sum += __uint_as_float(w[j] << 16) + __uint_as_float(w[j] & 0xFFFF0000u);
+    for (int j = 0; j < 4; ++j) {
+      f[2 * j] = __uint_as_float(w[j] << 16);
+      f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+    float sum = 0.0f, amax = 0.0f;
 #pragma unroll
-    for (int m = 1; m < S / 8; m <<= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, m);
+    for (int j = 0; j < 4; ++j) {
+      sum += f[2 * j] + f[2 * j + 1];
+      amax = fmaxf(amax, fmaxf(fabsf(f[2 * j]), fabsf(f[2 * j + 1])));
+    }
+#pragma unroll
+    for (int m = 1; m < S / 8; m <<= 1) {
+      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, m);
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
+    }
+    int fs = amax > 0.0f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 14 : 0;
+    fs = fs < -100 ? -100 : (fs > 100 ? 100 : fs);
+    const float down = __uint_as_float(static_cast<uint32_t>(127 - fs) << 23);   // 2^-fs, exact
+    uint32_t e[4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {   // entries (p0, p2), (p1, p3) of each group of four
+      const __half2 a = __floats2half2_rn(f[4 * j] * down, f[4 * j + 2] * down);
+      const __half2 b = __floats2half2_rn(f[4 * j + 1] * down, f[4 * j + 3] * down);
+      e[2 * j] = *reinterpret_cast<const uint32_t*>(&a);
+      e[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    sts128u(xsh + 16u * c, make_uint4(e[0], e[1], e[2], e[3]));
     if ((c & (S / 8 - 1)) == 0) {
-      asm volatile("st.shared.f32 [%0], %1;" ::"r"(xsum + 4u * (c / (S / 8))), "f"(sum) : "memory");
+      const int sb = c / (S / 8);
+      const float scale = __uint_as_float(static_cast<uint32_t>(127 + fs - 4 * (sb & 1)) << 23);
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(xsum + 4u * sb), "f"(sum) : "memory");
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(xscl + 4u * sb), "f"(scale) : "memory");
     }
   }
   if (threadIdx.x < 4)
-    sts128u(xsum + 4u * static_cast<uint32_t>(p.kpad / S) + 16u * threadIdx.x, make_uint4(0, 0, 0, 0));
+    sts128u(xscl + 4u * static_cast<uint32_t>(kpad / S) + 16u * threadIdx.x, make_uint4(0, 0, 0, 0));
+}
+
+template <int S>
+__device__ void stage_x_tc(const Params& p, uint32_t xsh, int kbase) {
+  stage_x_tc_raw<S>(p.x, p.K, p.kpad, xsh, kbase);
+}
+
+constexpr uint32_t kF16Magic2 = 0x64006400u;   // fp16 (1024, 1024)
+
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The single-token tensor-core product of one super-block for rows g and
+// g + 8 of a 16-row tile: lane t's qs chunk of each row starts at qa0 / qa1
+// (32 bytes), its B operands (the staged fp16 x of its column, or the zero
+// block) at xlo / xhi.  A is exact in fp16: one LOP3 makes (1024 + q) from
+// the low nibbles of bytes (0, 2) (mask 0x000F000F) and (1024 + 16 q) from
+// the high nibbles in place (mask 0x00F000F0: fp16's ten mantissa bits hold
+// bits 4..7), one fp16 subtraction of 1024 leaves q or 16 q; bytes (1, 3) go
+// through the same after one shift by 8.  The column scales of the staged x
+// absorb the factor 16 of the high nibbles.  d[0] / d[1]: the two mma
+// chains (bytes 0, 2 / bytes 1, 3); their sum per column is the dot product
+// of that column's sub-block.
+__device__ __forceinline__ void tc_sb_product(uint32_t qa0, uint32_t qa1, uint32_t xlo,
+                                              uint32_t xhi, float (&d)[2][4]) {
+  const uint32_t magic = kF16Magic2;
+  auto lo = [&](uint32_t w) { return f16x2_sub(lop_mask_or(w, 0x000F000Fu, magic), magic); };
+  auto hi = [&](uint32_t w) { return f16x2_sub(lop_mask_or(w, 0x00F000F0u, magic), magic); };
+#pragma unroll
+  for (int hv = 0; hv < 2; ++hv) {   // words 4 hv .. 4 hv + 3 of the chunk
+    const uint4 w0 = lds128(qa0 + 16 * hv), w8 = lds128(qa1 + 16 * hv);
+    const uint4 bl0 = lds128(xlo + 32 * hv), bl1 = lds128(xlo + 32 * hv + 16);
+    const uint4 bh0 = lds128(xhi + 32 * hv), bh1 = lds128(xhi + 32 * hv + 16);
+    const uint32_t W[2][4] = {{w0.x, w0.y, w0.z, w0.w}, {w8.x, w8.y, w8.z, w8.w}};
+    const uint32_t BL[8] = {bl0.x, bl0.y, bl0.z, bl0.w, bl1.x, bl1.y, bl1.z, bl1.w};
+    const uint32_t BH[8] = {bh0.x, bh0.y, bh0.z, bh0.w, bh1.x, bh1.y, bh1.z, bh1.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t a = W[0][m], b = W[1][m];
+      const uint32_t a8 = a >> 8, b8 = b >> 8;
+      mma_f16(d[0], lo(a), lo(b), hi(a), hi(b), BL[2 * m], BH[2 * m]);
+      mma_f16(d[1], lo(a8), lo(b8), hi(a8), hi(b8), BL[2 * m + 1], BH[2 * m + 1]);
+    }
+  }
 }
 
 // y += s1 D + s2 Sx for rows g (h = 0) and g+8 (h = 1), columns (2t, 2t+1)
@@ -1887,7 +1989,7 @@ __device__ __forceinline__ void tc_scales_q4(const Params& p, const Tile& tl, in
     const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
     const int grp = t >> 1;
     const float a = dd.x * static_cast<float>((pr.y >> (8 * grp)) & 0xFF);
-    const float b = -(128.0f * a + dd.y * static_cast<float>((pr.y >> (16 + 8 * grp)) & 0xFF));
+    const float b = -(dd.y * static_cast<float>((pr.y >> (16 + 8 * grp)) & 0xFF));
     s1 = make_float2(a, a);
     s2 = make_float2(b, b);
   } else {
@@ -1896,8 +1998,7 @@ __device__ __forceinline__ void tc_scales_q4(const Params& p, const Tile& tl, in
     uint32_t scp, mnp;
     scale_pair6(ss, hdr.y, hdr.z, hdr.w, scp, mnp);
     s1 = make_float2(dd.x * static_cast<float>(scp & 0xFF), dd.x * static_cast<float>(scp >> 8));
-    s2 = make_float2(-(128.0f * s1.x + dd.y * static_cast<float>(mnp & 0xFF)),
-                     -(128.0f * s1.y + dd.y * static_cast<float>(mnp >> 8)));
+    s2 = make_float2(-(dd.y * static_cast<float>(mnp & 0xFF)), -(dd.y * static_cast<float>(mnp >> 8)));
   }
 }
 
@@ -1909,10 +2010,9 @@ __device__ __forceinline__ void tc_stage_q4(const Params& p, const Tile& tl, int
   constexpr int F = G::kF;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const uint32_t magic = 0x43004300u;
-  const uint32_t mask = 0x000F000Fu;
   const uint32_t xsum = xsh + 2u * static_cast<uint32_t>(p.kpad);
-  const uint32_t zero = xsum + 4u * static_cast<uint32_t>(p.kpad / 32);
+  const uint32_t xscl = xsum + 4u * static_cast<uint32_t>(p.kpad / 32);
+  const uint32_t zero = xscl + 4u * static_cast<uint32_t>(p.kpad / 32);
   const bool act_lo = g == 2 * t, act_hi = g == 2 * t + 1;   // column g of the B operand
 #pragma unroll
   for (int s = 0; s < G::kSlabSB; ++s) {
@@ -1927,32 +2027,13 @@ __device__ __forceinline__ void tc_stage_q4(const Params& p, const Tile& tl, int
       qa[h] = (F == kG128) ? rs + 128 * s + 32 * t : rs + G::kBB * s + 16 + 32 * t;
     }
     float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-    for (int hv = 0; hv < 2; ++hv) {   // words 4 hv .. 4 hv + 3 of the chunk
-      const uint4 w0 = lds128(qa[0] + 16 * hv), w8 = lds128(qa[1] + 16 * hv);
-      const uint4 bl0 = lds128(xlo + 32 * hv), bl1 = lds128(xlo + 32 * hv + 16);
-      const uint4 bh0 = lds128(xhi + 32 * hv), bh1 = lds128(xhi + 32 * hv + 16);
-      const uint32_t W[2][4] = {{w0.x, w0.y, w0.z, w0.w}, {w8.x, w8.y, w8.z, w8.w}};
-      const uint32_t BL[8] = {bl0.x, bl0.y, bl0.z, bl0.w, bl1.x, bl1.y, bl1.z, bl1.w};
-      const uint32_t BH[8] = {bh0.x, bh0.y, bh0.z, bh0.w, bh1.x, bh1.y, bh1.z, bh1.w};
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        // nibbles at bits 0.. of every byte: low (sub-block 2t), high (2t+1)
-        const uint32_t lo[2] = {W[0][m], W[1][m]};
-        const uint32_t hi[2] = {W[0][m] >> 4, W[1][m] >> 4};
-        mma_bf16(d[0], lop_mask_or(lo[0], mask, magic), lop_mask_or(lo[1], mask, magic),
-                 lop_mask_or(hi[0], mask, magic), lop_mask_or(hi[1], mask, magic), BL[2 * m],
-                 BH[2 * m]);
-        mma_bf16(d[1], lop_mask_or(lo[0] >> 8, mask, magic), lop_mask_or(lo[1] >> 8, mask, magic),
-                 lop_mask_or(hi[0] >> 8, mask, magic), lop_mask_or(hi[1] >> 8, mask, magic),
-                 BL[2 * m + 1], BH[2 * m + 1]);
-      }
-    }
+    tc_sb_product(qa[0], qa[1], xlo, xhi, d);
     float2 s1g, s2g, s1h, s2h;
     tc_scales_q4<G>(p, tl, sl, st, rbase + g, s, ss, t, s1g, s2g);
     tc_scales_q4<G>(p, tl, sl, st, rbase + g + 8, s, ss, t, s1h, s2h);
     const float2 sx = lds_f2(xsum + 4u * (8 * sbx + 2 * t));
-    tc_epilogue(acc, d, s1g, s2g, s1h, s2h, sx);
+    const float2 cs = lds_f2(xscl + 4u * (8 * sbx + 2 * t));   // column scales
+    tc_epilogue(acc, d, __fmul2_rn(s1g, cs), s2g, __fmul2_rn(s1h, cs), s2h, sx);
   }
 }
 
@@ -2152,9 +2233,9 @@ __global__ void __launch_bounds__((WC + 2) * 32, WC <= 8 ? 2 : 1)
 // positions of one sub-block: lane t takes bytes 8t .. 8t+7 of a chunk, and
 // word m of them gives slots (2t, 2t+1) <- bytes (0, 2) and (2t+8, 2t+9) <-
 // bytes (1, 3): the low nibbles for the chunk's first sub-block, the high
-// nibbles (one more shift) for its second.  Two mmas per sub-block, token
-// block and row tile, then
-//   y[tok] += s1 D + s2 Sx[tok]
+// nibbles (one more shift) for its second; A = bf16(q) exactly, as in
+// gemv_tc1.  Two mmas per sub-block, token block and row tile, then
+//   y[tok] += s1 D + s2 Sx[tok],  s1 = d sc, s2 = -dmin m
 // per (row, sub-block), with s1, s2 from a per-warp table built once per
 // super-block (each lane decodes the four chunks of one row) and Sx staged
 // with x.  The staged x: token rows of kpad bf16 values, each group of four
@@ -2243,7 +2324,7 @@ __device__ __forceinline__ void tcv_scale_table(const Params& p, const Tile& tl,
 #pragma unroll
     for (int grp = 0; grp < 2; ++grp) {
       const float a = dd.x * static_cast<float>((pr.y >> (8 * grp)) & 0xFF);
-      const float b = -(128.0f * a + dd.y * static_cast<float>((pr.y >> (16 + 8 * grp)) & 0xFF));
+      const float b = -(dd.y * static_cast<float>((pr.y >> (16 + 8 * grp)) & 0xFF));
 #pragma unroll
       for (int j = 4 * grp; j < 4 * grp + 4; ++j) sts_f2(te + 16 * j, a, b);
     }
@@ -2256,8 +2337,8 @@ __device__ __forceinline__ void tcv_scale_table(const Params& p, const Tile& tl,
       scale_pair6(scale_sel(c), hdr.y, hdr.z, hdr.w, scp, mnp);
       const float a0 = dd.x * static_cast<float>(scp & 0xFF);
       const float a1 = dd.x * static_cast<float>(scp >> 8);
-      sts_f2(te + 32 * c, a0, -(128.0f * a0 + dd.y * static_cast<float>(mnp & 0xFF)));
-      sts_f2(te + 32 * c + 16, a1, -(128.0f * a1 + dd.y * static_cast<float>(mnp >> 8)));
+      sts_f2(te + 32 * c, a0, -(dd.y * static_cast<float>(mnp & 0xFF)));
+      sts_f2(te + 32 * c + 16, a1, -(dd.y * static_cast<float>(mnp >> 8)));
     }
   }
 }
@@ -2301,10 +2382,10 @@ __device__ __forceinline__ void tcv_stage_q4(const Params& p, const Tile& tl, in
           const uint32_t W[2] = {wv.x, wv.y};
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
-            l02[rt][h][m] = lop_mask_or(W[m], mask, magic);
-            l13[rt][h][m] = lop_mask_or(W[m] >> 8, mask, magic);
-            h02[rt][h][m] = lop_mask_or(W[m] >> 4, mask, magic);
-            h13[rt][h][m] = lop_mask_or(W[m] >> 12, mask, magic);
+            l02[rt][h][m] = bf16x2_sub(lop_mask_or(W[m], mask, magic), magic);
+            l13[rt][h][m] = bf16x2_sub(lop_mask_or(W[m] >> 8, mask, magic), magic);
+            h02[rt][h][m] = bf16x2_sub(lop_mask_or(W[m] >> 4, mask, magic), magic);
+            h13[rt][h][m] = bf16x2_sub(lop_mask_or(W[m] >> 12, mask, magic), magic);
           }
         }
       const int jlo = 8 * sbx + 2 * c;   // sub-block of the segment (low nibbles)
@@ -2475,6 +2556,231 @@ __global__ void __launch_bounds__((WC + 2) * 32, WC <= 4 ? 2 : 1)
   }
 }
 
+// ===================================================== small-launch kernel
+//
+// n_tok = 1 on Q4_K / Q4_G128 launches of a few megabytes (the attention
+// projections of a decoder layer).  Such a launch streams its weights in a
+// couple of microseconds, so what it costs beyond that is fixed: launch,
+// waiting for the previous kernel, staging x, handing partial sums between
+// CTAs.  This kernel keeps that small:
+//   * one wave of CTAs (at most one per SM); CTA c owns the 16-row tiles
+//     [c T / C, (c+1) T / C) over all of K, so no partial sum leaves a CTA;
+//   * warp w owns slice (tile w / ks, K slice w % ks) of at most sbs
+//     super-blocks; before waiting for the previous kernel its lanes copy
+//     the slice's 16 row segments into the warp's part of shared memory with
+//     cp.async.bulk (one mbarrier per warp counts the bytes), so every weight
+//     byte of the launch is requested at once, while the previous kernel
+//     finishes;
+//   * after griddepcontrol.wait the CTA stages x as gemv_tc1 does, and each
+//     warp runs gemv_tc1's tensor-core product (exact bf16 q, the eight n8
+//     columns carrying the eight sub-blocks of a super-block) on its slice as
+//     soon as its bytes have landed;
+//   * the ks slice sums of a row are added in slice order in shared memory
+//     (a fixed order: the result does not depend on timing) and written.
+// Row segments are copied at a pitch that is an odd multiple of 16 bytes, so
+// the eight rows a warp reads at once fall in different bank groups.
+
+constexpr int kSmallMaxWarps = 24;   // 768 threads: registers for the product without spills
+
+struct SmallParams {
+  GemvGroup g;
+  const uint16_t* x;
+  int K, nsb;
+  int tiles;                  // 16-row tiles of the group (a tile lies in one matrix)
+  int tile_end[kMaxGroup];    // cumulative tile counts per matrix
+  int ks;                     // K slices per tile (warps per tile)
+  int sbs;                    // super-blocks per slice (the last slice may have fewer)
+  int max_tiles;              // most tiles one CTA owns
+  uint32_t pitch;             // shared bytes per row of a slice: records (Q4_G128: q plane)
+  uint32_t ppitch;            // Q4_G128: shared bytes per row of the slice's params (+ halo)
+  uint32_t warp_bytes;        // shared bytes per warp: 16 rows x (pitch + ppitch), 128-aligned
+  uint32_t x_bytes;           // staged x, Sx, zero block and the slice sums, 128-aligned
+};
+
+__device__ __forceinline__ Tile small_tile(const SmallParams& p, int t) {
+  int mi = 0, base = 0;
+#pragma unroll
+  for (int i = 0; i < kMaxGroup - 1; ++i)
+    if (i < p.g.count - 1 && t >= p.tile_end[i]) {
+      mi = i + 1;
+      base = p.tile_end[i];
+    }
+  Tile r;
+  r.mi = mi;
+  r.row0 = (t - base) * 16;
+  r.rcnt = min(16, pick(p.g.N, mi) - r.row0);
+  return r;
+}
+
+// Issue the bulk copies of this warp's slice: lane r < 16 copies row r's
+// segment; returns the bytes the copies deliver (summed over the warp).
+// Q4_G128 param segments start on 8-byte boundaries: each is copied from
+// the 16-byte boundary at or below it (the consumer skips the offset), and
+// bytes past the plane's last 16-byte boundary are loaded with plain loads.
+template <int F>
+__device__ __forceinline__ uint32_t small_issue(const SmallParams& p, const Tile& tl, int sb0,
+                                                int nsl, uint32_t wreg, uint32_t bar,
+                                                uint8_t* smem) {
+  const int lane = threadIdx.x & 31;
+  uint32_t tx = 0;
+  if (lane < tl.rcnt) {
+    const uint8_t* W = pick(p.g.W, tl.mi);
+    const int64_t N = pick(p.g.N, tl.mi);
+    const int64_t idx = (tl.row0 + lane) * static_cast<int64_t>(p.nsb) + sb0;
+    if constexpr (F == kG128) {
+      const uint32_t qb = static_cast<uint32_t>(nsl) * 128u;
+      bulk_g2s(wreg + lane * p.pitch, W + idx * 128, qb, bar);
+      tx += qb;
+      const uint8_t* P = W + N * p.nsb * 128;
+      const int64_t off = idx * 8, end = off + 8 * nsl;
+      const int64_t lo = off & ~int64_t{15};
+      const int64_t cap = (N * p.nsb * 8) & ~int64_t{15};
+      int64_t hi = (end + 15) & ~int64_t{15};
+      if (hi > cap) hi = cap;
+      const uint32_t dst = wreg + 16u * p.pitch + lane * p.ppitch;
+      if (hi > lo) {
+        bulk_g2s(dst, P + lo, static_cast<uint32_t>(hi - lo), bar);
+        tx += static_cast<uint32_t>(hi - lo);
+      }
+      for (int64_t b = (hi > lo ? hi : lo); b < end; ++b)
+        smem[(dst - smem_addr(smem)) + (b - lo)] = __ldg(P + b);
+    } else {
+      const uint32_t bytes = static_cast<uint32_t>(nsl) * block_bytes(F);
+      bulk_g2s(wreg + lane * p.pitch, W + idx * block_bytes(F), bytes, bar);
+      tx += bytes;
+    }
+  }
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) tx += __shfl_xor_sync(0xFFFFFFFFu, tx, m);
+  return tx;
+}
+
+// One super-block s of this warp's slice (rows g, g + 8 of the tile; lane t
+// takes chunk t): gemv_tc1's product, operands from the warp's region.
+template <int F>
+__device__ __forceinline__ void small_sb_q4(const SmallParams& p, uint32_t wreg, int s, int sbx,
+                                            int64_t idx_g, int64_t idx_g8, uint32_t xsh,
+                                            const ScaleSel& ss, float2 (&acc)[2]) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t xsum = xsh + 2u * static_cast<uint32_t>(p.K);
+  const uint32_t xscl = xsum + 4u * static_cast<uint32_t>(p.K / 32);
+  const uint32_t zero = xscl + 4u * static_cast<uint32_t>(p.K / 32);
+  const bool act_lo = g == 2 * t, act_hi = g == 2 * t + 1;   // column g of the B operand
+  const uint32_t xlo = act_lo ? xsh + 64u * (8 * sbx + 2 * t) : zero;
+  const uint32_t xhi = act_hi ? xsh + 64u * (8 * sbx + 2 * t + 1) : zero;
+  uint32_t qa[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t rs = wreg + (g + 8 * h) * p.pitch;
+    qa[h] = (F == kG128) ? rs + 128 * s + 32 * t : rs + block_bytes(F) * s + 16 + 32 * t;
+  }
+  float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  tc_sb_product(qa[0], qa[1], xlo, xhi, d);
+  // (s1, s2) of sub-blocks (2t, 2t+1) of rows g and g + 8
+  float2 s1[2], s2[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t rs = wreg + (g + 8 * h) * p.pitch;
+    if constexpr (F == kG128) {
+      const int64_t idx = h ? idx_g8 : idx_g;
+      const uint32_t pa = wreg + 16u * p.pitch + (g + 8 * h) * p.ppitch +
+                          static_cast<uint32_t>((idx * 8) & 15) + 8 * s;
+      const uint2 pr = lds64(pa);
+      const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
+      const int grp = t >> 1;
+      const float a = dd.x * static_cast<float>((pr.y >> (8 * grp)) & 0xFF);
+      const float b = -(dd.y * static_cast<float>((pr.y >> (16 + 8 * grp)) & 0xFF));
+      s1[h] = make_float2(a, a);
+      s2[h] = make_float2(b, b);
+    } else {
+      const uint4 hdr = lds128(rs + block_bytes(F) * s);
+      const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
+      uint32_t scp, mnp;
+      scale_pair6(ss, hdr.y, hdr.z, hdr.w, scp, mnp);
+      s1[h] = make_float2(dd.x * static_cast<float>(scp & 0xFF), dd.x * static_cast<float>(scp >> 8));
+      s2[h] = make_float2(-(dd.y * static_cast<float>(mnp & 0xFF)), -(dd.y * static_cast<float>(mnp >> 8)));
+    }
+  }
+  const float2 sx = lds_f2(xsum + 4u * (8 * sbx + 2 * t));
+  const float2 cs = lds_f2(xscl + 4u * (8 * sbx + 2 * t));   // column scales
+  tc_epilogue(acc, d, __fmul2_rn(s1[0], cs), s2[0], __fmul2_rn(s1[1], cs), s2[1], sx);
+}
+
+template <int F>
+__global__ void __launch_bounds__(kSmallMaxWarps * 32, 1) gemv_small(const __grid_constant__ SmallParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kSmallMaxWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = static_cast<int>(gridDim.x);
+  const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * p.tiles / C);
+  const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * p.tiles / C);
+  const int lt = warp / p.ks, j = warp % p.ks;
+  const bool active = t0 + lt < t1;           // warp-uniform
+  const int sb0 = j * p.sbs;
+  const int nsl = min(p.sbs, p.nsb - sb0);    // >= 1 (no empty slices)
+  const uint32_t xsh = smem_addr(smem);
+  const uint32_t red = xsh + tc_x_only(p.K, 32);   // slice sums [max_tiles][ks][16]
+  const uint32_t wreg = xsh + p.x_bytes + static_cast<uint32_t>(warp) * p.warp_bytes;
+  const uint32_t bar = smem_addr(&bars[warp]);
+  Tile tl{};
+  if (active) tl = small_tile(p, t0 + lt);
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  // the next kernel may start as SMs free up; it reads what this kernel
+  // writes only after its own griddepcontrol.wait
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (active) {
+    const uint32_t tx = small_issue<F>(p, tl, sb0, nsl, wreg, bar, smem);
+    if (lane == 0) mbar_arrive_tx(bar, tx);
+  }
+  // x may be produced by the previous kernel
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  stage_x_tc_raw<32>(p.x, p.K, p.K, xsh, 0);
+  __syncthreads();
+  const int g = lane >> 2, t = lane & 3;
+  float v[2] = {0.0f, 0.0f};
+  if (active && mbar_wait_warp(bar, 0u)) {
+    const ScaleSel ss = scale_sel(t);
+    const int64_t idx_g = (tl.row0 + g) * static_cast<int64_t>(p.nsb) + sb0;
+    const int64_t idx_g8 = (tl.row0 + g + 8) * static_cast<int64_t>(p.nsb) + sb0;
+    float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+    for (int s = 0; s < nsl; ++s) small_sb_q4<F>(p, wreg, s, sb0 + s, idx_g, idx_g8, xsh, ss, acc);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float a = acc[h].x + acc[h].y;
+      a += __shfl_xor_sync(0xFFFFFFFFu, a, 1);
+      a += __shfl_xor_sync(0xFFFFFFFFu, a, 2);
+      v[h] = a;
+    }
+  }
+  if (active && t == 0) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(red + 4u * ((lt * p.ks + j) * 16 + g + 8 * h)),
+                   "f"(v[h])
+                   : "memory");
+  }
+  __syncthreads();
+  // row i of the CTA's tiles: its slice sums in slice order
+  const int nrows = (t1 - t0) * 16;
+  for (int i = static_cast<int>(threadIdx.x); i < nrows; i += static_cast<int>(blockDim.x)) {
+    const int tt = i >> 4, r = i & 15;
+    const Tile ti = small_tile(p, t0 + tt);
+    if (r >= ti.rcnt) continue;
+    float a = 0.0f;
+    for (int jj = 0; jj < p.ks; ++jj) {
+      float e;
+      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(e) : "r"(red + 4u * ((tt * p.ks + jj) * 16 + r)));
+      a += e;
+    }
+    pick(p.g.y, ti.mi)[ti.row0 + r] = a;
+  }
+}
+
 struct DevInfo {
   int sms = 0;
   size_t smem_optin = 0;      // dynamic + static shared memory one CTA may use
@@ -2482,22 +2788,69 @@ struct DevInfo {
   size_t smem_reserved = 0;   // shared memory the driver reserves per CTA
 };
 
-DevInfo& dev_info() {
-  static DevInfo info[64];
+// Per-device state is kept for device ordinals below kMaxDevices; a launch on
+// a higher ordinal (or when the current device cannot be read) is declined.
+constexpr int kMaxDevices = 64;
+int current_device() {
   int d = 0;
-  cudaGetDevice(&d);
-  DevInfo& i = info[d & 63];
-  if (i.sms == 0) {
-    cudaDeviceGetAttribute(&i.sms, cudaDevAttrMultiProcessorCount, d);
+  if (cudaGetDevice(&d) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return -1;
+  }
+  return d >= 0 && d < kMaxDevices ? d : -1;
+}
+
+// Attributes of the current device, read once per device (thread-safe);
+// nullptr if the device is out of range.
+const DevInfo* dev_info() {
+  static DevInfo info[kMaxDevices];
+  static std::once_flag once[kMaxDevices];
+  const int d = current_device();
+  if (d < 0) return nullptr;
+  std::call_once(once[d], [d] {
+    DevInfo& i = info[d];
     int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d);
+    i.sms = v;
     cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
     i.smem_optin = static_cast<size_t>(v);
     cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d);
     i.smem_sm = static_cast<size_t>(v);
     cudaDeviceGetAttribute(&v, cudaDevAttrReservedSharedMemoryPerBlock, d);
     i.smem_reserved = static_cast<size_t>(v);
+    (void)cudaGetLastError();
+  });
+  return info[d].sms > 0 ? &info[d] : nullptr;
+}
+
+// Dynamic shared memory above 48 KB is opt-in per kernel and per device:
+// raise `kern`'s limit on the current device to at least `smem`.
+// `configured` is that kernel's per-device record of the value set.
+std::mutex& attr_mutex() {
+  static std::mutex m;
+  return m;
+}
+template <typename Kern>
+bool raise_smem_limit(Kern* kern, size_t smem, size_t (&configured)[kMaxDevices]) {
+  const int d = current_device();
+  if (d < 0) return false;
+  std::lock_guard<std::mutex> lock(attr_mutex());
+  if (smem <= configured[d]) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
   }
-  return i;
+  configured[d] = smem;
+  return true;
+}
+
+// A launch that fails leaves no error behind for the caller's status check
+// (the dispatcher then tries the next configuration).
+bool launched(cudaError_t e) {
+  if (e == cudaSuccess) return true;
+  (void)cudaGetLastError();
+  return false;
 }
 
 constexpr size_t kStaticSmem = 256;   // the kernel's static shared memory (barriers, flag), rounded up
@@ -2516,14 +2869,16 @@ struct Scratch {
   void* base = nullptr;
   size_t bytes = 0;
 };
-Scratch& scratch_of_device() {
-  static Scratch sc[64];
-  int d = 0;
-  cudaGetDevice(&d);
-  return sc[d & 63];
+Scratch g_scratch[kMaxDevices];
+std::mutex& scratch_mutex() {
+  static std::mutex m;
+  return m;
 }
 void* scratch_get(size_t bytes, cudaStream_t s) {
-  Scratch& sc = scratch_of_device();
+  const int d = current_device();
+  if (d < 0) return nullptr;
+  std::lock_guard<std::mutex> lock(scratch_mutex());
+  Scratch& sc = g_scratch[d];
   if (sc.bytes >= bytes) return sc.base;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
@@ -2571,7 +2926,9 @@ Plan make_plan(int K, int ksplit, bool tma) {
   const size_t xb = XLayout<F, NT, XBF>::bytes(static_cast<size_t>(NT) * kpad) +
                     static_cast<size_t>(NT) * (kpad / G::kPart) * 4;
   pl.x_bytes = static_cast<uint32_t>((xb + 127) & ~size_t{127});
-  const DevInfo& di = dev_info();
+  const DevInfo* dip = dev_info();
+  if (dip == nullptr) return pl;
+  const DevInfo& di = *dip;
   for (int per_sm = stream_max_per_sm<WC>(); per_sm >= 1; --per_sm) {
     // dynamic shared memory of one CTA when per_sm CTAs share an SM
     size_t budget = di.smem_sm / per_sm;
@@ -2656,7 +3013,9 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
                 int ksplit, bool tma, ScratchSrc src = ScratchSrc::kDevice,
                 StaticScratch* st = nullptr) {
   using G = Geo<F, NT, RT, WC>;
-  const DevInfo& di = dev_info();
+  const DevInfo* dip = dev_info();
+  if (dip == nullptr) return false;
+  const DevInfo& di = *dip;
   Params p;
   p.g = g;
   p.x = x;
@@ -2720,16 +3079,8 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   p.static_tiles = (stages + p.slabs - 1) / p.slabs;
   if (ksplit > kMaxSegs) return false;
   const size_t smem = p.x_bytes + static_cast<size_t>(stages) * ss.bytes;
-  static size_t configured = 0;   // dynamic shared memory above 48 KB is opt-in
-  if (smem > configured) {
-    if (cudaFuncSetAttribute(gemv_stream<F, NT, RT, WC, XBF>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return false;
-    }
-    configured = smem;
-  }
+  static size_t configured[kMaxDevices] = {};   // per device: dynamic smem above 48 KB is opt-in
+  if (!raise_smem_limit(gemv_stream<F, NT, RT, WC, XBF>, smem, configured)) return false;
   p.tx = 0;
   if (tma) {
     for (int i = 0; i < g.count; ++i) {
@@ -2764,8 +3115,10 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
       // the array keeps the previous call's contents: clear the counters
       // this launch uses (a stream-ordered memset, not an allocation)
       if (cudaMemsetAsync(st->base, 0, static_cast<size_t>(p.tiles) * sizeof(unsigned int), s) !=
-          cudaSuccess)
+          cudaSuccess) {
+        (void)cudaGetLastError();
         return false;
+      }
       p.arrivals = reinterpret_cast<unsigned int*>(st->base);
       p.part = reinterpret_cast<float*>(st->base + kNoAllocCounterBytes);
     }
@@ -2780,7 +3133,7 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_stream<F, NT, RT, WC, XBF>, p, stages) == cudaSuccess;
+  return launched(cudaLaunchKernelEx(&cfg, gemv_stream<F, NT, RT, WC, XBF>, p, stages));
 }
 
 template <int F, int NT, int RT, int WC>
@@ -2814,8 +3167,7 @@ bool launch_rt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStre
   for (int ks = best_ks;; ks = 1) {
     const bool ok = best_bf ? launch_cfg<F, NT, RT, WC, true>(g, x, K, n_tok, s, ks, tma, src, st)
                             : launch_cfg<F, NT, RT, WC, false>(g, x, K, n_tok, s, ks, tma, src, st);
-    if (ok || ks == 1) return ok;   // no scratch (e.g. during capture): unsplit
-    if (st != nullptr && st->too_large) return false;
+    if (ok || ks == 1) return ok;   // no scratch (e.g. during capture, or beyond the fixed array): unsplit
     best_bf = static_cast<size_t>(NT) * K * 4 > 96 * 1024;
   }
 }
@@ -2823,7 +3175,9 @@ bool launch_rt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStre
 template <int F, int NT>
 bool launch_nt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
                ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
-  const DevInfo& di = dev_info();
+  const DevInfo* dip = dev_info();
+  if (dip == nullptr) return false;
+  const DevInfo& di = *dip;
   // Small matrices (fewer than 16 rows per SM) and n_tok 4 (whose x values
   // take twice the registers): 4 consumer warps x 2 rows per thread.  Large
   // matrices at n_tok 1, 2: 4 rows per thread, with 8 consumer warps for the
@@ -2850,7 +3204,9 @@ bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
                 ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
   constexpr int NTP = 8 * NB;
   using G = MGeo<F, WC>;
-  const DevInfo& di = dev_info();
+  const DevInfo* dip = dev_info();
+  if (dip == nullptr) return false;
+  const DevInfo& di = *dip;
   const bool tma = tma_possible<G>(K);
   const StageShape full = stage_shape<G>(tma);
   Params p;
@@ -2932,15 +3288,8 @@ bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
     int stages = static_cast<int>((budget - p.x_bytes) / full.bytes);
     if (stages > kMaxStages) stages = kMaxStages;
     const size_t smem = p.x_bytes + static_cast<size_t>(stages) * full.bytes;
-    static size_t configured = 0;
-    if (smem > configured) {
-      if (cudaFuncSetAttribute(gemv_mma<F, NB, WC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem)) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return false;
-      }
-      configured = smem;
-    }
+    static size_t configured[kMaxDevices] = {};   // per device: dynamic smem above 48 KB is opt-in
+    if (!raise_smem_limit(gemv_mma<F, NB, WC>, smem, configured)) return false;
     if (ksplit > 1) {
       const size_t part_bytes =
           static_cast<size_t>(ksplit) * p.tiles * p.tile_rows * NTP * sizeof(float);
@@ -2954,12 +3303,14 @@ bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
       } else {
         if (p.tiles > kNoAllocMaxTiles ||
             kNoAllocCounterBytes + part_bytes > kNoAllocScratchBytes) {
-          st->too_large = true;
-          return false;
+          st->too_large = true;   // beyond the fixed array: fewer segments
+          continue;
         }
         if (cudaMemsetAsync(st->base, 0, static_cast<size_t>(p.tiles) * sizeof(unsigned int), s) !=
-            cudaSuccess)
+            cudaSuccess) {
+          (void)cudaGetLastError();
           return false;
+        }
         p.arrivals = reinterpret_cast<unsigned int*>(st->base);
         p.part = reinterpret_cast<float*>(st->base + kNoAllocCounterBytes);
       }
@@ -2990,7 +3341,7 @@ bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_mma<F, NB, WC>, p, stages) == cudaSuccess;
+    return launched(cudaLaunchKernelEx(&cfg, gemv_mma<F, NB, WC>, p, stages));
   }
 }
 
@@ -3027,7 +3378,9 @@ template <int F, int WC>
 bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
                 ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
   using G = TGeo<F, WC>;
-  const DevInfo& di = dev_info();
+  const DevInfo* dip = dev_info();
+  if (dip == nullptr) return false;
+  const DevInfo& di = *dip;
   const bool tma = tma_possible<G>(K);
   if (!tma) return false;
   const int per_sm = WC <= 8 ? 2 : 1;
@@ -3083,12 +3436,14 @@ bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
     } else {
       if (p.tiles > kNoAllocMaxTiles ||
           kNoAllocCounterBytes + part_bytes > kNoAllocScratchBytes) {
-        st->too_large = true;
-        return false;
+        st->too_large = true;   // beyond the fixed array: unsplit
+        continue;
       }
       if (cudaMemsetAsync(st->base, 0, static_cast<size_t>(p.tiles) * sizeof(unsigned int), s) !=
-          cudaSuccess)
+          cudaSuccess) {
+        (void)cudaGetLastError();
         return false;
+      }
       p.arrivals = reinterpret_cast<unsigned int*>(st->base);
       p.part = reinterpret_cast<float*>(st->base + kNoAllocCounterBytes);
     }
@@ -3101,15 +3456,8 @@ bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
   if (cps < 1) cps = 1;
   p.static_tiles = (stages + p.slabs - 1) / p.slabs;
   const size_t smem = p.x_bytes + static_cast<size_t>(stages) * ss.bytes;
-  static size_t configured = 0;
-  if (smem > configured) {
-    if (cudaFuncSetAttribute(gemv_tc1<F, WC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return false;
-    }
-    configured = smem;
-  }
+  static size_t configured[kMaxDevices] = {};   // per device: dynamic smem above 48 KB is opt-in
+  if (!raise_smem_limit(gemv_tc1<F, WC>, smem, configured)) return false;
   p.tx = 0;
   if (tma) {
     for (int i = 0; i < g.count; ++i) {
@@ -3138,7 +3486,7 @@ bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_tc1<F, WC>, p, stages) == cudaSuccess;
+  return launched(cudaLaunchKernelEx(&cfg, gemv_tc1<F, WC>, p, stages));
 }
 
 // The multi-token tensor-core kernel (n_tok 5..16, NB = 1 or 2 blocks of
@@ -3148,7 +3496,9 @@ bool launch_tcv(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
                 ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
   using G = TGeo<F, WC, kTcvRT>;
   constexpr int NTP = 8 * NB;
-  const DevInfo& di = dev_info();
+  const DevInfo* dip = dev_info();
+  if (dip == nullptr) return false;
+  const DevInfo& di = *dip;
   const bool tma = tma_possible<G>(K);
   if (!tma) return false;
   Params p;
@@ -3206,12 +3556,14 @@ bool launch_tcv(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
     } else {
       if (p.tiles > kNoAllocMaxTiles ||
           kNoAllocCounterBytes + part_bytes > kNoAllocScratchBytes) {
-        st->too_large = true;
-        return false;
+        st->too_large = true;   // beyond the fixed array: unsplit
+        continue;
       }
       if (cudaMemsetAsync(st->base, 0, static_cast<size_t>(p.tiles) * sizeof(unsigned int), s) !=
-          cudaSuccess)
+          cudaSuccess) {
+        (void)cudaGetLastError();
         return false;
+      }
       p.arrivals = reinterpret_cast<unsigned int*>(st->base);
       p.part = reinterpret_cast<float*>(st->base + kNoAllocCounterBytes);
     }
@@ -3224,15 +3576,8 @@ bool launch_tcv(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   if (cps < 1) cps = 1;
   p.static_tiles = (stages + p.slabs - 1) / p.slabs;
   const size_t smem = p.x_bytes + static_cast<size_t>(stages) * ss.bytes;
-  static size_t configured = 0;
-  if (smem > configured) {
-    if (cudaFuncSetAttribute(gemv_tcv<F, WC, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return false;
-    }
-    configured = smem;
-  }
+  static size_t configured[kMaxDevices] = {};   // per device: dynamic smem above 48 KB is opt-in
+  if (!raise_smem_limit(gemv_tcv<F, WC, NB>, smem, configured)) return false;
   for (int i = 0; i < g.count; ++i) {
     const int64_t n = g.N[i];
     bool ok;
@@ -3258,13 +3603,75 @@ bool launch_tcv(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_tcv<F, WC, NB>, p, stages) == cudaSuccess;
+  return launched(cudaLaunchKernelEx(&cfg, gemv_tcv<F, WC, NB>, p, stages));
 }
 
-// Verify-width (n_tok 5..16) launches that take the multi-token tensor-core
+// The small-launch kernel: one wave, each CTA owning whole 16-row tiles
+// (at most kSmallMaxTiles), each warp one (tile, K slice); the slices are
+// as fine as kSmallMaxWarps warps per CTA allow.  Declines launches whose tiles do not
+// fit one CTA per SM in shared memory.
+constexpr int kSmallMaxTiles = 4;
+
+template <int F>
+bool launch_small(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s) {
+  const DevInfo* dip = dev_info();
+  if (dip == nullptr) return false;
+  const DevInfo& di = *dip;
+  SmallParams p;
+  p.g = g;
+  p.x = x;
+  p.K = K;
+  p.nsb = K / 256;
+  p.tiles = 0;
+  for (int i = 0; i < kMaxGroup; ++i) {
+    if (i < g.count) p.tiles += (g.N[i] + 15) / 16;
+    p.tile_end[i] = p.tiles;
+  }
+  const int C = p.tiles < di.sms ? p.tiles : di.sms;
+  if (C < 1) return false;
+  p.max_tiles = (p.tiles + C - 1) / C;
+  if (p.max_tiles > kSmallMaxTiles) return false;
+  int ks = kSmallMaxWarps / p.max_tiles;
+  if (ks > p.nsb) ks = p.nsb;
+  p.sbs = (p.nsb + ks - 1) / ks;
+  p.ks = (p.nsb + p.sbs - 1) / p.sbs;   // every slice has at least one super-block
+  auto odd16 = [](uint32_t b) { b = (b + 15u) / 16u * 16u; return (b / 16u) % 2u ? b : b + 16u; };
+  p.pitch = odd16(static_cast<uint32_t>(p.sbs) * (F == kG128 ? 128u : block_bytes(F)));
+  p.ppitch = F == kG128 ? (static_cast<uint32_t>(p.sbs) * 8u + 16u + 15u) / 16u * 16u : 0u;
+  p.warp_bytes = (16u * (p.pitch + p.ppitch) + 127u) & ~127u;
+  p.x_bytes = (tc_x_only(K, 32) + 4u * static_cast<uint32_t>(p.max_tiles * p.ks * 16) + 127u) & ~127u;
+  const int warps = p.max_tiles * p.ks;
+  const size_t smem = p.x_bytes + static_cast<size_t>(warps) * p.warp_bytes;
+  if (smem + kStaticSmem > di.smem_optin) return false;
+  static size_t configured[kMaxDevices] = {};
+  if (!raise_smem_limit(gemv_small<F>, smem, configured)) return false;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(C));
+  cfg.blockDim = dim3(static_cast<unsigned>(warps * 32));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return launched(cudaLaunchKernelEx(&cfg, gemv_small<F>, p));
+}
+
+// Single-token launches that take the small-launch kernel: Q4_K and Q4_G128
+// launches of fewer than 32 M weights (the single-token tensor-core kernel
+// takes the larger ones), as long as they fit one wave (launch_small).
+bool small_eligible(int fmt, const GemvGroup& g, int K, int n_tok) {
+  if (n_tok != 1 || (fmt != kQ4K && fmt != kG128)) return false;
+  int64_t rows = 0;
+  for (int i = 0; i < g.count; ++i) rows += g.N[i];
+  return rows * K < (int64_t{1} << 25);
+}
+
+// Multi-token (n_tok 2..16) launches that take the multi-token tensor-core
 // kernel: Q4_K and Q4_G128 matrices of at least 32 M weights.
 bool tcv_eligible(int fmt, const GemvGroup& g, int K, int n_tok) {
-  if (n_tok < 5 || n_tok > 16 || (fmt != kQ4K && fmt != kG128)) return false;
+  if (n_tok < 2 || n_tok > 16 || (fmt != kQ4K && fmt != kG128)) return false;
   int64_t rows = 0;
   for (int i = 0; i < g.count; ++i) rows += g.N[i];
   return rows * K >= (int64_t{1} << 25);
@@ -3300,43 +3707,6 @@ bool launch_tc1_fmt(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s
 
 }  // namespace
 
-bool launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
-                   cudaStream_t s) {
-  if (n_tok > 16) return false;
-  if (tcv_eligible(fmt, g, K, n_tok)) {
-    const bool ok = fmt == kQ4K ? launch_tcv_fmt<kQ4K>(g, x, K, n_tok, s)
-                                : launch_tcv_fmt<kG128>(g, x, K, n_tok, s);
-    if (ok) return true;
-  }
-  if (n_tok > 4) {
-    switch (fmt) {
-      case kQ4K: return launch_verify<kQ4K>(g, x, K, n_tok, s);
-      case kQ5K: return launch_verify<kQ5K>(g, x, K, n_tok, s);
-      case kQ6K: return launch_verify<kQ6K>(g, x, K, n_tok, s);
-      case kG128: return launch_verify<kG128>(g, x, K, n_tok, s);
-    }
-    return false;
-  }
-  if (tc1_eligible(fmt, g, K, n_tok)) {
-    const bool ok = fmt == kQ4K ? launch_tc1_fmt<kQ4K>(g, x, K, s) : launch_tc1_fmt<kG128>(g, x, K, s);
-    if (ok) return true;
-  }
-  const int nt = n_tok <= 1 ? 1 : (n_tok <= 2 ? 2 : 4);
-#define KQ_CASE(F)                                                  \
-  case F:                                                           \
-    if (nt == 1) return launch_nt<F, 1>(g, x, K, n_tok, s);         \
-    if (nt == 2) return launch_nt<F, 2>(g, x, K, n_tok, s);         \
-    return launch_nt<F, 4>(g, x, K, n_tok, s);
-  switch (fmt) {
-    KQ_CASE(kQ4K)
-    KQ_CASE(kQ5K)
-    KQ_CASE(kQ6K)
-    KQ_CASE(kG128)
-  }
-#undef KQ_CASE
-  return false;
-}
-
 // ------------------------------------------------------- no-allocation path
 //
 // Scratch of kq_gemv_noalloc: a fixed 2 MiB array in every device that loads
@@ -3348,74 +3718,129 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 namespace {
 // Device address of g_noalloc_scratch on the current device.  In host code
 // the array's name is only a host-side stand-in, never a device address: the
-// address is looked up once per device (with that device current) and
-// cached.  nullptr if the lookup fails.
+// address is looked up once per device (with that device current; thread-safe)
+// and cached.  nullptr if the lookup fails or the device ordinal is out of
+// range.
 void* noalloc_scratch_address() {
-  static void* addr[64] = {};
-  static bool looked_up[64] = {};
-  int d = 0;
-  if (cudaGetDevice(&d) != cudaSuccess) return nullptr;
-  d &= 63;
-  if (!looked_up[d]) {
+  static void* addr[kMaxDevices] = {};
+  static std::once_flag once[kMaxDevices];
+  const int d = current_device();
+  if (d < 0) return nullptr;
+  std::call_once(once[d], [d] {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) {
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) == cudaSuccess)
+      addr[d] = ptr;
+    else
       (void)cudaGetLastError();
-      return nullptr;
-    }
-    addr[d] = ptr;
-    looked_up[d] = true;
-  }
+  });
   return addr[d];
+}
+
+// The tensor cores serve every width from two tokens on: the cost of those
+// kernels is set by building the A operand from the packed weights, once per
+// weight whatever the token count, while the CUDA-core kernel spends a
+// multiply-add per weight and token.
+constexpr int kTensorCoreMinTokens = 2;
+}  // namespace
+
+// The kernel choice for one request (see kq_kernels.cuh).  `noalloc`: split-K
+// partial sums go to g_noalloc_scratch, and a configuration whose sums do not
+// fit there gives way to one with fewer K segments or to the next kernel.
+StreamResult launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
+                           cudaStream_t s, bool noalloc) {
+  if (n_tok < 1 || n_tok > 16 || fmt < kQ4K || fmt > kG128) return StreamResult::kNotServed;
+  StaticScratch sst{nullptr, false};
+  StaticScratch* st = nullptr;
+  ScratchSrc src = ScratchSrc::kDevice;
+  if (noalloc) {
+    sst.base = static_cast<uint8_t*>(noalloc_scratch_address());
+    if (sst.base == nullptr) return StreamResult::kFailed;
+    st = &sst;
+    src = ScratchSrc::kStatic;
+  }
+  auto done = [&](bool ok) {
+    return ok ? StreamResult::kLaunched
+              : (sst.too_large ? StreamResult::kTooLarge : StreamResult::kNotServed);
+  };
+  if (n_tok >= kTensorCoreMinTokens) {
+    // verify widths: the multi-token tensor-core kernels
+    if (tcv_eligible(fmt, g, K, n_tok)) {
+      const bool ok = fmt == kQ4K ? launch_tcv_fmt<kQ4K>(g, x, K, n_tok, s, src, st)
+                                  : launch_tcv_fmt<kG128>(g, x, K, n_tok, s, src, st);
+      if (ok) return StreamResult::kLaunched;
+    }
+    bool ok = false;
+    switch (fmt) {
+      case kQ4K: ok = launch_verify<kQ4K>(g, x, K, n_tok, s, src, st); break;
+      case kQ5K: ok = launch_verify<kQ5K>(g, x, K, n_tok, s, src, st); break;
+      case kQ6K: ok = launch_verify<kQ6K>(g, x, K, n_tok, s, src, st); break;
+      default: ok = launch_verify<kG128>(g, x, K, n_tok, s, src, st); break;
+    }
+    if (ok) return StreamResult::kLaunched;
+  } else if (small_eligible(fmt, g, K, n_tok)) {
+    // needs no scratch
+    const bool ok = fmt == kQ4K ? launch_small<kQ4K>(g, x, K, s) : launch_small<kG128>(g, x, K, s);
+    if (ok) return StreamResult::kLaunched;
+  } else if (tc1_eligible(fmt, g, K, n_tok)) {
+    const bool ok = fmt == kQ4K ? launch_tc1_fmt<kQ4K>(g, x, K, s, src, st)
+                                : launch_tc1_fmt<kG128>(g, x, K, s, src, st);
+    if (ok) return StreamResult::kLaunched;
+  }
+  // the CUDA-core streaming kernel: up to four tokens per launch; wider
+  // requests run as consecutive launches of up to four tokens (x and y rows
+  // of a token are contiguous, so a chunk is an offset view).  Every chunk
+  // has the shape of the first or fewer tokens, so if the first is served
+  // the rest are too.
+  auto stream_nt = [&](const GemvGroup& gc, const uint16_t* xc, int nt) {
+    const int w = nt <= 1 ? 1 : (nt <= 2 ? 2 : 4);
+#define KQ_CASE(F)                                                          \
+  case F:                                                                   \
+    return w == 1 ? launch_nt<F, 1>(gc, xc, K, nt, s, src, st)              \
+                  : w == 2 ? launch_nt<F, 2>(gc, xc, K, nt, s, src, st)     \
+                           : launch_nt<F, 4>(gc, xc, K, nt, s, src, st);
+    switch (fmt) {
+      KQ_CASE(kQ4K)
+      KQ_CASE(kQ5K)
+      KQ_CASE(kQ6K)
+      KQ_CASE(kG128)
+    }
+#undef KQ_CASE
+    return false;
+  };
+  for (int t0 = 0; t0 < n_tok; t0 += 4) {
+    const int nt = n_tok - t0 < 4 ? n_tok - t0 : 4;
+    GemvGroup gc = g;
+    for (int i = 0; i < g.count; ++i) gc.y[i] = g.y[i] + static_cast<int64_t>(t0) * g.N[i];
+    if (!stream_nt(gc, x + static_cast<int64_t>(t0) * K, nt)) {
+      // nothing launched for this chunk: the caller's fallback recomputes
+      // (and overwrites) every token
+      return done(false);
+    }
+  }
+  return StreamResult::kLaunched;
+}
+
+namespace {
+// One warp waits on a shared-memory barrier that nothing ever completes,
+// with the bounded wait shortened to `limit` cycles: the wait runs out, is
+// counted in g_wait_timeouts like any other, and the kernel returns.  It
+// exercises the failure path of the bounded waits without a GPU fault.
+__global__ void __launch_bounds__(32) wait_timeout_probe(long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  (void)mbar_wait_warp(b, 0u, limit);
 }
 }  // namespace
 
-NoAllocResult launch_stream_noalloc(int fmt, const GemvGroup& g, const uint16_t* x, int K,
-                                    int n_tok, cudaStream_t s) {
-  if (n_tok > 16) return NoAllocResult::kNotServed;
-  StaticScratch st{static_cast<uint8_t*>(noalloc_scratch_address()), false};
-  if (st.base == nullptr) return NoAllocResult::kFailed;
-  bool ok = false;
-  if (tcv_eligible(fmt, g, K, n_tok)) {
-    ok = fmt == kQ4K ? launch_tcv_fmt<kQ4K>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st)
-                     : launch_tcv_fmt<kG128>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st);
-    if (st.too_large) return NoAllocResult::kTooLarge;
-    if (ok) return NoAllocResult::kLaunched;
-  }
-  if (n_tok > 4) {
-    switch (fmt) {
-      case kQ4K: ok = launch_verify<kQ4K>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st); break;
-      case kQ5K: ok = launch_verify<kQ5K>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st); break;
-      case kQ6K: ok = launch_verify<kQ6K>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st); break;
-      case kG128: ok = launch_verify<kG128>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st); break;
-      default: return NoAllocResult::kFailed;
-    }
-    if (st.too_large) return NoAllocResult::kTooLarge;
-    return ok ? NoAllocResult::kLaunched : NoAllocResult::kNotServed;
-  }
-  if (tc1_eligible(fmt, g, K, n_tok)) {
-    ok = fmt == kQ4K ? launch_tc1_fmt<kQ4K>(g, x, K, s, ScratchSrc::kStatic, &st)
-                     : launch_tc1_fmt<kG128>(g, x, K, s, ScratchSrc::kStatic, &st);
-    if (st.too_large) return NoAllocResult::kTooLarge;
-    if (ok) return NoAllocResult::kLaunched;
-  }
-  const int nt = n_tok <= 1 ? 1 : (n_tok <= 2 ? 2 : 4);
-#define KQ_CASE(F)                                                                          \
-  case F:                                                                                   \
-    ok = nt == 1   ? launch_nt<F, 1>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st)           \
-         : nt == 2 ? launch_nt<F, 2>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st)           \
-                   : launch_nt<F, 4>(g, x, K, n_tok, s, ScratchSrc::kStatic, &st);          \
-    break;
-  switch (fmt) {
-    KQ_CASE(kQ4K)
-    KQ_CASE(kQ5K)
-    KQ_CASE(kQ6K)
-    KQ_CASE(kG128)
-    default:
-      return NoAllocResult::kFailed;
-  }
-#undef KQ_CASE
-  if (st.too_large) return NoAllocResult::kTooLarge;
-  return ok ? NoAllocResult::kLaunched : NoAllocResult::kNotServed;
+bool launch_wait_timeout_probe(unsigned int wait_us, cudaStream_t s) {
+  const long long limit = static_cast<long long>(wait_us) * 2000;   // ~2 GHz SM clock
+  wait_timeout_probe<<<1, 32, 0, s>>>(limit);
+  return launched(cudaGetLastError());
 }
 
 bool read_wait_timeouts(unsigned int* count, cudaStream_t s) {
@@ -3430,8 +3855,13 @@ bool read_wait_timeouts(unsigned int* count, cudaStream_t s) {
     if (cudaMemcpyToSymbolAsync(g_wait_timeouts, &zero, sizeof(unsigned int), 0,
                                 cudaMemcpyHostToDevice, s) != cudaSuccess)
       return false;
-    Scratch& sc = scratch_of_device();
-    if (sc.base != nullptr && cudaMemsetAsync(sc.base, 0, sc.bytes, s) != cudaSuccess) return false;
+    const int d = current_device();
+    if (d >= 0) {
+      std::lock_guard<std::mutex> lock(scratch_mutex());
+      const Scratch& sc = g_scratch[d];
+      if (sc.base != nullptr && cudaMemsetAsync(sc.base, 0, sc.bytes, s) != cudaSuccess) return false;
+    }
+    // the fixed array of kq_gemv_noalloc clears its counters on every call
     static const unsigned int zeros[2 * kMaxSegs] = {};
     if (cudaMemcpyToSymbolAsync(g_sched, zeros, sizeof(zeros), 0, cudaMemcpyHostToDevice, s) !=
         cudaSuccess)

@@ -41,6 +41,21 @@ def test_header_declares_the_boundary():
         assert required in names
 
 
+def test_every_declaration_states_its_source():
+    # the comment right above each function declaration carries a "Source:"
+    # line: the page passage that defines it, or that the pages define none
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(kq_\w+)\s*\(", text, flags=re.M):
+            before = text[:m.start()]
+            c0, c1 = before.rfind("/*"), before.rfind("*/")
+            assert c0 >= 0 and c1 > c0, m.group(1)
+            assert not before[c1 + 2:].strip(), f"{m.group(1)}: no comment right above"
+            assert "Source:" in before[c0:c1], f"{m.group(1)}: comment has no Source: line"
+
+
 def test_library_exports_every_declared_symbol(kq):
     L = ctypes.CDLL(kq.LIB_PATH)
     for name in _declared_functions():

@@ -2,8 +2,9 @@
 token and at the verify widths.  At n_tok = 1, Q4_K and Q4_G128 run on the
 tensor cores with the sub-blocks of the one token as the columns of the mma's
 n8 operand (gemv_tc1); Q5_K and Q6_K on the streaming CUDA-core kernel.  At
-n_tok 5..16, Q4_K and Q4_G128 run on the one-CTA-per-SM tensor-core kernel
-with tokens as columns (gemv_tcv); Q5_K and Q6_K on gemv_mma.
+n_tok 2..16, Q4_K and Q4_G128 run on the one-CTA-per-SM tensor-core kernel
+with tokens as columns (gemv_tcv); Q5_K and Q6_K on gemv_mma.  n_tok 3 on the
+1100 x 32768 shape is a full-size split-K launch at an odd width.
 
 Every row is checked against the fp64 oracle (|y - y_ref| <= 1e-3 sum|w^ x| +
 1e-5).  The shapes cover: ragged last tiles; an odd super-block count; Q6_K
@@ -151,7 +152,7 @@ def test_verify_widths_large_match_oracle(kq, oracle, fmt, case):
     Wb = oracle.quantize(fmt, _weights_f32(N, K), N, K)
     x = wl.activations_bf16(wl.derive_seed(707, fmt, N), 16, K, heavy=True)
     yref, A = oracle.gemv(fmt, Wb, N, K, x)
-    for T in (5, 8, 11, 16):
+    for T in (2, 3, 4, 5, 8, 11, 16):
         _assert_parity(_gemv_t(kq, fmt, Wb, x[:T], N, K), yref[:T], A[:T], f"fmt={fmt} {N}x{K} n_tok={T}")
 
 
