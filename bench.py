@@ -218,7 +218,7 @@ def build_pools_library(device):
     import quant_weight_gemv_dequant_b300 as kq
     pw = wl.pool_weights(wl.derive_seed(900), wl.POOL_BLOCKS)
     return {f: torch.from_numpy(kq.kq_quantize(f, pw, wl.POOL_BLOCKS, 256)).to(device)
-            for f in (wl.Q4_K, wl.Q6_K)}
+            for f in (wl.Q4_K, wl.Q5_K, wl.Q6_K)}
 
 
 def build_step(pools_dev, n_tok, layers, device):
@@ -303,6 +303,183 @@ def dominant_kernel_timing(step, steps, warmup, stream):
     nbytes = (L0["gate"][1].numel() + L0["up"][1].numel() + step.x[0]["x_ffn"].numel() * 2
               + (L0["gate"][2] + L0["up"][2]) * 4 * step.n_tok)
     return dur, nbytes, "gemv_q4k_gate_up"
+
+
+# ------------------------------------------- per-config and per-launch lines
+
+L2_BYTES = 126e6   # B300 L2
+
+
+def graph_time(launch, n_launch, stream, reps=5):
+    """Seconds per launch of launch(i) for i < n_launch, captured in one CUDA
+    graph and replayed `reps` times; CUDA events on the launching stream."""
+    import torch
+    for i in range(min(n_launch, 8)):      # shapes seen once outside capture
+        launch(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n_launch):
+            launch(i)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / (reps * n_launch)
+
+
+def copies_for(nbytes: int) -> int:
+    """Weight copies to rotate through so that one round streams >= 4x L2."""
+    return max(1, int(np.ceil(4 * L2_BYTES / nbytes)))
+
+
+def time_group(groups, T, K, stream, heavy=False, seed=0):
+    """Per-launch seconds of one grouped launch (fmt, [W], [N]) rotated over
+    the copies in `groups` (a list of (fmt, [W], [N]) with the same shapes)."""
+    import torch
+    import quant_weight_gemv_dequant_b300 as kq
+    dev = groups[0][1][0].device
+    x = torch.from_numpy(wl.activations_bf16(wl.derive_seed(60, seed, T), T, K, heavy=heavy)
+                         .view(np.int16)).to(dev).view(torch.bfloat16)
+    ys = [torch.empty((T, n), dtype=torch.float32, device=dev) for n in groups[0][2]]
+    R = len(groups)
+
+    def launch(i):
+        f, Ws, Ns = groups[i % R]
+        kq.kq_gemv_multi(f, Ws, ys, Ns, x, K, T, stream)
+
+    return graph_time(launch, max(2 * R, 24), stream)
+
+
+def rate_line(nbytes, seconds, hbm):
+    return {"us": seconds * 1e6, "weight_gb_s": nbytes / seconds / 1e9,
+            "frac_of_hbm_peak": nbytes / seconds / 1e9 / hbm}
+
+
+def measure_configs(pools, device, stream, hbm):
+    """The other workloads, each timed as graph replays of its launches over
+    rotated weight copies (>= 4x L2 per round): C1 single Q4_K 4096x4096 at
+    1 and 8 tokens; C2 attention projections (q/k/v grouped, o) plus q in the
+    merged group-128 layout; C3 the SwiGLU FFN with heavy-tailed x; C4 one
+    Q5_K layer (seven projections, four launches) at n_tok 1, 2, 4, 8, 16."""
+    import torch
+    import quant_weight_gemv_dequant_b300 as kq
+    out = {}
+
+    def host_quant(fmt, m, seed):
+        w = wl.weights_f32(wl.derive_seed(61, seed), m.N, m.K)
+        return torch.from_numpy(kq.kq_quantize(fmt, w, m.N, m.K)).to(device)
+
+    # C1
+    m = wl.SINGLE_Q4K[0]
+    W = host_quant(m.fmt, m, 1)
+    R = copies_for(m.nbytes)
+    groups = [(m.fmt, [W.clone()], [m.N]) for _ in range(R)]
+    c1 = {"workload": "single_q4k_4096x4096", "weight_bytes": m.nbytes, "copies": R}
+    for T in (1, 8):
+        c1[f"n_tok_{T}"] = rate_line(m.nbytes, time_group(groups, T, m.K, stream, seed=1), hbm)
+    out["C1"] = c1
+    del groups, W
+
+    # C2
+    q, k, v, o, qg = wl.ATTN_Q4K
+    Wq, Wk, Wv, Wo = (host_quant(mm.fmt, mm, 20 + i) for i, mm in enumerate((q, k, v, o)))
+    Wqg = torch.from_numpy(kq.kq_quantize(wl.Q4_G128, wl.weights_f32(wl.derive_seed(61, 20), q.N, q.K),
+                                          q.N, q.K)).to(device)
+    qkv_bytes = q.nbytes + k.nbytes + v.nbytes
+    c2 = {"workload": "attention_q4k_h5120_q4096_kv256_plus_q_g128",
+          "weight_bytes": qkv_bytes + o.nbytes, "q_g128_bytes": qg.nbytes}
+    R = copies_for(qkv_bytes)
+    t_qkv = time_group([(q.fmt, [Wq.clone(), Wk.clone(), Wv.clone()], [q.N, k.N, v.N]) for _ in range(R)],
+                       1, q.K, stream, seed=2)
+    R = copies_for(o.nbytes)
+    t_o = time_group([(o.fmt, [Wo.clone()], [o.N]) for _ in range(R)], 1, o.K, stream, seed=3)
+    R = copies_for(qg.nbytes)
+    t_qg = time_group([(qg.fmt, [Wqg.clone()], [qg.N]) for _ in range(R)], 1, qg.K, stream, seed=2)
+    c2["n_tok_1"] = {"qkv": rate_line(qkv_bytes, t_qkv, hbm), "o": rate_line(o.nbytes, t_o, hbm),
+                     "q_g128": rate_line(qg.nbytes, t_qg, hbm),
+                     "attention_total": rate_line(qkv_bytes + o.nbytes, t_qkv + t_o, hbm)}
+    out["C2"] = c2
+    del Wq, Wk, Wv, Wo, Wqg
+
+    # C3
+    gate, up, down = wl.FFN_Q4K_Q6K
+    gu_bytes = gate.nbytes + up.nbytes
+    R = copies_for(gu_bytes)
+    gu = [(gate.fmt, [wl.tile_matrix_device(pools[gate.fmt], gate.fmt, wl.derive_seed(62, r, 0), gate.N, gate.K),
+                      wl.tile_matrix_device(pools[up.fmt], up.fmt, wl.derive_seed(62, r, 1), up.N, up.K)],
+           [gate.N, up.N]) for r in range(R)]
+    t_gu = time_group(gu, 1, gate.K, stream, heavy=True, seed=4)
+    del gu
+    R = copies_for(down.nbytes)
+    dn = [(down.fmt, [wl.tile_matrix_device(pools[down.fmt], down.fmt, wl.derive_seed(62, r, 2), down.N, down.K)],
+           [down.N]) for r in range(R)]
+    t_dn = time_group(dn, 1, down.K, stream, heavy=True, seed=5)
+    del dn
+    out["C3"] = {"workload": "ffn_q4k_gate_up_2x32768x5120_q6k_down_5120x32768_heavy_tailed_x",
+                 "weight_bytes": gu_bytes + down.nbytes,
+                 "n_tok_1": {"gate_up": rate_line(gu_bytes, t_gu, hbm), "down": rate_line(down.nbytes, t_dn, hbm),
+                             "ffn_total": rate_line(gu_bytes + down.nbytes, t_gu + t_dn, hbm)}}
+
+    # C4
+    lay = wl.LAYER_Q5K
+    lay_bytes = sum(mm.nbytes for mm in lay)
+    R = copies_for(lay_bytes)
+    mats = [{mm.name: wl.tile_matrix_device(pools[wl.Q5_K], wl.Q5_K, wl.derive_seed(63, r, i), mm.N, mm.K)
+             for i, mm in enumerate(lay)} for r in range(R)]
+    by = {mm.name: mm for mm in lay}
+    launches = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
+    c4 = {"workload": "q5k_layer_h5120_i32768_seven_projections", "weight_bytes": lay_bytes, "copies": R}
+    for T in (1, 2, 4, 8, 16):
+        xs = {K: torch.from_numpy(wl.activations_bf16(wl.derive_seed(64, T, K), T, K).view(np.int16))
+              .to(device).view(torch.bfloat16) for K in {mm.K for mm in lay}}
+        ys = {mm.name: torch.empty((T, mm.N), dtype=torch.float32, device=device) for mm in lay}
+
+        def step(i, T=T, xs=xs, ys=ys):
+            Ws = mats[i % R]
+            for grp in launches:
+                K = by[grp[0]].K
+                kq.kq_gemv_multi(wl.Q5_K, [Ws[n] for n in grp], [ys[n] for n in grp],
+                                 [by[n].N for n in grp], xs[K], K, T, stream)
+
+        t = graph_time(step, max(2 * R, 8), stream)
+        c4[f"n_tok_{T}"] = {**rate_line(lay_bytes, t, hbm), "us_per_token": t * 1e6 / T}
+    out["C4"] = c4
+    del mats
+    torch.cuda.empty_cache()
+    return out
+
+
+def step_launch_table(pools, device, stream, hbm, n_toks=(1, 8)):
+    """Per-launch time of each launch type of the decode step (layer-0
+    shapes, rotated copies >= 4x L2) at the given widths, with its share of
+    a step (52 layers + head); the largest share per width is the dominant
+    kernel of that width."""
+    table = {}
+    for T in n_toks:
+        row = {}
+        for case, names in CASES.items():
+            mats = [wl.LM_HEAD] if names == ("lm_head",) else [m for m in wl.DECODE_LAYER if m.name in names]
+            nbytes = sum(m.nbytes for m in mats)
+            R = copies_for(nbytes)
+            groups = [(mats[0].fmt, [wl.tile_matrix_device(pools[m.fmt], m.fmt, wl.derive_seed(65, r, i), m.N, m.K)
+                                     for i, m in enumerate(mats)], [m.N for m in mats]) for r in range(R)]
+            t = time_group(groups, T, mats[0].K, stream, seed=6)
+            del groups
+            per_step = 1 if case == "lm_head" else wl.LAYERS
+            row[case] = {**rate_line(nbytes, t, hbm), "bytes_per_launch": nbytes, "launches_per_step": per_step,
+                         "us_per_step": t * 1e6 * per_step}
+        tot = sum(r["us_per_step"] for r in row.values())
+        for r in row.values():
+            r["share"] = r["us_per_step"] / tot
+        table[f"n_tok_{T}"] = row
+    return table
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -437,6 +614,18 @@ def run_kq(args):
     dur, kbytes, kname = dominant_kernel_timing(step, args.steps, 3, stream)
     achieved = kbytes / dur / 1e9
 
+    # the other workloads, and every launch type of the step at 1 and 8 tokens
+    configs, table, roofline_n8 = None, None, None
+    if not args.no_extra and rank == 0:
+        configs = measure_configs(pools, device, stream, hbm)
+        table = step_launch_table(pools, device, stream, hbm)
+        dom = max(table["n_tok_8"].items(), key=lambda kv: kv[1]["share"])
+        roofline_n8 = {"bound": "hbm", "kernel": f"{dom[0]} at n_tok 8", "achieved": dom[1]["weight_gb_s"],
+                       "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
+                       "frac": dom[1]["weight_gb_s"] / hbm, "traffic": None,
+                       "bytes_per_launch": dom[1]["bytes_per_launch"], "launch_us": dom[1]["us"],
+                       "share_of_step": dom[1]["share"]}
+
     # end to end through the public API with host buffers: per step, H2D of
     # every activation input from pinned memory, the graph, D2H of the logits
     e2e = None
@@ -489,6 +678,7 @@ def run_kq(args):
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
                          "traffic": profiled_traffic(kname), "bytes_per_launch": kbytes,
                          "launch_us": dur * 1e6},
+            "roofline_n8": roofline_n8, "configs": configs, "launch_table": table,
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": step.launches() * args.steps,
             "clocks": clocks, **extra,

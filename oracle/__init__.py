@@ -70,6 +70,13 @@ def _load():
         lib.kqo_quantize.argtypes = [I, P, I64, I64, P]
         lib.kqo_quantize_q4k_group128.argtypes = [P, I64, I64, P]
         lib.kqo_merge_g128.argtypes = [P, I64, I64, P]
+        lib.kqo_silu.argtypes = [ctypes.c_double]
+        lib.kqo_silu.restype = ctypes.c_double
+        lib.kqo_bf16_from_double.argtypes = [ctypes.c_double]
+        lib.kqo_bf16_from_double.restype = ctypes.c_uint16
+        lib.kqo_swiglu.argtypes = [P, P, I64, P, P]
+        lib.kqo_swiglu.restype = None
+        lib.kqo_gemv_absw.argtypes = [I, P, I64, I64, P, P]
         _lib = lib
     return _lib
 
@@ -157,6 +164,36 @@ def merge_g128(q4k: np.ndarray, N: int, K: int):
     out = np.zeros(matrix_bytes(Q4_G128, N, K), dtype=np.uint8)
     st = _load().kqo_merge_g128(_ptr(q4k), N, K, _ptr(out))
     return st, out
+
+
+def silu(v: float) -> float:
+    """silu(v) = v / (1 + e^-v) in fp64."""
+    return _load().kqo_silu(float(v))
+
+
+def bf16_from_double(v: float) -> int:
+    """bf16 bits of v rounded to nearest, ties to even (from the double)."""
+    return _load().kqo_bf16_from_double(float(v))
+
+
+def swiglu(g: np.ndarray, u: np.ndarray):
+    """(h_exact fp64, h_bf16 uint16 bits) with h = silu(g) * u elementwise."""
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    assert g.shape == u.shape
+    h = np.empty(g.shape, dtype=np.float64)
+    hb = np.empty(g.shape, dtype=np.uint16)
+    _load().kqo_swiglu(_ptr(g), _ptr(u), g.size, _ptr(h), _ptr(hb))
+    return h, hb
+
+
+def gemv_absw(fmt: int, W: np.ndarray, N: int, K: int, e: np.ndarray) -> np.ndarray:
+    """sum_k |w^[n][k]| e[k] for every row n (fp64 [N]); e >= 0, length K."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    e = np.ascontiguousarray(e, dtype=np.float64).reshape(K)
+    out = np.empty(N, dtype=np.float64)
+    _check(_load().kqo_gemv_absw(fmt, _ptr(W), N, K, _ptr(e), _ptr(out)), "gemv_absw")
+    return out
 
 
 def tolerance(A: np.ndarray) -> np.ndarray:

@@ -556,3 +556,75 @@ int kqo_merge_g128(const uint8_t* q4k, int64_t N, int64_t K, uint8_t* out) {
   }
   return KQO_OK;
 }
+
+/* ------------------------- SwiGLU activation ---------------------------- */
+/*
+ * The decoder's feed-forward block is SwiGLU (the Core AI card for
+ * Muse-Glimmer-30B, section "The architecture, and what the port had to do
+ * about it"): the input of the down projection is silu(gate) * up, element
+ * by element, with gate and up the outputs of the two projections that read
+ * the same hidden state.  The pages name the block but do not write the
+ * function out; the reading taken is the standard one, silu(v) = v * s(v)
+ * with s the logistic function s(v) = 1 / (1 + e^-v).  The result feeds the
+ * next GEMV as bf16 (the activation type of the whole path), rounded to
+ * nearest, ties to even.
+ */
+
+/* silu(v) = v / (1 + e^-v), plain fp64.  For v -> -inf, e^-v -> +inf and
+ * the quotient -> -0. */
+double kqo_silu(double v) { return v / (1.0 + exp(-v)); }
+
+/* double -> bf16 bits, round to nearest, ties to even, directly from the
+ * double (no intermediate rounding).  bf16 = 1 sign, 8 exponent (bias 127),
+ * 7 fraction bits; the quantum of a value in [2^e, 2^(e+1)) is 2^(e-7),
+ * and never below 2^-133 (the subnormal quantum).  Magnitudes that round
+ * to 2^128 or more become infinity. */
+uint16_t kqo_bf16_from_double(double v) {
+  if (v != v) return 0x7FC0;                      /* NaN */
+  uint16_t sign = signbit(v) ? 0x8000 : 0;
+  double a = fabs(v);
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e);                                   /* a = m 2^e, m in [0.5, 1) */
+  int qexp = (e - 1) - 7;                         /* quantum exponent */
+  if (qexp < -133) qexp = -133;
+  double r = nearbyint(ldexp(a, -qexp));          /* default mode: to nearest, ties to even */
+  r = ldexp(r, qexp);
+  if (r >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80);
+  float f = (float)r;                             /* exact: 8 significant bits */
+  uint32_t bits;
+  memcpy(&bits, &f, 4);
+  return (uint16_t)(sign | (uint16_t)(bits >> 16));
+}
+
+/* h_exact[i] = silu(g[i]) * u[i] (fp64) and h_bf16[i] its bf16 rounding,
+ * for i < n. */
+void kqo_swiglu(const double* g, const double* u, int64_t n, double* h_exact,
+                uint16_t* h_bf16) {
+  for (int64_t i = 0; i < n; i++) {
+    h_exact[i] = kqo_silu(g[i]) * u[i];
+    h_bf16[i] = kqo_bf16_from_double(h_exact[i]);
+  }
+}
+
+/* out[n] = sum_k |w^[n][k]| * e[k] (k ascending, fp64), for an error
+ * vector e >= 0 over the K inputs: how far y[n] may move when every input
+ * k may move by e[k]. */
+int kqo_gemv_absw(int fmt, const uint8_t* W, int64_t N, int64_t K, const double* e,
+                  double* out) {
+  int st = kqo_check(fmt, N, K);
+  if (st) return st;
+  int64_t nsb = K / 256;
+  double w[256];
+  for (int64_t n = 0; n < N; n++) {
+    double acc = 0.0;
+    for (int64_t b = 0; b < nsb; b++) {
+      const uint8_t *blk, *par;
+      kqo_locate(fmt, W, N, K, n, b, &blk, &par);
+      kqo_dequant_sb(fmt, blk, par, w);
+      for (int i = 0; i < 256; i++) acc += fabs(w[i]) * e[b * 256 + i];
+    }
+    out[n] = acc;
+  }
+  return KQO_OK;
+}
