@@ -77,6 +77,8 @@ def _load():
         lib.kqo_swiglu.argtypes = [P, P, I64, P, P]
         lib.kqo_swiglu.restype = None
         lib.kqo_gemv_absw.argtypes = [I, P, I64, I64, P, P]
+        lib.kqo_quantize_x_q8.argtypes = [P, I, I64, P, P]
+        lib.kqo_gemv_q8.argtypes = [I, P, I64, I64, P, P, I, P, P]
         _lib = lib
     return _lib
 
@@ -194,6 +196,30 @@ def gemv_absw(fmt: int, W: np.ndarray, N: int, K: int, e: np.ndarray) -> np.ndar
     out = np.empty(N, dtype=np.float64)
     _check(_load().kqo_gemv_absw(fmt, _ptr(W), N, K, _ptr(e), _ptr(out)), "gemv_absw")
     return out
+
+
+def quantize_x_q8(x_bf16: np.ndarray, K: int):
+    """int8 activations of the dp4a path: (xq int8 [n_tok][K], dx fp32
+    [n_tok][K/32]) with dx = amax/127 per 32-block, xq = rint(x / dx)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(-1, K)
+    n_tok = x.shape[0]
+    xq = np.empty((n_tok, K), dtype=np.int8)
+    dx = np.empty((n_tok, K // 32), dtype=np.float32)
+    _check(_load().kqo_quantize_x_q8(_ptr(x), n_tok, K, _ptr(xq), _ptr(dx)), "quantize_x_q8")
+    return xq, dx
+
+
+def gemv_q8(fmt: int, W: np.ndarray, N: int, K: int, xq: np.ndarray, dx: np.ndarray):
+    """(y, A) fp64 [n_tok][N] of the int8-activation GEMV: sum_k w^ * dx * xq."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.int8).reshape(-1, K)
+    dx = np.ascontiguousarray(dx, dtype=np.float32).reshape(xq.shape[0], K // 32)
+    n_tok = xq.shape[0]
+    y = np.empty((n_tok, N), dtype=np.float64)
+    A = np.empty((n_tok, N), dtype=np.float64)
+    _check(_load().kqo_gemv_q8(fmt, _ptr(W), N, K, _ptr(xq), _ptr(dx), n_tok, _ptr(y), _ptr(A)),
+           "gemv_q8")
+    return y, A
 
 
 def tolerance(A: np.ndarray) -> np.ndarray:

@@ -628,3 +628,77 @@ int kqo_gemv_absw(int fmt, const uint8_t* W, int64_t N, int64_t K, const double*
   }
   return KQO_OK;
 }
+
+/* ------------------- int8 activations (dp4a GEMV) ---------------------- */
+/*
+ * The CUDA backend of the pages runs the packed K-quant weights as integer
+ * GEMV kernels with dp4a (the daily.dev summary, answer on exporting GGUF
+ * checkpoints): the activations are quantised to int8 as well, and each
+ * sub-block's dot product is an integer sum.  The pages give no block size
+ * or rounding; the reading taken is per 32 activations of a token (the
+ * Q4_K / Q5_K sub-block), symmetric:
+ *     dx = amax / 127,  xq = round_to_nearest_even(x / dx),  x~ = dx * xq
+ * with amax the largest |x| of the block, both operations in fp32
+ * (binary32 division, round to nearest), and xq = 0, dx = 0 for an all-zero
+ * block.  The GEMV of this path is then exactly
+ *     y[t][n] = sum_k w^[n][k] * x~[t][k]
+ * which this file computes in fp64 like kqo_gemv, and A = sum |w^ x~|.
+ */
+int kqo_quantize_x_q8(const uint16_t* x, int n_tok, int64_t K, int8_t* xq, float* dx) {
+  if (n_tok < 1 || K <= 0 || K % 32 != 0) return KQO_BAD_SHAPE;
+  for (int t = 0; t < n_tok; t++)
+    for (int64_t b = 0; b < K / 32; b++) {
+      const uint16_t* xb = x + (int64_t)t * K + 32 * b;
+      float amax = 0.0f;
+      for (int i = 0; i < 32; i++) {
+        float v = (float)kqo_bf16_to_double(xb[i]);   /* exact: bf16 -> fp32 */
+        float a = fabsf(v);
+        if (a > amax) amax = a;
+      }
+      float d = amax / 127.0f;                         /* binary32, to nearest */
+      dx[(int64_t)t * (K / 32) + b] = d;
+      for (int i = 0; i < 32; i++) {
+        float v = (float)kqo_bf16_to_double(xb[i]);
+        long q = 0;
+        if (d > 0.0f) {
+          float r = v / d;                             /* binary32, to nearest */
+          q = lrintf(r);                               /* to nearest, ties to even */
+          if (q > 127) q = 127;
+          if (q < -127) q = -127;
+        }
+        xq[(int64_t)t * K + 32 * b + i] = (int8_t)q;
+      }
+    }
+  return KQO_OK;
+}
+
+/* y[t][n] = sum_k w^[n][k] * dx[t][k/32] * xq[t][k] (fp64, k ascending),
+ * A[t][n] = sum_k |.|; xq, dx from kqo_quantize_x_q8. */
+int kqo_gemv_q8(int fmt, const uint8_t* W, int64_t N, int64_t K, const int8_t* xq,
+                const float* dx, int n_tok, double* y, double* A) {
+  int st = kqo_check(fmt, N, K);
+  if (st) return st;
+  int64_t nsb = K / 256;
+  double w[256];
+  for (int64_t n = 0; n < N; n++) {
+    for (int t = 0; t < n_tok; t++) {
+      y[t * N + n] = 0.0;
+      if (A) A[t * N + n] = 0.0;
+    }
+    for (int64_t b = 0; b < nsb; b++) {
+      const uint8_t *blk, *par;
+      kqo_locate(fmt, W, N, K, n, b, &blk, &par);
+      kqo_dequant_sb(fmt, blk, par, w);
+      for (int t = 0; t < n_tok; t++) {
+        for (int i = 0; i < 256; i++) {
+          int64_t k = b * 256 + i;
+          double xv = (double)dx[(int64_t)t * (K / 32) + k / 32] * (double)xq[(int64_t)t * K + k];
+          double p = w[i] * xv;
+          y[t * N + n] += p;
+          if (A) A[t * N + n] += fabs(p);
+        }
+      }
+    }
+  }
+  return KQO_OK;
+}
