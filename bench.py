@@ -221,26 +221,30 @@ def build_pools_library(device):
             for f in (wl.Q4_K, wl.Q5_K, wl.Q6_K)}
 
 
-def build_step(pools_dev, n_tok, layers, device):
+def build_step(pools_dev, n_tok, layers, device, spec=None, head_spec=None, base=5):
+    """The decode step of `layers` layers of `spec` (default: the benchmark
+    layer) plus `head_spec`, tiled from the pools; returns (step, pinned
+    host copy of all its activation inputs)."""
     import torch
     from quant_weight_gemv_dequant_b300.decode_step import DecodeStep
+    spec = wl.DECODE_LAYER if spec is None else spec
+    h = wl.LM_HEAD if head_spec is None else head_spec
     Ls = []
     for l in range(layers):
         L = {}
-        for i, m in enumerate(wl.DECODE_LAYER):
-            seed = wl.derive_seed(5, l, i)
+        for i, m in enumerate(spec):
+            seed = wl.derive_seed(base, l, i)
             L[m.name] = (m.fmt, wl.tile_matrix_device(pools_dev[m.fmt], m.fmt, seed, m.N, m.K), m.N, m.K)
         Ls.append(L)
-    h = wl.LM_HEAD
-    head = (h.fmt, wl.tile_matrix_device(pools_dev[h.fmt], h.fmt, wl.derive_seed(5, 999), h.N, h.K), h.N, h.K)
+    head = (h.fmt, wl.tile_matrix_device(pools_dev[h.fmt], h.fmt, wl.derive_seed(base, 999), h.N, h.K), h.N, h.K)
     step = DecodeStep(Ls, head, n_tok, device=device)
     # the step's activation inputs, in the order of step.x_all (layer by layer:
     # x_attn, x_o, x_ffn, x_down; then the head), in one pinned host buffer
     parts = []
     for l in range(layers):
         for j, key in enumerate(("x_attn", "x_o", "x_ffn", "x_down")):
-            parts.append(wl.activations_bf16(wl.derive_seed(5, l, 100 + j), n_tok, step.x[l][key].shape[1]))
-    parts.append(wl.activations_bf16(wl.derive_seed(5, 998), n_tok, h.K))
+            parts.append(wl.activations_bf16(wl.derive_seed(base, l, 100 + j), n_tok, step.x[l][key].shape[1]))
+    parts.append(wl.activations_bf16(wl.derive_seed(base, 998), n_tok, h.K))
     flat = np.concatenate([p_.reshape(-1) for p_ in parts])
     host_x = torch.from_numpy(flat.view(np.int16)).view(torch.bfloat16).pin_memory()
     step.x_all.copy_(host_x)
@@ -609,6 +613,36 @@ def run_kq(args):
                             "cuda_core_ms_per_step": 2 * t4 * 1e3,
                             "cuda_core_path": "two n_tok=4 passes (CUDA cores)",
                             "n_tok_4_ms_per_step": t4 * 1e3}
+
+    # the same step with the SwiGLU chain fused: each layer's gate/up launch
+    # writes h = bf16(silu(gate) * up) and its down projection reads h
+    if not args.no_extra and args.n_tok == 1:
+        sf = type(step)(step.layers, step.lm_head, 1, device=device, fused_ffn=True)
+        sf.x_all.copy_(step.x_all)
+        gf = sf.capture(stream)
+        tf = max_over_ranks(dist, time_graph(gf, stream, args.steps, 3, dist))
+        extra["fused_ffn"] = {"ms_per_step": tf * 1e3, "weight_gb_s": wbytes / tf / 1e9 * world,
+                              "pct_of_hbm_peak": 100 * wbytes / tf / 1e9 / hbm,
+                              "launches_per_step": sf.launches(),
+                              "path": "per layer: q/k/v, o, gate/up writing bf16 silu(gate)*up, down reading it"}
+        del gf, sf
+
+    # the pages' own shapes (hidden 6656, intermediate 19968, vocab 202048;
+    # q, k, v and the attention's sigmoid gate in one launch): a second
+    # 52-layer step of 17.0 GB
+    if not args.no_extra and args.n_tok == 1:
+        sp, _ = build_step(pools, 1, args.layers, device, spec=wl.GLIMMER_LAYER,
+                           head_spec=wl.GLIMMER_HEAD, base=7)
+        gp = sp.capture(stream)
+        tp = max_over_ranks(dist, time_graph(gp, stream, args.steps, 3, dist))
+        pb = sp.weight_bytes()
+        extra["pages_shapes"] = {"workload": "decode_step_52L_h6656_i19968_qkvg_q4k_q6k_lmhead202048",
+                                 "weight_bytes_per_step": pb, "ms_per_step": tp * 1e3,
+                                 "weight_gb_s": pb / tp / 1e9 * world,
+                                 "pct_of_hbm_peak": 100 * pb / tp / 1e9 / hbm,
+                                 "tok_per_s": 1 / tp * world, "launches_per_step": sp.launches()}
+        del gp, sp
+        torch.cuda.empty_cache()
 
     # dominant kernel: grouped gate/up Q4_K GEMV launches
     dur, kbytes, kname = dominant_kernel_timing(step, args.steps, 3, stream)

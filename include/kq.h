@@ -223,6 +223,60 @@ typedef struct {
 kq_status kq_layer_step(const kq_layer* L, const kq_layer_io* io, int n_tok,
                         kq_stream_t stream);
 
+/* The int8-activation (dp4a) GEMV: y[t][n] = sum_k w^[n][k] * x~[t][k],
+ * where x~ = dx * xq is x quantised per 32 positions of a token:
+ *     dx = amax / 127,  xq = round_to_nearest_even(x / dx)   (binary32; 0 if amax = 0)
+ * with amax the largest |x| of the 32.  Every sub-block's dot product is an
+ * exact integer sum (dp4a: four int8 products per instruction); the scales
+ * apply in fp32.  Arguments, requirements and statuses as kq_gemv.  The
+ * result differs from kq_gemv's by the activation rounding: at most
+ * sum_k |w^[n][k]| dx(k) / 2 (plus the usual fp32 accumulation).
+ * Source: the daily.dev summary, answer on exporting GGUF checkpoints (the
+ * CUDA backend runs the K-quant weights as integer GEMV with dp4a); the
+ * pages give no activation block size or rounding: per 32 (the Q4_K / Q5_K
+ * sub-block) and round-to-nearest are this library's reading. */
+kq_status kq_gemv_q8(kq_format f, const void* W_blocks, const void* x_bf16, float* y,
+                     int64_t N_out, int64_t K, int n_tok, kq_stream_t stream);
+
+/* The activation codes of kq_gemv_q8 alone: xq_int8 (device, int8
+ * [n_tok][K]) and dx (device, fp32 [n_tok][K/32]) from x (bf16 [n_tok][K]),
+ * with the kernel's own steps.  K % 256 == 0, 1 <= n_tok <= 16.
+ * Source: as kq_gemv_q8. */
+kq_status kq_quantize_x_q8(const void* x_bf16, int64_t K, int n_tok, void* xq_int8, float* dx,
+                           kq_stream_t stream);
+
+/* The SwiGLU activation fused into the gate/up launch:
+ *     y_gate = w^_gate x,  y_up = w^_up x,
+ *     h[t][n] = bf16( silu(y_gate[t][n]) * y_up[t][n] ),  silu(v) = v / (1 + e^-v)
+ * (silu and the product in fp32, h rounded to nearest, ties to even): h is
+ * the bf16 input of the down projection.
+ *   W_gate, W_up : device, two N_out x K matrices of format f, 16-B aligned
+ *   x_bf16       : device, bf16 [n_tok][K], 16-B aligned
+ *   y_gate, y_up : device, fp32 [n_tok][N_out], overwritten
+ *   h_bf16       : device, bf16 [n_tok][N_out], 16-B aligned, overwritten
+ * One launch where the single-token tensor-core kernel serves the pair (one
+ * token, Q4_K or Q4_G128, 2 * N_out * K >= 2^25): each of its tiles stages
+ * the gate rows and the up rows of the same outputs, and its epilogue forms
+ * h.  Otherwise the grouped GEMV and then a small elementwise kernel.
+ * Statuses as kq_gemv_multi; KQ_ERR_ALIGN if h_bf16 is not 16-B aligned.
+ * Source: the Core AI card's architecture section (SwiGLU feed-forward:
+ * the down projection reads silu(gate) * up); silu is the standard
+ * definition, which the pages do not write out. */
+kq_status kq_gemv_swiglu(kq_format f, const void* W_gate, const void* W_up, const void* x_bf16,
+                         float* y_gate, float* y_up, void* h_bf16, int64_t N_out, int64_t K,
+                         int n_tok, kq_stream_t stream);
+
+/* One SwiGLU feed-forward block: kq_gemv_swiglu(gate, up) into h, then
+ * y_down = w^_down h (kq_gemv), on `stream`.  Requires gate and up of one
+ * format and shape and down.K == gate.N_out; buffers as kq_gemv_swiglu plus
+ * y_down (fp32 [n_tok][down.N_out]).  Nothing but h passes between the two
+ * launches.
+ * Source: as kq_gemv_swiglu (the feed-forward block of the Core AI card's
+ * architecture section). */
+kq_status kq_ffn_swiglu(const kq_matrix* gate, const kq_matrix* up, const kq_matrix* down,
+                        const void* x_ffn, float* y_gate, float* y_up, void* h_bf16,
+                        float* y_down, int n_tok, kq_stream_t stream);
+
 /* W_out[n][k] = w^[n][k] as fp32 (device, [N_out][K]).  Every w^ of these
  * formats is computed with at most one rounding (at the subtraction of the
  * min term), so the result is bit-exact: the fp32 round-to-nearest-even of

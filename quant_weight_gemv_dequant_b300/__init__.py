@@ -66,6 +66,10 @@ def lib() -> ctypes.CDLL:
         L.kq_gemv_multi.argtypes = [I, I, P, P, P, P, I64, I, P]
         L.kq_gemv_noalloc.argtypes = [I, P, P, P, I64, I64, I, P]
         L.kq_layer_step.argtypes = [ctypes.POINTER(kq_layer), ctypes.POINTER(kq_layer_io), I, P]
+        L.kq_gemv_swiglu.argtypes = [I, P, P, P, P, P, P, I64, I64, I, P]
+        L.kq_gemv_q8.argtypes = [I, P, P, P, I64, I64, I, P]
+        L.kq_quantize_x_q8.argtypes = [P, I64, I, P, P, P]
+        L.kq_ffn_swiglu.argtypes = [ctypes.POINTER(kq_matrix)] * 3 + [P, P, P, P, P, I, P]
         L.kq_dequantize.argtypes = [I, P, P, I64, I64, P]
         L.kq_quantize.argtypes = [I, P, I64, I64, P]
         L.kq_merge_g128.argtypes = [P, I64, I64, P]
@@ -75,7 +79,9 @@ def lib() -> ctypes.CDLL:
         L.kq_test_wait_timeout.restype = I
         L.kq_status_str.argtypes = [I]
         L.kq_status_str.restype = ctypes.c_char_p
-        for name in ("kq_gemv", "kq_gemv_multi", "kq_gemv_noalloc", "kq_layer_step", "kq_dequantize", "kq_quantize", "kq_merge_g128"):
+        for name in ("kq_gemv", "kq_gemv_multi", "kq_gemv_noalloc", "kq_layer_step", "kq_dequantize",
+                     "kq_quantize", "kq_merge_g128", "kq_gemv_swiglu", "kq_ffn_swiglu",
+                     "kq_gemv_q8", "kq_quantize_x_q8"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -154,6 +160,35 @@ def kq_gemv_multi(fmt, Ws, ys, N_outs, x, K, n_tok, stream=None, check=True) -> 
     Na = (ctypes.c_int64 * n)(*N_outs)
     st = lib().kq_gemv_multi(fmt, n, Wa, ya, Na, _addr(x), K, n_tok, _stream(stream))
     return _check(st, "kq_gemv_multi") if check else st
+
+
+def kq_gemv_q8(fmt, W, x, y, N_out, K, n_tok, stream=None, check=True) -> int:
+    """The int8-activation (dp4a) GEMV: y = w^ x~, x~ = x quantised per 32."""
+    st = lib().kq_gemv_q8(fmt, _addr(W), _addr(x), _addr(y), N_out, K, n_tok, _stream(stream))
+    return _check(st, "kq_gemv_q8") if check else st
+
+
+def kq_quantize_x_q8(x, K, n_tok, xq, dx, stream=None, check=True) -> int:
+    """The activation codes (int8 [n_tok][K]) and steps (fp32 [n_tok][K/32]) of kq_gemv_q8."""
+    st = lib().kq_quantize_x_q8(_addr(x), K, n_tok, _addr(xq), _addr(dx), _stream(stream))
+    return _check(st, "kq_quantize_x_q8") if check else st
+
+
+def kq_gemv_swiglu(fmt, W_gate, W_up, x, y_gate, y_up, h, N_out, K, n_tok, stream=None,
+                   check=True) -> int:
+    """y_gate, y_up = w^ x for the pair; h = bf16(silu(y_gate) * y_up) (bf16 tensor)."""
+    st = lib().kq_gemv_swiglu(fmt, _addr(W_gate), _addr(W_up), _addr(x), _addr(y_gate), _addr(y_up),
+                              _addr(h), N_out, K, n_tok, _stream(stream))
+    return _check(st, "kq_gemv_swiglu") if check else st
+
+
+def kq_ffn_swiglu(gate: kq_matrix, up: kq_matrix, down: kq_matrix, x, y_gate, y_up, h, y_down,
+                  n_tok: int, stream=None, check=True) -> int:
+    """kq_gemv_swiglu(gate, up) into h, then y_down = w^_down h."""
+    st = lib().kq_ffn_swiglu(ctypes.byref(gate), ctypes.byref(up), ctypes.byref(down), _addr(x),
+                             _addr(y_gate), _addr(y_up), _addr(h), _addr(y_down), n_tok,
+                             _stream(stream))
+    return _check(st, "kq_ffn_swiglu") if check else st
 
 
 def kq_layer_step(layer: kq_layer, io: kq_layer_io, n_tok: int, stream=None, check=True) -> int:

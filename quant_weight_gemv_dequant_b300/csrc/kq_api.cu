@@ -100,6 +100,77 @@ kq_status kq_gemv_multi(kq_format f, int count, const void* const* W, float* con
                                    n_tok, reinterpret_cast<cudaStream_t>(stream), false));
 }
 
+kq_status kq_gemv_q8(kq_format f, const void* W_blocks, const void* x_bf16, float* y,
+                     int64_t N_out, int64_t K, int n_tok, kq_stream_t stream) {
+  kq_status st = check_matrix(f, W_blocks, N_out, K);
+  if (st != KQ_OK) return st;
+  st = check_io(x_bf16, y, n_tok);
+  if (st != KQ_OK) return st;
+  kq::GemvGroup g{};
+  g.count = 1;
+  g.W[0] = static_cast<const uint8_t*>(W_blocks);
+  g.y[0] = y;
+  g.N[0] = static_cast<int>(N_out);
+  return status_of(kq::launch_q8(f, g, static_cast<const uint16_t*>(x_bf16), static_cast<int>(K),
+                                 n_tok, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kq_status kq_quantize_x_q8(const void* x_bf16, int64_t K, int n_tok, void* xq_int8, float* dx,
+                           kq_stream_t stream) {
+  if (x_bf16 == nullptr || xq_int8 == nullptr || dx == nullptr) return KQ_ERR_ARG;
+  if (n_tok < 1 || n_tok > 16) return KQ_ERR_ARG;
+  if (K <= 0 || K % 256 != 0 || K > (int64_t{1} << 30)) return KQ_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(dx) & 3) != 0 || (reinterpret_cast<uintptr_t>(x_bf16) & 1) != 0)
+    return KQ_ERR_ALIGN;
+  return kq::launch_quantize_x_q8(static_cast<const uint16_t*>(x_bf16), K * n_tok,
+                                  static_cast<int8_t*>(xq_int8), dx,
+                                  reinterpret_cast<cudaStream_t>(stream))
+             ? KQ_OK
+             : KQ_ERR_CUDA;
+}
+
+kq_status kq_gemv_swiglu(kq_format f, const void* W_gate, const void* W_up, const void* x_bf16,
+                         float* y_gate, float* y_up, void* h_bf16, int64_t N_out, int64_t K,
+                         int n_tok, kq_stream_t stream) {
+  kq_status st = check_matrix(f, W_gate, N_out, K);
+  if (st != KQ_OK) return st;
+  st = check_matrix(f, W_up, N_out, K);
+  if (st != KQ_OK) return st;
+  st = check_io(x_bf16, y_gate, n_tok);
+  if (st != KQ_OK) return st;
+  st = check_io(x_bf16, y_up, n_tok);
+  if (st != KQ_OK) return st;
+  if (h_bf16 == nullptr) return KQ_ERR_ARG;
+  if (!aligned16(h_bf16)) return KQ_ERR_ALIGN;
+  kq::GemvGroup g{};
+  g.count = 2;
+  g.W[0] = static_cast<const uint8_t*>(W_gate);
+  g.W[1] = static_cast<const uint8_t*>(W_up);
+  g.y[0] = y_gate;
+  g.y[1] = y_up;
+  g.N[0] = g.N[1] = static_cast<int>(N_out);
+  return status_of(kq::launch_swiglu(f, g, static_cast<const uint16_t*>(x_bf16), static_cast<int>(K),
+                                     n_tok, static_cast<uint16_t*>(h_bf16),
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kq_status kq_ffn_swiglu(const kq_matrix* gate, const kq_matrix* up, const kq_matrix* down,
+                        const void* x_ffn, float* y_gate, float* y_up, void* h_bf16,
+                        float* y_down, int n_tok, kq_stream_t stream) {
+  if (gate == nullptr || up == nullptr || down == nullptr) return KQ_ERR_ARG;
+  if (gate->format != up->format || gate->N_out != up->N_out || gate->K != up->K ||
+      down->K != gate->N_out)
+    return KQ_ERR_SHAPE;
+  kq_status st = check_matrix(down->format, down->W, down->N_out, down->K);
+  if (st != KQ_OK) return st;
+  st = check_io(h_bf16, y_down, n_tok);
+  if (st != KQ_OK) return st;
+  st = kq_gemv_swiglu(gate->format, gate->W, up->W, x_ffn, y_gate, y_up, h_bf16, gate->N_out,
+                      gate->K, n_tok, stream);
+  if (st != KQ_OK) return st;
+  return kq_gemv(down->format, down->W, h_bf16, y_down, down->N_out, down->K, n_tok, stream);
+}
+
 kq_status kq_layer_step(const kq_layer* L, const kq_layer_io* io, int n_tok, kq_stream_t stream) {
   if (L == nullptr || io == nullptr) return KQ_ERR_ARG;
   const kq_matrix* mats[7] = {&L->q, &L->k, &L->v, &L->o, &L->gate, &L->up, &L->down};

@@ -37,6 +37,22 @@ StreamResult launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K
 StreamResult launch_gemv(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
                          cudaStream_t stream, bool noalloc);
 
+// The dp4a path: x quantised to int8 per 32 positions of a token (dx =
+// amax / 127, xq = rint(x / dx), binary32), integer sub-block dot products,
+// on the streaming kernel in launches of up to four tokens.
+StreamResult launch_q8(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
+                       cudaStream_t stream);
+// The codes and steps of the dp4a path alone (n a multiple of 32).
+bool launch_quantize_x_q8(const uint16_t* x, int64_t n, int8_t* xq, float* dx,
+                          cudaStream_t stream);
+
+// SwiGLU input of the down projection: g = {gate, up} (same format and
+// shape), y written as for launch_gemv, and h = bf16(silu(gate) * up)
+// ([n_tok][N]).  Fused into the gate/up launch on the single-token
+// tensor-core kernel; otherwise the grouped GEMV then an elementwise kernel.
+StreamResult launch_swiglu(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
+                           uint16_t* h, cudaStream_t stream);
+
 // One warp whose bounded wait (limit ~wait_us) runs out on a barrier that
 // nothing completes; the event is counted like any other timeout.
 bool launch_wait_timeout_probe(unsigned int wait_us, cudaStream_t stream);

@@ -288,8 +288,15 @@ struct Params {
   int tma;                   // 1: a stage arrives as one tensor copy per plane
   uint32_t slot, pslot, pbase, stage;   // StageShape of the ring
   uint32_t tx;               // bytes the tensor copies of one stage deliver
+  // SwiGLU mode of the single-token tensor-core kernel: g holds (gate, up)
+  // of the same shape; a tile is tile_rows / 2 output features, staged as
+  // their gate rows then their up rows, and the kernel also writes
+  // h = bf16(silu(gate) * up) (bf16 [N]).
+  int swiglu = 0;
+  uint16_t* h = nullptr;
   // per matrix: 2-D tensor maps (8-byte elements x rows) of the records / the
   // G128 q plane [0] and the G128 param plane [1]; box = slot bytes x tile_rows
+  // (SwiGLU mode: x tile_rows / 2)
   CUtensorMap tm[kMaxGroup][2];
 };
 
@@ -303,8 +310,9 @@ __device__ __forceinline__ Tile tile_of(const Params& p, int t) {
     }
   Tile r;
   r.mi = mi;
-  r.row0 = (t - base) * p.tile_rows;
-  r.rcnt = min(p.tile_rows, pick(p.g.N, mi) - r.row0);
+  const int feat = p.swiglu ? p.tile_rows / 2 : p.tile_rows;   // output features per tile
+  r.row0 = (t - base) * feat;
+  r.rcnt = min(feat, pick(p.g.N, mi) - r.row0);
   return r;
 }
 
@@ -576,10 +584,20 @@ __device__ __forceinline__ void issue_stage(const Params& p, uint8_t* smem, uint
     // rows past the matrix and bytes past a row are zero-filled and counted
     if ((threadIdx.x & 31) == 0) {
       mbar_arrive_tx(full, p.tx);
-      tma_load_2d(st_a, &p.tm[tl.mi][0], ((sl * G::kQBytes) & ~15) / 8, tl.row0, full);
-      if constexpr (F == kG128)
-        tma_load_2d(st_a + p.pbase, &p.tm[tl.mi][1], ((sl * G::kPBytes) & ~15) / 8, tl.row0,
-                    full);
+      const int xq = ((sl * G::kQBytes) & ~15) / 8, xp = ((sl * G::kPBytes) & ~15) / 8;
+      if (p.swiglu) {
+        // the tile's gate rows, then the same rows of up
+        const uint32_t half = static_cast<uint32_t>(p.tile_rows / 2);
+        tma_load_2d(st_a, &p.tm[0][0], xq, tl.row0, full);
+        tma_load_2d(st_a + half * p.slot, &p.tm[1][0], xq, tl.row0, full);
+        if constexpr (F == kG128) {
+          tma_load_2d(st_a + p.pbase, &p.tm[0][1], xp, tl.row0, full);
+          tma_load_2d(st_a + p.pbase + half * p.pslot, &p.tm[1][1], xp, tl.row0, full);
+        }
+      } else {
+        tma_load_2d(st_a, &p.tm[tl.mi][0], xq, tl.row0, full);
+        if constexpr (F == kG128) tma_load_2d(st_a + p.pbase, &p.tm[tl.mi][1], xp, tl.row0, full);
+      }
     }
     return;
   }
@@ -1103,12 +1121,314 @@ __device__ __forceinline__ void stage_q6(const Params& p, const Tile& tl, int sl
   }
 }
 
+// ------------------------------------------- int8 activations (dp4a)
+//
+// The x mode XM == kXQ8 of gemv_stream: the activations are quantised to
+// int8 per 32 positions of a token, dx = amax / 127 and xq = rint(x / dx),
+// both in binary32 (the daily.dev summary says the CUDA backend runs the
+// K-quant weights as integer GEMV with dp4a; block size and rounding are
+// this library's reading), and every sub-block's dot product is an exact
+// integer sum built with dp4a (four int8 products per instruction):
+//   y += dx (d sc sum q xq - dmin m sum xq)        (Q4_K, Q5_K, Q4_G128)
+//   y += dx  d sc (sum q xq - 32 sum xq)            (Q6_K)
+// The staged segment holds the codes in position order (16 bytes of padding
+// per 64 positions, so a half-warp's 16-byte loads of different units hit
+// different banks), then dx per 32 positions, then the code sum of every
+// part (kPart positions: the run of one unit within one sub-block).
+constexpr int kXF32 = 0, kXBF16 = 1, kXQ8 = 2;
+
+__host__ __device__ constexpr uint32_t q8_row_bytes(int kpad) {
+  return static_cast<uint32_t>(kpad + 16 * (kpad / 64));
+}
+__host__ __device__ constexpr uint32_t q8_x_bytes(int nt, int kpad, int part) {
+  return (static_cast<uint32_t>(nt) * q8_row_bytes(kpad) + 4u * nt * (kpad / 32) +
+          4u * nt * (kpad / part) + 127u) & ~127u;
+}
+__device__ __forceinline__ uint32_t q8_pos(int pos) { return static_cast<uint32_t>(pos + 16 * (pos / 64)); }
+
+// The int8 code of x (binary32) for the block step d: rint(x / d) with the
+// division rounded to nearest, 0 when d == 0.
+__device__ __forceinline__ int q8_code(float v, float d) {
+  if (!(d > 0.0f)) return 0;
+  int q = __float2int_rn(__fdiv_rn(v, d));
+  return q > 127 ? 127 : (q < -127 ? -127 : q);
+}
+
+template <int F, int NT>
+__device__ void stage_x_q8(const Params& p, uint8_t* smem, int kbase) {
+  using G = Geo<F, NT, 1, 1>;
+  constexpr int P = G::kPart;              // positions per part sum: 32..4
+  const uint32_t rowb = q8_row_bytes(p.kpad);
+  float* dxs = reinterpret_cast<float*>(smem + NT * rowb);
+  int* ps = reinterpret_cast<int*>(dxs + NT * (p.kpad / 32));
+  const int per_tok = p.kpad / 8;          // items of 8 positions (a multiple of 32)
+  const int lane = threadIdx.x & 31;
+  for (int base = static_cast<int>(threadIdx.x) & ~31; base < NT * per_tok;
+       base += static_cast<int>(blockDim.x)) {
+    const int q = base + lane;
+    const int tk = q / per_tok, c = q % per_tok;
+    const int k = kbase + 8 * c;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (tk < p.nt && k < p.K) v = *reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(tk) * p.K + k);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[2 * j] = __uint_as_float(w[j] << 16);
+      f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      amax = fmaxf(amax, fmaxf(fabsf(f[2 * j]), fabsf(f[2 * j + 1])));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    const float d = __fdiv_rn(amax, 127.0f);
+    int qs[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) qs[j] = q8_code(f[j], d);
+    uint32_t b0 = 0, b1 = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      b0 |= (static_cast<uint32_t>(qs[j]) & 0xFFu) << (8 * j);
+      b1 |= (static_cast<uint32_t>(qs[4 + j]) & 0xFFu) << (8 * j);
+    }
+    *reinterpret_cast<uint2*>(smem + tk * rowb + q8_pos(8 * c)) = make_uint2(b0, b1);
+    if ((c & 3) == 0) dxs[tk * (p.kpad / 32) + c / 4] = d;
+    // code sums per part
+    int s0 = qs[0] + qs[1] + qs[2] + qs[3], s1 = qs[4] + qs[5] + qs[6] + qs[7];
+    if constexpr (P == 4) {
+      ps[tk * (p.kpad / 4) + 2 * c] = s0;
+      ps[tk * (p.kpad / 4) + 2 * c + 1] = s1;
+    } else {
+      int sp = s0 + s1;
+      if constexpr (P >= 16) sp += __shfl_xor_sync(0xFFFFFFFFu, sp, 1);
+      if constexpr (P >= 32) sp += __shfl_xor_sync(0xFFFFFFFFu, sp, 2);
+      if ((c & (P / 8 - 1)) == 0) ps[tk * (p.kpad / P) + c / (P / 8)] = sp;
+    }
+  }
+}
+
+// NW consecutive 32-bit words of the staged codes from shared address a
+// (16-byte aligned for NW >= 4, 8-byte aligned for NW == 2)
+template <int NW>
+__device__ __forceinline__ void lds_codes(uint32_t a, uint32_t (&w)[NW]) {
+#pragma unroll
+  for (int i = 0; i < NW; i += 4) {
+    if constexpr (NW >= 4) {
+      const uint4 v = lds128(a + 4 * i);
+      w[i] = v.x; w[i + 1] = v.y; w[i + 2] = v.z; w[i + 3] = v.w;
+    } else {
+      const uint2 v = lds64(a);
+      w[0] = v.x; w[1] = v.y;
+    }
+  }
+}
+
+// One stage of a Q4_K / Q5_K / Q4_G128 tile on int8 activations, for the NR
+// live rows of this thread (unit and accumulators as in stage_q4).
+template <int F, int NT, int RT, int WC, int NR>
+__device__ __forceinline__ void stage_q4_q8(const Params& p, const Tile& tl, int sl, int xsl,
+                                            uint32_t st, uint32_t xs, int hw, int sbl, int c,
+                                            int off, const ScaleSel& ss, float2 (&acc)[RT][NT]) {
+  using G = Geo<F, NT, RT, WC>;
+  constexpr int kCW = G::kCW, NW = kCW / 8, P = G::kPart;
+  const int kb = xsl * G::kSlabK + sbl * 256 + 64 * c;   // the chunk's 64-block
+  const uint32_t rowb = q8_row_bytes(p.kpad);
+  const uint32_t dxa = xs + NT * rowb;
+  const uint32_t psa = dxa + 4u * NT * (p.kpad / 32);
+  uint32_t w[NR][NW], hq[NR][NW];
+  uint32_t rec[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    const uint32_t rs = st + (hw + 2 * WC * r) * p.slot;
+#pragma unroll
+    for (int j = 0; j < NW; ++j) hq[r][j] = 0;
+    if constexpr (F == kG128) {
+      rec[r] = rs;
+      lds_words<NW>(rs + 128 * sbl + 32 * c + off, w[r]);
+    } else {
+      rec[r] = rs + G::kBB * sbl;
+      lds_words<NW>(rec[r] + (F == kQ4K ? 16 : 48) + 32 * c + off, w[r]);
+      if constexpr (F == kQ5K) lds_words<NW>(rec[r] + 16 + off, hq[r]);
+    }
+  }
+  const int rlo = (2 * c + 28) & 31, rhi = (2 * c + 29) & 31;   // Q5_K: bit 2c(+1) -> bit 4
+  int il[NR][NT], ih[NR][NT];
+#pragma unroll
+  for (int r = 0; r < NR; ++r)
+#pragma unroll
+    for (int k = 0; k < NT; ++k) il[r][k] = ih[r][k] = 0;
+#pragma unroll
+  for (int k = 0; k < NT; ++k) {
+    uint32_t xl[NW], xh[NW];
+    lds_codes<NW>(xs + k * rowb + q8_pos(kb + off), xl);
+    lds_codes<NW>(xs + k * rowb + q8_pos(kb + 32 + off), xh);
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+      for (int i = 0; i < NW; ++i) {
+        uint32_t lo = w[r][i] & 0x0F0F0F0Fu, hi = (w[r][i] >> 4) & 0x0F0F0F0Fu;
+        if constexpr (F == kQ5K) {
+          lo |= __funnelshift_r(hq[r][i], hq[r][i], rlo) & 0x10101010u;
+          hi |= __funnelshift_r(hq[r][i], hq[r][i], rhi) & 0x10101010u;
+        }
+        il[r][k] = __dp4a(static_cast<int>(lo), static_cast<int>(xl[i]), il[r][k]);
+        ih[r][k] = __dp4a(static_cast<int>(hi), static_cast<int>(xh[i]), ih[r][k]);
+      }
+  }
+  // scales: acc += (dx_lo, dx_hi) * (d sc * sum q xq - dmin m * sum xq)
+  float2 dxp[NT], sxp[NT];
+#pragma unroll
+  for (int k = 0; k < NT; ++k) {
+    dxp[k] = lds_f2(dxa + 4u * (k * (p.kpad / 32) + kb / 32));
+    int slo, shi;
+    asm volatile("ld.shared.s32 %0, [%1];" : "=r"(slo) : "r"(psa + 4u * (k * (p.kpad / P) + (kb + off) / P)));
+    asm volatile("ld.shared.s32 %0, [%1];" : "=r"(shi) : "r"(psa + 4u * (k * (p.kpad / P) + (kb + 32 + off) / P)));
+    sxp[k] = make_float2(static_cast<float>(slo), static_cast<float>(shi));
+  }
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    float2 dsc, ndm;
+    if constexpr (F == kG128) {
+      const int row = hw + 2 * WC * r;
+      const uint32_t po =
+          (static_cast<uint32_t>(tl.row0 + row) * ((8u * p.nsb) & 15u) + sl * G::kPBytes) & 15u;
+      const uint2 pr = lds64(st + p.pbase + row * p.pslot + po + 8 * sbl);
+      const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
+      const int g = c >> 1;
+      const float sc = static_cast<float>((pr.y >> (8 * g)) & 0xFF);
+      const float mn = static_cast<float>((pr.y >> (16 + 8 * g)) & 0xFF);
+      dsc = make_float2(dd.x * sc, dd.x * sc);
+      ndm = make_float2(-dd.y * mn, -dd.y * mn);
+    } else {
+      const uint4 hdr = lds128(rec[r]);
+      const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
+      uint32_t scp, mnp;
+      scale_pair6(ss, hdr.y, hdr.z, hdr.w, scp, mnp);
+      dsc = make_float2(dd.x * static_cast<float>(scp & 0xFF), dd.x * static_cast<float>(scp >> 8));
+      ndm = make_float2(-dd.y * static_cast<float>(mnp & 0xFF), -dd.y * static_cast<float>(mnp >> 8));
+    }
+#pragma unroll
+    for (int k = 0; k < NT; ++k) {
+      const float2 t = __ffma2_rn(dsc, make_float2(static_cast<float>(il[r][k]), static_cast<float>(ih[r][k])),
+                                  __fmul2_rn(ndm, sxp[k]));
+      acc[r][k] = __ffma2_rn(dxp[k], t, acc[r][k]);
+    }
+  }
+}
+
+// One stage of a Q6_K tile on int8 activations (unit as in stage_q6: four
+// t-runs of kCW/4 positions; each 6-bit field is assembled into a byte and
+// multiplied with dp4a, and q - 32 becomes sum q xq - 32 sum xq, exactly).
+template <int NT, int RT, int WC, int NR>
+__device__ __forceinline__ void stage_q6_q8(const Params& p, const Tile& tl, int sl, int xsl,
+                                            uint32_t st, uint32_t xs, int hw, int sbl, int un,
+                                            float2 (&acc)[RT][NT]) {
+  using G = Geo<kQ6K, NT, RT, WC>;
+  constexpr int kCW = G::kCW, QW = kCW / 16, P = G::kPart;
+  const int h = un / (G::kUnitsPerSB / 2);
+  const int u2 = un % (G::kUnitsPerSB / 2);
+  const int l0 = u2 * (kCW / 4);
+  const int su = l0 >> 4;
+  const int kb = xsl * G::kSlabK + sbl * 256 + 128 * h;   // the unit's 128-block
+  const uint32_t rowb = q8_row_bytes(p.kpad);
+  const uint32_t dxa = xs + NT * rowb;
+  const uint32_t psa = dxa + 4u * NT * (p.kpad / 32);
+  uint32_t rb[NR], rsh[NR];
+  uint32_t A[NR][QW], B[NR][QW], H[NR][QW];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    const int row = hw + 2 * WC * r;
+    const uint32_t ro =
+        (static_cast<uint32_t>(tl.row0 + row) * ((210u * p.nsb) & 15u) + sl * G::kQBytes) & 15u;
+    const uint32_t rec = st + row * p.slot + ro + 210 * sbl;
+    rb[r] = rec & ~3u;
+    rsh[r] = (rec & 3u) * 8u;
+    lds_words_rec<QW>(rb[r], rsh[r], 64 * h + l0, A[r]);
+    lds_words_rec<QW>(rb[r], rsh[r], 64 * h + 32 + l0, B[r]);
+    lds_words_rec<QW>(rb[r], rsh[r], 128 + 32 * h + l0, H[r]);
+  }
+  int it[NR][NT][4];
+#pragma unroll
+  for (int r = 0; r < NR; ++r)
+#pragma unroll
+    for (int k = 0; k < NT; ++k)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) it[r][k][t] = 0;
+  const uint32_t M = 0x0F0F0F0Fu, M6 = 0x3F3F3F3Fu;
+#pragma unroll
+  for (int k = 0; k < NT; ++k) {
+    uint32_t xt[4][QW];   // codes of t-run t, positions l0 .. l0 + kCW/4
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if constexpr (QW >= 4) {
+        lds_codes<QW>(xs + k * rowb + q8_pos(kb + 32 * t + l0), xt[t]);
+      } else if constexpr (QW == 2) {
+        lds_codes<2>(xs + k * rowb + q8_pos(kb + 32 * t + l0), xt[t]);
+      } else {
+        xt[t][0] = lds32(xs + k * rowb + q8_pos(kb + 32 * t + l0));
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+      for (int j = 0; j < QW; ++j) {
+        const uint32_t q0 = bitsel(A[r][j], H[r][j] << 4, M) & M6;
+        const uint32_t q2 = bitsel(A[r][j] >> 4, H[r][j], M) & M6;
+        const uint32_t q1 = bitsel(B[r][j], H[r][j] << 2, M) & M6;
+        const uint32_t q3 = bitsel(B[r][j] >> 4, H[r][j] >> 2, M) & M6;
+        it[r][k][0] = __dp4a(static_cast<int>(q0), static_cast<int>(xt[0][j]), it[r][k][0]);
+        it[r][k][1] = __dp4a(static_cast<int>(q1), static_cast<int>(xt[1][j]), it[r][k][1]);
+        it[r][k][2] = __dp4a(static_cast<int>(q2), static_cast<int>(xt[2][j]), it[r][k][2]);
+        it[r][k][3] = __dp4a(static_cast<int>(q3), static_cast<int>(xt[3][j]), it[r][k][3]);
+      }
+  }
+  // per t-run: the code sum of its part and dx of its 32 positions
+  float2 dx02[NT], dx13[NT];
+  int s[NT][4];
+#pragma unroll
+  for (int k = 0; k < NT; ++k) {
+    const float4 d4 = lds_f4(dxa + 4u * (k * (p.kpad / 32) + kb / 32));   // t-runs 0..3
+    dx02[k] = make_float2(d4.x, d4.z);
+    dx13[k] = make_float2(d4.y, d4.w);
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      asm volatile("ld.shared.s32 %0, [%1];"
+                   : "=r"(s[k][t])
+                   : "r"(psa + 4u * (k * (p.kpad / P) + (kb + 32 * t + l0) / P)));
+  }
+  const uint32_t sel0 = su | ((8 | su) << 4) | ((8 | su) << 8) | ((8 | su) << 12);
+  const uint32_t sel2 = (su + 2) | ((10 + su) << 4) | ((10 + su) << 8) | ((10 + su) << 12);
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    uint32_t S[2], D[1];
+    lds_words_rec<2>(rb[r], rsh[r], 192 + 8 * h, S);
+    lds_words_rec<1>(rb[r], rsh[r], 208, D);
+    const float d = half_bits_to_float(D[0] & 0xFFFFu);
+    const float2 ds02 = make_float2(d * static_cast<float>(static_cast<int>(prmt(S[0], 0, sel0))),
+                                    d * static_cast<float>(static_cast<int>(prmt(S[1], 0, sel0))));
+    const float2 ds13 = make_float2(d * static_cast<float>(static_cast<int>(prmt(S[0], 0, sel2))),
+                                    d * static_cast<float>(static_cast<int>(prmt(S[1], 0, sel2))));
+#pragma unroll
+    for (int k = 0; k < NT; ++k) {
+      const float2 i02 = make_float2(static_cast<float>(it[r][k][0] - 32 * s[k][0]),
+                                     static_cast<float>(it[r][k][2] - 32 * s[k][2]));
+      const float2 i13 = make_float2(static_cast<float>(it[r][k][1] - 32 * s[k][1]),
+                                     static_cast<float>(it[r][k][3] - 32 * s[k][3]));
+      acc[r][k] = __ffma2_rn(__fmul2_rn(dx02[k], ds02), i02, acc[r][k]);
+      acc[r][k] = __ffma2_rn(__fmul2_rn(dx13[k], ds13), i13, acc[r][k]);
+    }
+  }
+}
+
 constexpr int kMaxStages = 8;
 
 // Registers capped so that three CTAs (two with eight consumer warps) fit an SM.
-template <int F, int NT, int RT, int WC, bool XBF>
+// XM: how x is staged -- kXF32 (fp32, pre-scaled), kXBF16 (bf16, when fp32
+// would not fit) or kXQ8 (int8 codes: the dp4a path).
+template <int F, int NT, int RT, int WC, int XM>
 __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
     gemv_stream(const __grid_constant__ Params p, int stages) {
+  constexpr bool XBF = XM == kXBF16;
   using G = Geo<F, NT, RT, WC>;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
@@ -1145,7 +1465,10 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
   if (producer) produce_prefill<G>(p, smem, ring_a, bar_full, stage_tile, stages, cta, cps, sl0, ring);
   // x may be produced by the previous kernel: wait for it to complete
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  stage_x<F, NT, XBF>(p, smem, kseg * p.kpad);
+  if constexpr (XM == kXQ8)
+    stage_x_q8<F, NT>(p, smem, kseg * p.kpad);
+  else
+    stage_x<F, NT, XBF>(p, smem, kseg * p.kpad);
   __syncthreads();
   if (producer) {
     produce_rest<G>(p, smem, ring_a, bar_full, bar_empty, stage_tile, stages, cta, cps, kseg, sl0,
@@ -1186,10 +1509,16 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
       const int nr = tl.rcnt > hw ? min(RT, (tl.rcnt - hw + 2 * WC - 1) / (2 * WC)) : 0;
       auto run = [&](auto nrc) {
         constexpr int NR = decltype(nrc)::value;
-        if constexpr (F == kQ6K)
+        if constexpr (XM == kXQ8) {
+          if constexpr (F == kQ6K)
+            stage_q6_q8<NT, RT, WC, NR>(p, tl, sl, xsl, st, xs, hw, sbl, un, acc);
+          else
+            stage_q4_q8<F, NT, RT, WC, NR>(p, tl, sl, xsl, st, xs, hw, sbl, c, off, ss, acc);
+        } else if constexpr (F == kQ6K) {
           stage_q6<NT, RT, WC, NR, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, un, acc);
-        else
+        } else {
           stage_q4<F, NT, RT, WC, NR, XBF>(p, tl, sl, xsl, st, xs, hw, sbl, c, off, ss, acc);
+        }
       };
       if (nr == RT) {
         run(std::integral_constant<int, RT>{});
@@ -2002,10 +2331,12 @@ __device__ __forceinline__ void tc_scales_q4(const Params& p, const Tile& tl, in
   }
 }
 
-// One stage for this warp's 16 rows (rbase .. rbase + 15): Q4_K, Q4_G128.
+// One stage for this warp's 16 stage rows: lane (g, t) takes stage rows ra +
+// g and rb + g (the mma's rows g and g + 8): ra, rb = 16 w, 16 w + 8, or in
+// SwiGLU mode the gate row 8 w + g and the same feature's up row.
 template <class G>
 __device__ __forceinline__ void tc_stage_q4(const Params& p, const Tile& tl, int sl, int xsl,
-                                            uint32_t st, int rbase, uint32_t xsh,
+                                            uint32_t st, int ra, int rb, uint32_t xsh,
                                             const ScaleSel& ss, float2 (&acc)[2]) {
   constexpr int F = G::kF;
   const int lane = threadIdx.x & 31;
@@ -2020,21 +2351,45 @@ __device__ __forceinline__ void tc_stage_q4(const Params& p, const Tile& tl, int
     const int sbx = xsl * G::kSlabSB + s;   // super-block of the staged segment
     const uint32_t xlo = act_lo ? xsh + 64u * (8 * sbx + 2 * t) : zero;
     const uint32_t xhi = act_hi ? xsh + 64u * (8 * sbx + 2 * t + 1) : zero;
-    uint32_t qa[2];   // rows g, g+8: the chunk's qs bytes
+    uint32_t qa[2];   // rows ra + g, rb + g: the chunk's qs bytes
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const uint32_t rs = st + (rbase + g + 8 * h) * p.slot;
+      const uint32_t rs = st + ((h ? rb : ra) + g) * p.slot;
       qa[h] = (F == kG128) ? rs + 128 * s + 32 * t : rs + G::kBB * s + 16 + 32 * t;
     }
     float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     tc_sb_product(qa[0], qa[1], xlo, xhi, d);
     float2 s1g, s2g, s1h, s2h;
-    tc_scales_q4<G>(p, tl, sl, st, rbase + g, s, ss, t, s1g, s2g);
-    tc_scales_q4<G>(p, tl, sl, st, rbase + g + 8, s, ss, t, s1h, s2h);
+    tc_scales_q4<G>(p, tl, sl, st, ra + g, s, ss, t, s1g, s2g);
+    tc_scales_q4<G>(p, tl, sl, st, rb + g, s, ss, t, s1h, s2h);
     const float2 sx = lds_f2(xsum + 4u * (8 * sbx + 2 * t));
     const float2 cs = lds_f2(xscl + 4u * (8 * sbx + 2 * t));   // column scales
     tc_epilogue(acc, d, __fmul2_rn(s1g, cs), s2g, __fmul2_rn(s1h, cs), s2h, sx);
   }
+}
+
+// bf16(silu(g) * u), silu(v) = v / (1 + e^-v), evaluated in fp32 and
+// rounded to nearest (ties to even).
+__device__ __forceinline__ uint16_t swiglu_bf16(float gv, float uv) {
+  const __nv_bfloat16 hb = __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
+  return *reinterpret_cast<const uint16_t*>(&hb);
+}
+
+// SwiGLU mode: feature n's gate and up sums -> y_gate, y_up (fp32) and h.
+__device__ __forceinline__ void swiglu_store(const Params& p, int64_t n, float gv, float uv) {
+  p.g.y[0][n] = gv;
+  p.g.y[1][n] = uv;
+  p.h[n] = swiglu_bf16(gv, uv);
+}
+
+// h[i] = bf16(silu(g[i]) * u[i]) for i < n (the SwiGLU activation after a
+// gate/up launch that did not fuse it).
+__global__ void __launch_bounds__(256) swiglu_elementwise(const float* __restrict__ gv,
+                                                          const float* __restrict__ uv,
+                                                          uint16_t* __restrict__ h, int64_t n) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (i < n) h[i] = swiglu_bf16(gv[i], uv[i]);
 }
 
 // The reducer warp: for every unit the consumers finish (in order), publish
@@ -2052,7 +2407,8 @@ __device__ __forceinline__ void tc_reduce(const Params& p, uint32_t psum, uint32
     const int tix = part_tile[b];
     if (tix < 0) return;
     const Tile tl = tile_of(p, tix);
-    const int n = tl.rcnt * NTP;
+    // SwiGLU mode: all stage rows (gate rows, then up rows)
+    const int n = p.swiglu ? p.tile_rows * NTP : tl.rcnt * NTP;
     float* part = p.part + static_cast<int64_t>(tix) * p.tile_rows * NTP;
     const uint32_t buf = psum + 4u * static_cast<uint32_t>(b * p.tile_rows * NTP);
     for (int e = lane; e < n; e += 32) {
@@ -2084,6 +2440,16 @@ __device__ __forceinline__ void tc_reduce(const Params& p, uint32_t psum, uint32
 #pragma unroll
           for (int i = 0; i < kR; ++i)
             if (e0 + lane + 32 * i < n) a[i] += __ldcg(pj + 32 * i);
+        }
+        if (NTP == 1 && p.swiglu) {
+          // one 256-value pass (kR = 8, tile_rows = 256): a[i], i < 4, is the
+          // gate sum of feature lane + 32 i and a[i + 4] its up sum
+#pragma unroll
+          for (int i = 0; i < kR / 2; ++i) {
+            const int r = lane + 32 * i;
+            if (r < tl.rcnt) swiglu_store(p, tl.row0 + r, a[i], a[i + kR / 2]);
+          }
+          continue;
         }
 #pragma unroll
         for (int i = 0; i < kR; ++i) {
@@ -2146,7 +2512,12 @@ __global__ void __launch_bounds__((WC + 2) * 32, WC <= 8 ? 2 : 1)
     return;
   }
   const int g = lane >> 2, t = lane & 3;
-  const int rbase = 16 * warp;
+  // stage rows of this warp: ra + g and rb + g; in SwiGLU mode the gate and
+  // up rows of the tile's features 8 warp .. 8 warp + 7
+  const int half = p.tile_rows / 2;
+  const int ra = p.swiglu ? 8 * warp : 16 * warp;
+  const int rb = p.swiglu ? half + 8 * warp : 16 * warp + 8;
+  const int rfirst = p.swiglu ? 8 * warp : 16 * warp;   // this warp's first feature of the tile
   const ScaleSel ss = scale_sel(t);
   float2 acc[2];
   Tile tl{};
@@ -2163,7 +2534,7 @@ __global__ void __launch_bounds__((WC + 2) * 32, WC <= 8 ? 2 : 1)
       const uint32_t buf = psum + 4u * static_cast<uint32_t>(b * p.tile_rows);
 #pragma unroll
       for (int h = 0; h < 2; ++h)
-        asm volatile("st.shared.f32 [%0], %1;" ::"r"(buf + 4u * (rbase + g + 8 * h)), "f"(v[h])
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(buf + 4u * ((h ? rb : ra) + g)), "f"(v[h])
                      : "memory");
     }
     if (warp == 0 && lane == 0) part_tile[b] = tix;
@@ -2188,7 +2559,7 @@ __global__ void __launch_bounds__((WC + 2) * 32, WC <= 8 ? 2 : 1)
       acc[0] = acc[1] = make_float2(0.0f, 0.0f);
     }
     const uint32_t st = ring_a + slot * p.stage;
-    if (rbase < tl.rcnt) tc_stage_q4<G>(p, tl, sl, xsl, st, rbase, xsh, ss, acc);
+    if (rfirst < tl.rcnt) tc_stage_q4<G>(p, tl, sl, xsl, st, ra, rb, xsh, ss, acc);
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
     if (xsl == p.slabs - 1) {
@@ -2204,10 +2575,14 @@ __global__ void __launch_bounds__((WC + 2) * 32, WC <= 8 ? 2 : 1)
       if (p.ksplit == 1) {
         float* y = pick(p.g.y, tl.mi);
         if (t == 0) {
+          if (p.swiglu) {
+            if (ra + g < tl.rcnt) swiglu_store(p, tl.row0 + ra + g, v[0], v[1]);
+          } else {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int row = rbase + g + 8 * h;
-            if (row < tl.rcnt) y[tl.row0 + row] = v[h];
+            for (int h = 0; h < 2; ++h) {
+              const int row = (h ? rb : ra) + g;
+              if (row < tl.rcnt) y[tl.row0 + row] = v[h];
+            }
           }
         }
       } else if (!hand_over(v)) {
@@ -2915,7 +3290,7 @@ constexpr int stream_max_per_sm() {
   return WC == 8 ? 2 : 3;
 }
 
-template <int F, int NT, int RT, int WC, bool XBF>
+template <int F, int NT, int RT, int WC, int XM>
 Plan make_plan(int K, int ksplit, bool tma) {
   using G = Geo<F, NT, RT, WC>;
   const size_t stage = stage_shape<G>(tma).bytes;
@@ -2923,8 +3298,9 @@ Plan make_plan(int K, int ksplit, bool tma) {
   const int slabs_row = (K / 256 + G::kSlabSB - 1) / G::kSlabSB;
   if (slabs_row % ksplit != 0) return pl;
   const int kpad = slabs_row / ksplit * G::kSlabK;
-  const size_t xb = XLayout<F, NT, XBF>::bytes(static_cast<size_t>(NT) * kpad) +
-                    static_cast<size_t>(NT) * (kpad / G::kPart) * 4;
+  const size_t xb = XM == kXQ8 ? static_cast<size_t>(q8_x_bytes(NT, kpad, G::kPart))
+                               : XLayout<F, NT, XM == kXBF16>::bytes(static_cast<size_t>(NT) * kpad) +
+                                     static_cast<size_t>(NT) * (kpad / G::kPart) * 4;
   pl.x_bytes = static_cast<uint32_t>((xb + 127) & ~size_t{127});
   const DevInfo* dip = dev_info();
   if (dip == nullptr) return pl;
@@ -3008,7 +3384,7 @@ bool tma_possible(int K) {
   return true;
 }
 
-template <int F, int NT, int RT, int WC, bool XBF>
+template <int F, int NT, int RT, int WC, int XM>
 bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
                 int ksplit, bool tma, ScratchSrc src = ScratchSrc::kDevice,
                 StaticScratch* st = nullptr) {
@@ -3029,14 +3405,14 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   p.nt = n_tok;
   p.part = nullptr;
   p.arrivals = nullptr;
-  const Plan pl = make_plan<F, NT, RT, WC, XBF>(K, ksplit, tma);
+  const Plan pl = make_plan<F, NT, RT, WC, XM>(K, ksplit, tma);
   if (pl.per_sm == 0) return false;
   p.tma = tma ? 1 : 0;
   p.x_bytes = pl.x_bytes;
   int per_sm = pl.per_sm;
   {
     int occ = 0;   // registers may allow fewer CTAs than shared memory does
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_stream<F, NT, RT, WC, XBF>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_stream<F, NT, RT, WC, XM>,
                                                       G::kThreads, pl.smem) == cudaSuccess &&
         occ >= 1 && occ < per_sm)
       per_sm = occ;
@@ -3080,7 +3456,7 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   if (ksplit > kMaxSegs) return false;
   const size_t smem = p.x_bytes + static_cast<size_t>(stages) * ss.bytes;
   static size_t configured[kMaxDevices] = {};   // per device: dynamic smem above 48 KB is opt-in
-  if (!raise_smem_limit(gemv_stream<F, NT, RT, WC, XBF>, smem, configured)) return false;
+  if (!raise_smem_limit(gemv_stream<F, NT, RT, WC, XM>, smem, configured)) return false;
   p.tx = 0;
   if (tma) {
     for (int i = 0; i < g.count; ++i) {
@@ -3133,10 +3509,10 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return launched(cudaLaunchKernelEx(&cfg, gemv_stream<F, NT, RT, WC, XBF>, p, stages));
+  return launched(cudaLaunchKernelEx(&cfg, gemv_stream<F, NT, RT, WC, XM>, p, stages));
 }
 
-template <int F, int NT, int RT, int WC>
+template <int F, int NT, int RT, int WC, bool Q8 = false>
 bool launch_rt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
                ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
   using G = Geo<F, NT, RT, WC>;
@@ -3145,34 +3521,52 @@ bool launch_rt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStre
   // reach the most CTAs per SM.
   const int slabs_row = (K / 256 + G::kSlabSB - 1) / G::kSlabSB;
   const bool tma = tma_possible<G>(K);
-  int best_ks = 0, best_sm = 0;
-  bool best_bf = false;
-  // fp32 x first (no conversion in the consumers); bf16 x only where it
-  // admits more CTAs per SM than any fp32 plan (e.g. the LM head's per-row
-  // copies, whose stages with fp32 x leave room for two CTAs only)
   constexpr int kMaxPer = stream_max_per_sm<WC>();
-  for (int bf = 0; bf < 2 && best_sm < kMaxPer; ++bf) {
+  if constexpr (Q8) {
+    // int8 codes: one x mode
+    int best_ks = 0, best_sm = 0;
     for (int ks = 1; ks <= 16 && slabs_row % ks == 0; ks *= 2) {
-      const Plan pl = bf ? make_plan<F, NT, RT, WC, true>(K, ks, tma)
-                         : make_plan<F, NT, RT, WC, false>(K, ks, tma);
+      const Plan pl = make_plan<F, NT, RT, WC, kXQ8>(K, ks, tma);
       if (pl.per_sm > best_sm) {
         best_sm = pl.per_sm;
         best_ks = ks;
-        best_bf = bf != 0;
       }
       if (best_sm == kMaxPer) break;
     }
-  }
-  if (best_ks == 0) return false;
-  for (int ks = best_ks;; ks = 1) {
-    const bool ok = best_bf ? launch_cfg<F, NT, RT, WC, true>(g, x, K, n_tok, s, ks, tma, src, st)
-                            : launch_cfg<F, NT, RT, WC, false>(g, x, K, n_tok, s, ks, tma, src, st);
-    if (ok || ks == 1) return ok;   // no scratch (e.g. during capture, or beyond the fixed array): unsplit
-    best_bf = static_cast<size_t>(NT) * K * 4 > 96 * 1024;
+    if (best_ks == 0) return false;
+    for (int ks = best_ks;; ks = 1) {
+      const bool ok = launch_cfg<F, NT, RT, WC, kXQ8>(g, x, K, n_tok, s, ks, tma, src, st);
+      if (ok || ks == 1) return ok;
+    }
+  } else {
+    int best_ks = 0, best_sm = 0;
+    bool best_bf = false;
+    // fp32 x first (no conversion in the consumers); bf16 x only where it
+    // admits more CTAs per SM than any fp32 plan (e.g. the LM head's per-row
+    // copies, whose stages with fp32 x leave room for two CTAs only)
+    for (int bf = 0; bf < 2 && best_sm < kMaxPer; ++bf) {
+      for (int ks = 1; ks <= 16 && slabs_row % ks == 0; ks *= 2) {
+        const Plan pl = bf ? make_plan<F, NT, RT, WC, kXBF16>(K, ks, tma)
+                           : make_plan<F, NT, RT, WC, kXF32>(K, ks, tma);
+        if (pl.per_sm > best_sm) {
+          best_sm = pl.per_sm;
+          best_ks = ks;
+          best_bf = bf != 0;
+        }
+        if (best_sm == kMaxPer) break;
+      }
+    }
+    if (best_ks == 0) return false;
+    for (int ks = best_ks;; ks = 1) {
+      const bool ok = best_bf ? launch_cfg<F, NT, RT, WC, kXBF16>(g, x, K, n_tok, s, ks, tma, src, st)
+                              : launch_cfg<F, NT, RT, WC, kXF32>(g, x, K, n_tok, s, ks, tma, src, st);
+      if (ok || ks == 1) return ok;   // no scratch (e.g. during capture, or beyond the fixed array): unsplit
+      best_bf = static_cast<size_t>(NT) * K * 4 > 96 * 1024;
+    }
   }
 }
 
-template <int F, int NT>
+template <int F, int NT, bool Q8 = false>
 bool launch_nt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s,
                ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
   const DevInfo* dip = dev_info();
@@ -3185,13 +3579,13 @@ bool launch_nt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStre
   // (three CTAs per SM; measured faster than eight warps for its records).
   int64_t rows = 0;
   for (int i = 0; i < g.count; ++i) rows += g.N[i];
-  if (NT == 4 || rows < 16LL * di.sms) return launch_rt<F, NT, 2, 4>(g, x, K, n_tok, s, src, st);
+  if (NT == 4 || rows < 16LL * di.sms) return launch_rt<F, NT, 2, 4, Q8>(g, x, K, n_tok, s, src, st);
   if constexpr (NT == 4)
     return false;
   else if constexpr (F == kQ6K)
-    return launch_rt<F, NT, 4, 4>(g, x, K, n_tok, s, src, st);
+    return launch_rt<F, NT, 4, 4, Q8>(g, x, K, n_tok, s, src, st);
   else
-    return launch_rt<F, NT, 4, 8>(g, x, K, n_tok, s, src, st);
+    return launch_rt<F, NT, 4, 8, Q8>(g, x, K, n_tok, s, src, st);
 }
 
 // The verify kernel: tiles of 16 WC rows, slabs of two super-blocks; shared
@@ -3374,10 +3768,15 @@ bool launch_verify(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cuda
 constexpr int kTcUnits = 6;
 constexpr int kTcMinStages = 4;
 
+// h != nullptr: SwiGLU mode (g = {gate, up} of one shape; tiles of
+// kRows / 2 features; h = bf16(silu(gate) * up) written beside y).
 template <int F, int WC>
 bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
-                ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
+                ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr,
+                uint16_t* h = nullptr) {
   using G = TGeo<F, WC>;
+  const bool swiglu = h != nullptr;
+  if (swiglu && (g.count != 2 || g.N[0] != g.N[1])) return false;
   const DevInfo* dip = dev_info();
   if (dip == nullptr) return false;
   const DevInfo& di = *dip;
@@ -3400,9 +3799,14 @@ bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
   p.pbase = ss.pbase;
   p.stage = ss.bytes;
   p.tile_rows = G::kRows;
+  p.swiglu = swiglu ? 1 : 0;
+  p.h = h;
   p.tiles = 0;
   for (int i = 0; i < kMaxGroup; ++i) {
-    if (i < g.count) p.tiles += (g.N[i] + G::kRows - 1) / G::kRows;
+    if (swiglu)
+      p.tiles = (g.N[0] + G::kRows / 2 - 1) / (G::kRows / 2);   // one tile holds both matrices' rows
+    else if (i < g.count)
+      p.tiles += (g.N[i] + G::kRows - 1) / G::kRows;
     p.tile_end[i] = p.tiles;
   }
   size_t budget = di.smem_sm / per_sm > di.smem_reserved + kStaticSmem
@@ -3460,17 +3864,18 @@ bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
   if (!raise_smem_limit(gemv_tc1<F, WC>, smem, configured)) return false;
   p.tx = 0;
   if (tma) {
+    const uint32_t box_rows = swiglu ? G::kRows / 2 : G::kRows;
     for (int i = 0; i < g.count; ++i) {
       const int64_t n = g.N[i];
       bool ok;
       if constexpr (F == kG128) {
         ok = encode_plane(&p.tm[i][0], g.W[i], 128 * static_cast<uint64_t>(p.nsb), n, ss.slot,
-                          G::kRows) &&
+                          box_rows) &&
              encode_plane(&p.tm[i][1], g.W[i] + n * p.nsb * 128, 8 * static_cast<uint64_t>(p.nsb), n,
-                          ss.pslot, G::kRows);
+                          ss.pslot, box_rows);
       } else {
         ok = encode_plane(&p.tm[i][0], g.W[i], static_cast<uint64_t>(p.nsb) * G::kBB, n, ss.slot,
-                          G::kRows);
+                          box_rows);
       }
       if (!ok) return false;
     }
@@ -3736,11 +4141,20 @@ void* noalloc_scratch_address() {
   return addr[d];
 }
 
-// The tensor cores serve every width from two tokens on: the cost of those
-// kernels is set by building the A operand from the packed weights, once per
-// weight whatever the token count, while the CUDA-core kernel spends a
-// multiply-add per weight and token.
-constexpr int kTensorCoreMinTokens = 2;
+// The narrowest width the tensor cores serve.  Their cost is set by building
+// the A operand from the packed weights, once per weight whatever the token
+// count, while the CUDA-core kernel spends a multiply-add per weight and
+// token: from three tokens on the tensor cores win everywhere (by about 2x
+// in every launch of the decode step and of the Q5_K layer).  At two tokens
+// the CUDA-core kernel still wins where the integer work of building A is
+// largest: Q6_K (down 56.6 against 64.5 us, the LM head 369 against 495 us)
+// and Q5_K on long rows (down, K = 32768: 52.9 against 57.3 us); Q4_K,
+// Q4_G128 and short Q5_K rows are faster on the tensor cores.
+int tensor_core_min_tokens(int fmt, int K) {
+  if (fmt == kQ6K) return 3;
+  if (fmt == kQ5K && K >= 16384) return 3;
+  return 2;
+}
 }  // namespace
 
 // The kernel choice for one request (see kq_kernels.cuh).  `noalloc`: split-K
@@ -3762,7 +4176,7 @@ StreamResult launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K
     return ok ? StreamResult::kLaunched
               : (sst.too_large ? StreamResult::kTooLarge : StreamResult::kNotServed);
   };
-  if (n_tok >= kTensorCoreMinTokens) {
+  if (n_tok >= tensor_core_min_tokens(fmt, K)) {
     // verify widths: the multi-token tensor-core kernels
     if (tcv_eligible(fmt, g, K, n_tok)) {
       const bool ok = fmt == kQ4K ? launch_tcv_fmt<kQ4K>(g, x, K, n_tok, s, src, st)
@@ -3818,6 +4232,91 @@ StreamResult launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K
     }
   }
   return StreamResult::kLaunched;
+}
+
+StreamResult launch_q8(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
+                       cudaStream_t s) {
+  if (n_tok < 1 || n_tok > 16 || fmt < kQ4K || fmt > kG128) return StreamResult::kNotServed;
+  // up to four tokens per launch (x and y rows of a token are contiguous, so
+  // a chunk is an offset view)
+  for (int t0 = 0; t0 < n_tok; t0 += 4) {
+    const int nt = n_tok - t0 < 4 ? n_tok - t0 : 4;
+    const int w = nt <= 1 ? 1 : (nt <= 2 ? 2 : 4);
+    GemvGroup gc = g;
+    for (int i = 0; i < g.count; ++i) gc.y[i] = g.y[i] + static_cast<int64_t>(t0) * g.N[i];
+    const uint16_t* xc = x + static_cast<int64_t>(t0) * K;
+    bool ok = false;
+#define KQ_CASE(F)                                                              \
+  case F:                                                                       \
+    ok = w == 1 ? launch_nt<F, 1, true>(gc, xc, K, nt, s)                       \
+                : w == 2 ? launch_nt<F, 2, true>(gc, xc, K, nt, s)              \
+                         : launch_nt<F, 4, true>(gc, xc, K, nt, s);             \
+    break;
+    switch (fmt) {
+      KQ_CASE(kQ4K)
+      KQ_CASE(kQ5K)
+      KQ_CASE(kQ6K)
+      KQ_CASE(kG128)
+    }
+#undef KQ_CASE
+    if (!ok) return t0 == 0 ? StreamResult::kNotServed : StreamResult::kFailed;
+  }
+  return StreamResult::kLaunched;
+}
+
+namespace {
+// The int8 codes of the dp4a path on their own: one warp per 32-position
+// block, lane i quantising position i with the kernel's own steps.
+__global__ void __launch_bounds__(256) quantize_x_q8_kernel(const uint16_t* __restrict__ x,
+                                                            int64_t blocks, int8_t* __restrict__ xq,
+                                                            float* __restrict__ dx) {
+  const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (b >= blocks) return;   // warp-uniform
+  const float v = __uint_as_float(static_cast<uint32_t>(x[32 * b + lane]) << 16);
+  float amax = fabsf(v);
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
+  const float d = __fdiv_rn(amax, 127.0f);
+  xq[32 * b + lane] = static_cast<int8_t>(q8_code(v, d));
+  if (lane == 0) dx[b] = d;
+}
+}  // namespace
+
+bool launch_quantize_x_q8(const uint16_t* x, int64_t n, int8_t* xq, float* dx, cudaStream_t s) {
+  const int64_t blocks = n / 32;
+  quantize_x_q8_kernel<<<static_cast<unsigned>((blocks * 32 + 255) / 256), 256, 0, s>>>(x, blocks, xq, dx);
+  return launched(cudaGetLastError());
+}
+
+StreamResult launch_swiglu(int fmt, const GemvGroup& g, const uint16_t* x, int K, int n_tok,
+                           uint16_t* h, cudaStream_t s) {
+  if (g.count != 2 || g.N[0] != g.N[1]) return StreamResult::kNotServed;
+  // one token on a large Q4_K / Q4_G128 pair: fused in the single-token
+  // tensor-core kernel
+  if (n_tok == 1 && tc1_eligible(fmt, g, K, n_tok)) {
+    const bool ok =
+        fmt == kQ4K ? launch_tc1<kQ4K, 16>(g, x, K, s, ScratchSrc::kDevice, nullptr, h)
+                    : launch_tc1<kG128, 16>(g, x, K, s, ScratchSrc::kDevice, nullptr, h);
+    if (ok) return StreamResult::kLaunched;
+  }
+  // otherwise: the grouped GEMV, then the activation as its own kernel
+  const StreamResult r = launch_gemv(fmt, g, x, K, n_tok, s, false);
+  if (r != StreamResult::kLaunched) return r;
+  const int64_t n = static_cast<int64_t>(n_tok) * g.N[0];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((n + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return launched(cudaLaunchKernelEx(&cfg, swiglu_elementwise, static_cast<const float*>(g.y[0]),
+                                     static_cast<const float*>(g.y[1]), h, n))
+             ? StreamResult::kLaunched
+             : StreamResult::kFailed;
 }
 
 namespace {

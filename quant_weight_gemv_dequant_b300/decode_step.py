@@ -13,21 +13,31 @@ from __future__ import annotations
 
 import torch
 
-from . import (kq_gemv, kq_layer, kq_layer_io, kq_layer_step, make_matrix)
+from . import (kq_ffn_swiglu, kq_gemv, kq_gemv_multi, kq_layer, kq_layer_io, kq_layer_step,
+               make_matrix)
 
 LAYER_NAMES = ("q", "k", "v", "o", "gate", "up", "down")
-X_OF = {"q": "x_attn", "k": "x_attn", "v": "x_attn", "o": "x_o",
+# the matrices that read the pre-attention hidden state (the attention's
+# sigmoid output gate is optional: the pages' own layer has it)
+ATTN_NAMES = ("q", "k", "v", "attn_gate")
+X_OF = {"q": "x_attn", "k": "x_attn", "v": "x_attn", "attn_gate": "x_attn", "o": "x_o",
         "gate": "x_ffn", "up": "x_ffn", "down": "x_down"}
 
 
 class DecodeStep:
     """layers: list of {name: (fmt, W_device_uint8, N_out, K)} for the seven
-    projections; lm_head: (fmt, W, N_out, K) or None."""
+    projections; lm_head: (fmt, W, N_out, K) or None.
 
-    def __init__(self, layers, lm_head, n_tok: int, device="cuda"):
+    fused_ffn: the feed-forward block of every layer runs as kq_ffn_swiglu --
+    the gate/up launch writes h = bf16(silu(gate) * up) (``self.h[l]``) and
+    the down projection reads it -- instead of reading its own input
+    ``x_down``."""
+
+    def __init__(self, layers, lm_head, n_tok: int, device="cuda", fused_ffn=False):
         self.n_tok = n_tok
         self.layers = layers
         self.lm_head = lm_head
+        self.fused_ffn = fused_ffn
         self.x, self.y = [], []
         self._structs = []
         # every activation input of the step is a view into one contiguous
@@ -44,36 +54,67 @@ class DecodeStep:
         for li, L in enumerate(layers):
             xs = dict(zip(("x_attn", "x_o", "x_ffn", "x_down"), views[4 * li:4 * li + 4]))
             ys = {n: torch.empty((n_tok, L[n][2]), dtype=torch.float32, device=device)
-                  for n in LAYER_NAMES}
+                  for n in L}
             layer = kq_layer(*[make_matrix(L[n][0], L[n][1], L[n][2], L[n][3]) for n in LAYER_NAMES])
             io = kq_layer_io(*[xs[k].data_ptr() for k in ("x_attn", "x_o", "x_ffn", "x_down")],
                              *[ys[n].data_ptr() for n in LAYER_NAMES])
             self.x.append(xs)
             self.y.append(ys)
             self._structs.append((layer, io))
+        self.h = [torch.empty((n_tok, L["gate"][2]), dtype=torch.bfloat16, device=device)
+                  for L in layers] if fused_ffn else []
         if lm_head is not None:
             self.x_head = views[-1]
             self.y_head = torch.empty((n_tok, lm_head[2]), dtype=torch.float32, device=device)
         self.graph = None
 
     def weight_bytes(self) -> int:
-        total = sum(L[n][1].numel() for L in self.layers for n in LAYER_NAMES)
+        total = sum(L[n][1].numel() for L in self.layers for n in L)
         if self.lm_head is not None:
             total += self.lm_head[1].numel()
         return total
 
     def launches(self) -> int:
-        """Kernel launches per step (one per format-group of a layer step)."""
+        """Kernel launches per step (one per format-group of a layer step;
+        fused_ffn: plus the activation kernel where the gate/up launch does
+        not fuse it, i.e. unless one token on Q4_K / Q4_G128 pairs of at
+        least 2^25 weights)."""
         per_layer = 0
         for L in self.layers[:1]:
-            for group in (("q", "k", "v"), ("o",), ("gate", "up"), ("down",)):
-                per_layer += len({L[n][0] for n in group})
+            for group in (ATTN_NAMES, ("o",), ("gate", "up"), ("down",)):
+                per_layer += len({L[n][0] for n in group if n in L})
+            if self.fused_ffn:
+                f, _, N, K = L["gate"]
+                if not (self.n_tok == 1 and f in (0, 3) and 2 * N * K >= (1 << 25)):
+                    per_layer += 1
         return per_layer * len(self.layers) + (1 if self.lm_head is not None else 0)
 
     def run(self, stream=None):
         s = stream if stream is not None else torch.cuda.current_stream()
-        for layer, io in self._structs:
-            kq_layer_step(layer, io, self.n_tok, s)
+        for li, (layer, io) in enumerate(self._structs):
+            L, xs, ys = self.layers[li], self.x[li], self.y[li]
+            if not self.fused_ffn and "attn_gate" not in L:
+                kq_layer_step(layer, io, self.n_tok, s)
+                continue
+            # q, k, v (and the attention's output gate, which reads the same
+            # hidden state) in one launch per format; o
+            q, o = L["q"], L["o"]
+            groups = {}
+            for n in ATTN_NAMES:
+                if n in L:
+                    groups.setdefault(L[n][0], []).append(n)
+            for f, names in groups.items():
+                kq_gemv_multi(f, [L[n][1] for n in names], [ys[n] for n in names],
+                              [L[n][2] for n in names], xs["x_attn"], q[3], self.n_tok, s)
+            kq_gemv(o[0], o[1], xs["x_o"], ys["o"], o[2], o[3], self.n_tok, s)
+            if self.fused_ffn:
+                kq_ffn_swiglu(layer.gate, layer.up, layer.down, xs["x_ffn"], ys["gate"], ys["up"],
+                              self.h[li], ys["down"], self.n_tok, s)
+            else:
+                gt, up, dn = L["gate"], L["up"], L["down"]
+                kq_gemv_multi(gt[0], [gt[1], up[1]], [ys["gate"], ys["up"]], [gt[2], up[2]],
+                              xs["x_ffn"], gt[3], self.n_tok, s)
+                kq_gemv(dn[0], dn[1], xs["x_down"], ys["down"], dn[2], dn[3], self.n_tok, s)
         if self.lm_head is not None:
             f, W, N, K = self.lm_head
             kq_gemv(f, W, self.x_head, self.y_head, N, K, self.n_tok, s)

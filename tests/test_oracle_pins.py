@@ -457,3 +457,16 @@ def test_pages_parameter_count():
     per_layer = sum(m.N * m.K for m in L) + q_width * int(p["hidden"])   # + attention gate
     total = int(p["layers"]) * per_layer + 2 * int(p["vocab"]) * int(p["hidden"])
     assert abs(total / 1e9 - p["text_params_b"]) / p["text_params_b"] < 1e-4
+
+
+def test_pages_shape_workload_is_the_cards_model():
+    # the second workload (the card's own shapes, q/k/v and the attention
+    # gate in one launch) has exactly the card's text-tower parameters
+    p = _pages()
+    assert (wl.GLIMMER_HIDDEN, wl.GLIMMER_INTER, wl.GLIMMER_VOCAB) == \
+        (int(p["hidden"]), int(p["intermediate"]), int(p["vocab"]))
+    per_layer = sum(m.N * m.K for m in wl.GLIMMER_LAYER)
+    total = int(p["layers"]) * per_layer + 2 * wl.GLIMMER_HEAD.N * wl.GLIMMER_HEAD.K   # + embedding
+    assert abs(total / 1e9 - p["text_params_b"]) / p["text_params_b"] < 1e-4
+    assert [m.name for m in wl.GLIMMER_LAYER[:4]] == ["q", "k", "v", "attn_gate"]
+    assert all(m.K == wl.GLIMMER_HIDDEN for m in wl.GLIMMER_LAYER[:4])

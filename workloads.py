@@ -20,7 +20,8 @@ Workload shapes.  The pages (Muse-Glimmer-30B: 52 layers, GQA 32 q / 2 kv
 heads of dim 128, SwiGLU; Core AI card architecture section and SGLang day-0
 post) fix the layer structure; the hidden size 5120 and intermediate size
 32768 used for the benchmark shapes are assumptions, with the Core AI card's
-6656 / 19968 / vocab 202048 kept as a second shape set (``glimmer_card``).
+6656 / 19968 / vocab 202048 kept as a second shape set (``GLIMMER_LAYER``,
+with the attention's sigmoid gate as a fourth matrix of the q/k/v launch).
 
 Large workloads (the FFN layer, the Q5_K layer sweep and the whole decode
 step) are tiled from a pool of quantised super-blocks: super-block i of a
@@ -200,6 +201,28 @@ FFN_Q4K_Q6K = layer_matrices(Q4_K, Q4_K, Q6_K)[4:]
 LAYER_Q5K = layer_matrices(Q5_K, Q5_K, Q5_K)
 DECODE_LAYER = layer_matrices(Q4_K, Q4_K, Q6_K)
 LM_HEAD = Matrix("lm_head", Q6_K, VOCAB, HIDDEN)
+
+
+# The pages' own shapes (Core AI card, "The architecture, and what the port
+# had to do about it"): hidden 6656, SwiGLU intermediate 19968, vocab 202048,
+# 32 q / 2 kv heads of 128, and a sigmoid output gate of the attention read
+# from the pre-attention hidden state, which the card folds with q, k and v
+# into one qkvg projection (one launch of four matrices here).
+GLIMMER_HIDDEN, GLIMMER_INTER, GLIMMER_VOCAB = 6656, 19968, 202048
+
+
+def glimmer_layer(fmt_attn: int = Q4_K, fmt_ffn: int = Q4_K, fmt_down: int = Q6_K):
+    L = layer_matrices(fmt_attn, fmt_ffn, fmt_down, hidden=GLIMMER_HIDDEN, inter=GLIMMER_INTER)
+    q = L[0]
+    return L[:3] + [Matrix("attn_gate", fmt_attn, q.N, q.K)] + L[3:]
+
+
+GLIMMER_LAYER = glimmer_layer()
+GLIMMER_HEAD = Matrix("lm_head", Q6_K, GLIMMER_VOCAB, GLIMMER_HIDDEN)
+
+
+def glimmer_step_bytes(layers: int = LAYERS) -> int:
+    return layers * sum(m.nbytes for m in GLIMMER_LAYER) + GLIMMER_HEAD.nbytes
 
 
 def decode_step_bytes(layers: int = LAYERS) -> int:
