@@ -335,6 +335,35 @@ kq_status kq_device_status(kq_stream_t stream);
  * Source: none in the pages; tests this library's failure detection. */
 kq_status kq_test_wait_timeout(unsigned int wait_us, kq_stream_t stream);
 
+/* One tensor of a GGUF checkpoint (kq_gguf_index). */
+typedef struct {
+  char name[128];         /* tensor name (truncated to 127 bytes), 0-terminated */
+  int32_t ggml_type;      /* the file's tensor type (12 Q4_K, 13 Q5_K, 14 Q6_K, ...) */
+  int32_t format;         /* the kq_format of that type, or -1 if the library has none */
+  int32_t n_dims;
+  int64_t dims[4];        /* dims[0] = row length; unused dims are 1 */
+  int64_t N_out, K;       /* K-quant tensors: rows, row length (dims[0]) */
+  uint64_t data_offset;   /* byte offset of the tensor's data in the file */
+  uint64_t bytes;         /* K-quant tensors: kq_matrix_bytes(format, N_out, K) */
+} kq_gguf_tensor;
+
+/* Index of a GGUF checkpoint held in host memory (file, size bytes): the
+ * first min(max_tensors, count) tensors into out[], the tensor count into
+ * *n_tensors, the data alignment into *alignment (may be NULL).  For a
+ * Q4_K / Q5_K / Q6_K tensor, the `bytes` bytes at file + data_offset are
+ * the N_out x K matrix in the layout above, ready for kq_gemv once copied
+ * to the device (they are 16-B aligned on the device if the copy is).
+ * Host only; nothing is allocated.  Every read is checked against `size`:
+ * a truncated or malformed file returns KQ_ERR_ARG (KQ_ERR_UNSUPPORTED for
+ * a version other than 2 or 3, KQ_ERR_SHAPE for a K-quant tensor whose row
+ * length is not a multiple of 256).
+ * Source: the daily.dev summary (answer on exporting GGUF checkpoints) and
+ * the SGLang day-0 post (GGUF paragraph) name GGUF checkpoints as the input;
+ * the container is read as the public GGUF description lays it out
+ * (header, typed key/value metadata, tensor infos, aligned data section). */
+kq_status kq_gguf_index(const void* file, size_t size, kq_gguf_tensor* out, int max_tensors,
+                        int* n_tensors, uint32_t* alignment);
+
 /* Static string for a status code.
  * Source: none in the pages. */
 const char* kq_status_str(kq_status s);

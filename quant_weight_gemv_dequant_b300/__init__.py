@@ -39,6 +39,13 @@ class kq_matrix(ctypes.Structure):
                 ("N_out", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
+class kq_gguf_tensor(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 128), ("ggml_type", ctypes.c_int32),
+                ("format", ctypes.c_int32), ("n_dims", ctypes.c_int32),
+                ("dims", ctypes.c_int64 * 4), ("N_out", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("data_offset", ctypes.c_uint64), ("bytes", ctypes.c_uint64)]
+
+
 class kq_layer(ctypes.Structure):
     _fields_ = [(n, kq_matrix) for n in ("q", "k", "v", "o", "gate", "up", "down")]
 
@@ -68,6 +75,9 @@ def lib() -> ctypes.CDLL:
         L.kq_layer_step.argtypes = [ctypes.POINTER(kq_layer), ctypes.POINTER(kq_layer_io), I, P]
         L.kq_gemv_swiglu.argtypes = [I, P, P, P, P, P, P, I64, I64, I, P]
         L.kq_gemv_q8.argtypes = [I, P, P, P, I64, I64, I, P]
+        L.kq_gguf_index.argtypes = [P, ctypes.c_size_t, ctypes.POINTER(kq_gguf_tensor), I,
+                                    ctypes.POINTER(I), ctypes.POINTER(ctypes.c_uint32)]
+        L.kq_gguf_index.restype = I
         L.kq_quantize_x_q8.argtypes = [P, I64, I, P, P, P]
         L.kq_ffn_swiglu.argtypes = [ctypes.POINTER(kq_matrix)] * 3 + [P, P, P, P, P, I, P]
         L.kq_dequantize.argtypes = [I, P, P, I64, I64, P]
@@ -207,6 +217,21 @@ def kq_quantize(fmt: int, W_host: np.ndarray, N_out: int, K: int) -> np.ndarray:
     out = np.zeros(max(1, kq_matrix_bytes(fmt, N_out, K)), dtype=np.uint8)
     _check(lib().kq_quantize(fmt, W.ctypes.data, N_out, K, out.ctypes.data), "kq_quantize")
     return out
+
+
+def kq_gguf_index(data, max_tensors: int = 4096):
+    """Index a GGUF checkpoint held in host memory (bytes or a uint8 array):
+    (status, [kq_gguf_tensor], alignment)."""
+    buf = np.frombuffer(data, dtype=np.uint8) if isinstance(data, (bytes, bytearray)) else \
+        np.ascontiguousarray(data, dtype=np.uint8)
+    out = (kq_gguf_tensor * max_tensors)()
+    n = ctypes.c_int(0)
+    al = ctypes.c_uint32(0)
+    st = lib().kq_gguf_index(buf.ctypes.data, buf.size, out, max_tensors, ctypes.byref(n),
+                             ctypes.byref(al))
+    if st != KQ_OK:
+        return st, [], 0
+    return st, [out[i] for i in range(min(n.value, max_tensors))], al.value
 
 
 def kq_merge_g128(q4k_host: np.ndarray, N_out: int, K: int):
