@@ -53,6 +53,9 @@ def parse():
     p.add_argument("--no-extra", action="store_true", help="skip the n_tok=8 line and e2e")
     p.add_argument("--case", default="step", choices=["step"] + sorted(CASES),
                    help="one launch of the decode step instead of the whole step (for profiling)")
+    p.add_argument("--path", default="bf16", choices=["bf16", "q8"],
+                   help="--case: the bf16-activation kernels, or the int8-activation dp4a "
+                        "kernel (one launch per matrix)")
     return p.parse_args()
 
 
@@ -744,7 +747,11 @@ def run_case(args):
     stream = torch.cuda.current_stream(device)
 
     def launch():
-        kq.kq_gemv_multi(fmt, Ws, ys, Ns, x, K, T)
+        if args.path == "q8":
+            for W, y, N in zip(Ws, ys, Ns):
+                kq.kq_gemv_q8(fmt, W, x, y, N, K, T)
+        else:
+            kq.kq_gemv_multi(fmt, Ws, ys, Ns, x, K, T)
 
     for _ in range(max(3, args.warmup)):
         launch()
@@ -757,7 +764,8 @@ def run_case(args):
     torch.cuda.synchronize()
     t = e0.elapsed_time(e1) / 1e3 / args.steps
     nbytes = sum(m.nbytes for m in mats)
-    print(json.dumps({"case": args.case, "matrices": [f"{m.name} {m.N}x{m.K} fmt {m.fmt}" for m in mats],
+    print(json.dumps({"case": args.case, "path": args.path,
+                      "matrices": [f"{m.name} {m.N}x{m.K} fmt {m.fmt}" for m in mats],
                       "n_tok": T, "launches": args.steps, "us_per_launch": t * 1e6,
                       "weight_gb_s": nbytes / t / 1e9,
                       "l2": "weights resident in L2" if nbytes < 100e6 else "weights larger than L2",
