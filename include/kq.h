@@ -150,7 +150,7 @@ kq_status kq_gemv(kq_format f, const void* W_blocks, const void* x_bf16,
  * that cannot afford an allocation's implicit device synchronisation.
  * kq_gemv may allocate a split-K scratch buffer on its first long-row call;
  * this variant never allocates (no cudaMalloc, cudaFree or allocating
- * library call on any path) and keeps that scratch in a fixed 2 MiB array
+ * library call on any path) and keeps that scratch in a fixed 4 MiB array
  * compiled into the library, which every GPU that loads the library holds
  * until the process exits.
  *   Same arguments, requirements and result as kq_gemv (within the same
@@ -159,9 +159,9 @@ kq_status kq_gemv(kq_format f, const void* W_blocks, const void* x_bf16,
  *   fewer K segments, or the next kernel kq_gemv would try, runs instead.
  *   Limits: a request that the streaming and tensor-core kernels can serve
  *   only with more than 16384 row tiles or more partial sums than fit in
- *   2 MiB - 64 KiB (roughly N_out * n_tok * K-segments > 500000, e.g. rows
- *   of 32768 weights at 4 tokens and 200000 outputs) returns
- *   KQ_ERR_TOO_LARGE and launches nothing.
+ *   4 MiB - 64 KiB at 8 bytes each (roughly N_out * n_tok * K-segments >
+ *   500000, e.g. rows of 32768 weights at 4 tokens and 200000 outputs)
+ *   returns KQ_ERR_TOO_LARGE and launches nothing.
  *   Set-up: the first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current and caches it; make
  *   that first call before any stream capture.

@@ -155,7 +155,7 @@ def kq_gemv(fmt, W, x, y, N_out, K, n_tok, stream=None, check=True) -> int:
 
 
 def kq_gemv_noalloc(fmt, W, x, y, N_out, K, n_tok, stream=None, check=True) -> int:
-    """kq_gemv that never allocates device memory (fixed 2 MiB scratch);
+    """kq_gemv that never allocates device memory (fixed 4 MiB scratch);
     KQ_ERR_TOO_LARGE for requests beyond that array."""
     st = lib().kq_gemv_noalloc(fmt, _addr(W), _addr(x), _addr(y), N_out, K, n_tok,
                                _stream(stream))

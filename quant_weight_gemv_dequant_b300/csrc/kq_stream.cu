@@ -35,6 +35,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 #include <type_traits>
@@ -282,8 +283,10 @@ struct Params {
   int tile_rows;             // rows per tile (<= the CTA's 2 * WC * RT)
   int tile_end[kMaxGroup];   // cumulative tile counts per matrix
   uint32_t x_bytes;          // shared bytes of the staged x (+ part sums), 16-aligned
-  float* part;               // split-K partial sums [ksplit][tiles][tile_rows][NT]
+  void* part;                // split-K partial sums [ksplit][tiles][tile_rows][NT]: float,
+                             // or tagged 64-bit words (gemv_stream, put_partial)
   unsigned int* arrivals;    // split-K per-tile arrival counters (left at zero)
+  uint32_t tag;              // this launch's partial-sum tag (nonzero; gemv_stream)
   int static_tiles;          // tiles a CTA takes without claiming: cta + i * cps, i < this
   int tma;                   // 1: a stage arrives as one tensor copy per plane
   uint32_t slot, pslot, pbase, stage;   // StageShape of the ring
@@ -729,6 +732,69 @@ __device__ __forceinline__ void produce_rest(const Params& p, uint8_t* smem, uin
                    sl0 + r.xsl);
     r.advance(p.slabs, stages);
   }
+}
+
+// Split-K partial sums.  A partial sum travels in one 64-bit word with a
+// nonzero tag in its high half, written and read with relaxed device-scope
+// accesses: a reader that sees the tag sees the value, so no fence has to
+// order a value before a separate flag (a device-scope fence stalls for
+// microseconds while the SM has its ring of copies in flight).  The tile's
+// last segment to arrive (a relaxed counter) adds a value's segments in
+// segment order 0..ksplit-1, so the result does not depend on arrival order;
+// a partial not yet visible is waited for (bounded).  The reader clears
+// every slot it read, so all slots are zero between launches; the tag
+// changes from launch to launch (a graph replays its own), so slots left
+// behind by a launch that stopped early are not taken for this launch's.
+__device__ __forceinline__ void put_partial(uint64_t* slot, float v, uint32_t tag) {
+  const uint64_t w = (static_cast<uint64_t>(tag) << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(slot), "l"(w) : "memory");
+}
+__device__ __forceinline__ uint64_t load_partial(const uint64_t* slot) {
+  uint64_t w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(slot) : "memory");
+  return w;
+}
+__device__ __forceinline__ void clear_partial(uint64_t* slot) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(slot), "l"(uint64_t{0}) : "memory");
+}
+// The word at `slot` once it carries `tag` (bounded wait; a timeout is
+// counted and the value read last is returned).
+__device__ __noinline__ uint64_t wait_partial(const uint64_t* slot, uint32_t tag) {
+  const long long t0 = clock64();
+  for (;;) {
+    const uint64_t w = load_partial(slot);
+    if (static_cast<uint32_t>(w >> 32) == tag) return w;
+    if (clock64() - t0 > kWaitCycles) {
+      atomicAdd(&g_wait_timeouts, 1u);
+      return w;
+    }
+  }
+}
+__device__ __forceinline__ float partial_value(uint64_t w) {
+  return __uint_as_float(static_cast<uint32_t>(w));
+}
+// One value's partial sums (ksplit <= 16 segments, seg_stride slots apart)
+// added in segment order; every slot is cleared.  The loads of eight
+// segments are issued together rather than one L2 round trip after another.
+__device__ __forceinline__ float take_partials(uint64_t* part, int64_t seg_stride, int ksplit,
+                                               uint32_t tag) {
+  constexpr int kJ = 8;
+  float v = 0.0f;
+  for (int j0 = 0; j0 < ksplit; j0 += kJ) {
+    uint64_t w[kJ];
+#pragma unroll
+    for (int j = 0; j < kJ; ++j)
+      w[j] = j0 + j < ksplit ? load_partial(part + (j0 + j) * seg_stride) : 0;
+#pragma unroll
+    for (int j = 0; j < kJ; ++j)
+      if (j0 + j < ksplit) {
+        if (static_cast<uint32_t>(w[j] >> 32) != tag)
+          w[j] = wait_partial(part + (j0 + j) * seg_stride, tag);
+        v += partial_value(w[j]);
+      }
+  }
+  for (int j = 0; j < ksplit; ++j) clear_partial(part + j * seg_stride);
+  return v;
 }
 
 // The sum of a value's split-K partial sums (ksplit <= 16 segments, seg_stride
@@ -1535,7 +1601,6 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
     if (xsl == p.slabs - 1) {
-#pragma unroll
       float red[RT][NT];
 #pragma unroll
       for (int r = 0; r < RT; ++r)
@@ -1563,10 +1628,10 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
           }
         }
       } else {
-        // split-K: publish this segment's partial sums; the last CTA of the
-        // tile to arrive adds the segments in order 0..ksplit-1 (the result
-        // does not depend on arrival order) and re-arms the counter
-        float* part = p.part + static_cast<int64_t>(t) * p.tile_rows * NT;
+        // split-K: publish this segment's partial sums (tagged); the last
+        // CTA of the tile to arrive adds the segments in order
+        // 0..ksplit-1 and re-arms the counter
+        uint64_t* part = static_cast<uint64_t*>(p.part) + static_cast<int64_t>(t) * p.tile_rows * NT;
         const int64_t seg_stride = static_cast<int64_t>(p.tiles) * p.tile_rows * NT;
         if (ul == 0) {
 #pragma unroll
@@ -1574,24 +1639,21 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC == 8 ? 2 : 3)
             const int row = hw + 2 * WC * r;
             if (row < tl.rcnt) {
 #pragma unroll
-              for (int k = 0; k < NT; ++k) __stcg(part + kseg * seg_stride + row * NT + k, red[r][k]);
+              for (int k = 0; k < NT; ++k)
+                put_partial(part + kseg * seg_stride + row * NT + k, red[r][k], p.tag);
             }
           }
         }
-        // the consumer barrier orders every warp's stores before thread 0's
-        // fence, which makes them visible device-wide before its arrival
+        // one arrival per CTA, after every warp has published
         asm volatile("bar.sync 1, %0;" ::"r"(WC * 32) : "memory");
-        if (threadIdx.x == 0) {
-          __threadfence();
+        if (threadIdx.x == 0)
           last_flag = atomicAdd(p.arrivals + t, 1u) == static_cast<unsigned>(p.ksplit - 1);
-        }
         asm volatile("bar.sync 1, %0;" ::"r"(WC * 32) : "memory");
         if (last_flag) {
-          __threadfence();
           // every consumer thread takes (row, token) values of the tile
           for (int e = static_cast<int>(threadIdx.x); e < tl.rcnt * NT; e += WC * 32) {
             const int row = e / NT, k = e % NT;
-            const float v = sum_segments(part + e, seg_stride, p.ksplit);
+            const float v = take_partials(part + e, seg_stride, p.ksplit, p.tag);
             if (k < p.nt) y[static_cast<int64_t>(k) * N + tl.row0 + row] = v;
           }
           if (threadIdx.x == 0) p.arrivals[t] = 0u;
@@ -2050,7 +2112,7 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC <= 4 ? 2 : 1)
             }
           }
       } else {
-        float* part = p.part + static_cast<int64_t>(tix) * p.tile_rows * NTP;
+        float* part = static_cast<float*>(p.part) + static_cast<int64_t>(tix) * p.tile_rows * NTP;
         const int64_t seg_stride = static_cast<int64_t>(p.tiles) * p.tile_rows * NTP;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
@@ -2103,40 +2165,65 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC <= 4 ? 2 : 1)
 
 // ===================================================== single-token tensor-core kernel
 //
-// n_tok = 1 on large Q4_K / Q4_G128 matrices.  The products run on the tensor cores as
-// mma.sync m16n8k16 (bf16 operands, fp32 accumulation), and the eight
-// columns of the n8 operand carry eight SUB-BLOCKS of the one token instead
-// of eight tokens.  The k slots of an mma are assigned per lane: slots (2t,
-// 2t+1) of lane t (t = lane & 3) hold weights of sub-block lo(t), slots
-// (2t+8, 2t+9) weights of sub-block hi(t), and B holds x at those slots in
-// column lo(t) / hi(t) and zero in the other columns.  After the 16 mmas of
-// a super-block, D[row][n] is the dot product of sub-block n alone, the
-// quantity one scale multiplies:
+// n_tok = 1 on large Q4_K / Q4_G128 matrices.  The products run on the
+// tensor cores as mma.sync m16n8k16 (fp16 operands, fp32 accumulation), and
+// the eight columns of the n8 operand carry eight SUB-BLOCKS of the one token
+// instead of eight tokens.  The k slots of an mma are assigned per lane:
+// slots (2t, 2t+1) of lane t (t = lane & 3) hold weights of sub-block lo(t),
+// slots (2t+8, 2t+9) weights of sub-block hi(t), and B holds x at those
+// slots in column lo(t) / hi(t) and zero in the other columns.  After the 16
+// mmas of a super-block, D[row][n] is the dot product of sub-block n alone,
+// the quantity one scale multiplies:
 //   y_row += s1[n] D[row][n] + s2[n] Sx[n]
-// A = bf16(q), exact: one LOP3 per two weights builds bf16 (128 + q, 128 +
-// q) as (w & 0x000F000F) | 0x43004300 and one bf16 subtraction of (128, 128)
-// leaves (q, q), so no offset term remains in D (a record of zero weights
-// gives D = 0 whatever its scales); s1 = d sc, s2 = -dmin m, Sx[n] the sum of
-// x over sub-block n, staged once per launch.  Lane t takes chunk t of the
-// super-block (sub-block 2t: low nibbles -> slots 2t.., sub-block 2t+1: high
-// nibbles -> slots 2t+8..); word m of the chunk gives mma 2m (bytes 0, 2) and
-// 2m+1 (bytes 1, 3).  Per weight: half a LOP3, half a bf16 subtraction (on
-// the FMA pipe) plus the shifts that bring the next byte's nibbles down; per
-// sub-block and row: one scale pair.  (Q5_K and
-// Q6_K would need their fields assembled first, which costs more integer
+// A is exact (tc_sb_product: q or 16 q from (1024 + q) minus 1024 in fp16),
+// so no offset term remains in D (a record of zero weights gives D = 0
+// whatever its scales); x is staged in fp16 with a power-of-two scale per
+// sub-block (stage_x_tc_raw) that the column scale undoes; s1 = d sc, s2 =
+// -dmin m, Sx[n] the sum of x over sub-block n.  Lane t takes chunk t of the
+// super-block (sub-block 2t: low nibbles, sub-block 2t+1: high nibbles);
+// word m of the chunk gives mma 2m (bytes 0, 2) and 2m+1 (bytes 1, 3).  (Q5_K
+// and Q6_K would need their fields assembled first, which costs more integer
 // work than their CUDA-core path; they stay on gemv_stream.)
-// The column-n lane of each slot pair loads the x entries of sub-block n in
-// that order; the other lanes read a zero block.  Two accumulator chains
-// (bytes 0, 2 / bytes 1, 3) keep consecutive mmas independent.
 //
-// One CTA per SM: kWC consumer warps (a warp owns 16 rows of a 16 kWC-row
-// tile), a producer warp (the ring of one-super-block stages, tile claiming:
-// as in gemv_stream) and, when K is split, a reducer warp.  At the end of a
-// (tile, K segment) unit the consumers leave the unit's row sums in one of two
-// shared buffers and go on; the reducer warp publishes them to the split-K
-// scratch, counts the arrival and, for the last segment of the tile, adds the
-// segments in order 0..ksplit-1 and writes y.  So the device-wide fence and
-// atomic of the reduction never stall the consumers.
+// gemv_tc1 (TGeo1): one CTA per SM, 16 consumer warps and a producer warp.
+// A tile is 64 rows over ALL of K, so no partial sum ever leaves the CTA: a
+// stage is the tile's 64 rows x 4 super-blocks (one tensor copy per plane),
+// warp w takes rows 16 (w & 3) .. + 15 of the stage's super-block w >> 2,
+// and at the tile's end the four warps of a row group add their row sums in
+// shared memory, super-block column 0 to 3 (a fixed order).  Tiles are
+// claimed at run time (as in gemv_stream); x is staged once per CTA.
+// (Splitting K across CTAs instead needs a device-scope exchange of partial
+// sums whose latency ends up on the launch's critical path.)
+//
+// TGeo: the stage geometry of the multi-token kernel gemv_tcv (one-super-block
+// stages of 16 kWC RTW rows, a producer and a split-K reducer warp).
+
+template <int F>
+struct TGeo1 {
+  static constexpr int kF = F;
+  static constexpr int kWC = 16;
+  static constexpr int kThreads = (kWC + 1) * 32;   // + producer
+  static constexpr int kRowGroups = 4;              // 16-row mma tiles per tile
+  static constexpr int kRows = 16 * kRowGroups;
+  static constexpr int kSlabSB = kWC / kRowGroups;  // super-blocks per stage
+  static constexpr int kSlabK = 256 * kSlabSB;
+  static constexpr int kBB = block_bytes(F);
+  static constexpr int kSub = 32;   // weights per sub-block
+  static_assert(F == kQ4K || F == kG128, "Q4_K and Q4_G128 only");
+  static constexpr int kQBytes = (F == kG128) ? 128 * kSlabSB : kBB * kSlabSB;
+  static constexpr int kPBytes = (F == kG128) ? 8 * kSlabSB : 0;
+  static constexpr int round16(int b) { return (b + 15) / 16 * 16; }
+  // row pitch an odd multiple of 16 bytes: the 8 rows a warp reads at once
+  // start in 8 different 16-byte bank groups (the box reads 16 bytes of the
+  // next stage's records, or zeros past the row)
+  static constexpr int odd16(int b) { return (b / 16) % 2 ? b : b + 16; }
+  static constexpr int kSlotTma = odd16(round16(kQBytes + (kQBytes % 16 ? 15 : 0)));
+  static constexpr int kPSlotTma = (F == kG128) ? round16(kPBytes + (kPBytes % 16 ? 15 : 0)) : 0;
+  static constexpr int kSlotBulk = odd16(round16(kQBytes + 16));
+  static constexpr int kPSlotBulk = (F == kG128) ? round16(kPBytes + 16) : 0;
+  // the row-sum exchange at a tile's end: two buffers of [column][row] floats
+  static constexpr uint32_t kCombBytes = 2u * kSlabSB * kRows * 4u;
+};
 
 template <int F, int WC_, int RTW = 1>
 struct TGeo {
@@ -2167,13 +2254,18 @@ struct TGeo {
 // so that 32-bit entry i of a sub-block holds positions 4 (i >> 1) + (i & 1)
 // and that + 2), then Sx (the fp32 sum of x over every sub-block), then the
 // column scale of every sub-block (see stage_x_tc_raw), then 64 zero bytes,
-// then the reducer's two row-sum buffers of `rows` floats.
-__host__ __device__ constexpr uint32_t tc_x_only(int kpad, int sub) {
-  return (2u * static_cast<uint32_t>(kpad) + 8u * static_cast<uint32_t>(kpad / sub) + 64u + 15u) &
-         ~15u;
+// then the kernel's row-sum buffers.
+//
+// The zero block starts 32 bytes past a 128-byte boundary.  In a quarter-warp
+// of the product one lane reads its sub-block's x (at 0 or 64 modulo 128
+// bytes, plus the same 0..48 as the zero block's readers) and the other seven
+// read the zero block, so the two addresses always fall in different banks.
+__host__ __device__ constexpr uint32_t tc_zero_off(int kpad, int sub) {
+  return ((2u * static_cast<uint32_t>(kpad) + 8u * static_cast<uint32_t>(kpad / sub) + 127u) &
+          ~127u) + 32u;
 }
-__host__ __device__ constexpr uint32_t tc_x_bytes(int kpad, int sub, int rows) {
-  return (tc_x_only(kpad, sub) + 8u * static_cast<uint32_t>(rows) + 127u) & ~127u;
+__host__ __device__ constexpr uint32_t tc_x_only(int kpad, int sub) {
+  return (tc_zero_off(kpad, sub) + 64u + 15u) & ~15u;
 }
 
 // x of a K segment for the tensor-core product (fp16 operands), with the
@@ -2236,8 +2328,7 @@ __device__ void stage_x_tc_raw(const uint16_t* x, int K, int kpad, uint32_t xsh,
       asm volatile("st.shared.f32 [%0], %1;" ::"r"(xscl + 4u * sb), "f"(scale) : "memory");
     }
   }
-  if (threadIdx.x < 4)
-    sts128u(xscl + 4u * static_cast<uint32_t>(kpad / S) + 16u * threadIdx.x, make_uint4(0, 0, 0, 0));
+  if (threadIdx.x < 4) sts128u(xsh + tc_zero_off(kpad, S) + 16u * threadIdx.x, make_uint4(0, 0, 0, 0));
 }
 
 template <int S>
@@ -2331,43 +2422,6 @@ __device__ __forceinline__ void tc_scales_q4(const Params& p, const Tile& tl, in
   }
 }
 
-// One stage for this warp's 16 stage rows: lane (g, t) takes stage rows ra +
-// g and rb + g (the mma's rows g and g + 8): ra, rb = 16 w, 16 w + 8, or in
-// SwiGLU mode the gate row 8 w + g and the same feature's up row.
-template <class G>
-__device__ __forceinline__ void tc_stage_q4(const Params& p, const Tile& tl, int sl, int xsl,
-                                            uint32_t st, int ra, int rb, uint32_t xsh,
-                                            const ScaleSel& ss, float2 (&acc)[2]) {
-  constexpr int F = G::kF;
-  const int lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const uint32_t xsum = xsh + 2u * static_cast<uint32_t>(p.kpad);
-  const uint32_t xscl = xsum + 4u * static_cast<uint32_t>(p.kpad / 32);
-  const uint32_t zero = xscl + 4u * static_cast<uint32_t>(p.kpad / 32);
-  const bool act_lo = g == 2 * t, act_hi = g == 2 * t + 1;   // column g of the B operand
-#pragma unroll
-  for (int s = 0; s < G::kSlabSB; ++s) {
-    if (sl * G::kSlabSB + s >= p.nsb) break;
-    const int sbx = xsl * G::kSlabSB + s;   // super-block of the staged segment
-    const uint32_t xlo = act_lo ? xsh + 64u * (8 * sbx + 2 * t) : zero;
-    const uint32_t xhi = act_hi ? xsh + 64u * (8 * sbx + 2 * t + 1) : zero;
-    uint32_t qa[2];   // rows ra + g, rb + g: the chunk's qs bytes
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t rs = st + ((h ? rb : ra) + g) * p.slot;
-      qa[h] = (F == kG128) ? rs + 128 * s + 32 * t : rs + G::kBB * s + 16 + 32 * t;
-    }
-    float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    tc_sb_product(qa[0], qa[1], xlo, xhi, d);
-    float2 s1g, s2g, s1h, s2h;
-    tc_scales_q4<G>(p, tl, sl, st, ra + g, s, ss, t, s1g, s2g);
-    tc_scales_q4<G>(p, tl, sl, st, rb + g, s, ss, t, s1h, s2h);
-    const float2 sx = lds_f2(xsum + 4u * (8 * sbx + 2 * t));
-    const float2 cs = lds_f2(xscl + 4u * (8 * sbx + 2 * t));   // column scales
-    tc_epilogue(acc, d, __fmul2_rn(s1g, cs), s2g, __fmul2_rn(s1h, cs), s2h, sx);
-  }
-}
-
 // bf16(silu(g) * u), silu(v) = v / (1 + e^-v), evaluated in fp32 and
 // rounded to nearest (ties to even).
 __device__ __forceinline__ uint16_t swiglu_bf16(float gv, float uv) {
@@ -2409,7 +2463,7 @@ __device__ __forceinline__ void tc_reduce(const Params& p, uint32_t psum, uint32
     const Tile tl = tile_of(p, tix);
     // SwiGLU mode: all stage rows (gate rows, then up rows)
     const int n = p.swiglu ? p.tile_rows * NTP : tl.rcnt * NTP;
-    float* part = p.part + static_cast<int64_t>(tix) * p.tile_rows * NTP;
+    float* part = static_cast<float*>(p.part) + static_cast<int64_t>(tix) * p.tile_rows * NTP;
     const uint32_t buf = psum + 4u * static_cast<uint32_t>(b * p.tile_rows * NTP);
     for (int e = lane; e < n; e += 32) {
       float v;
@@ -2463,131 +2517,148 @@ __device__ __forceinline__ void tc_reduce(const Params& p, uint32_t psum, uint32
   }
 }
 
-template <int F, int WC>
-__global__ void __launch_bounds__((WC + 2) * 32, WC <= 8 ? 2 : 1)
+template <int F>
+__global__ void __launch_bounds__(TGeo1<F>::kThreads, 1)
     gemv_tc1(const __grid_constant__ Params p, int stages) {
-  using G = TGeo<F, WC>;
+  using G = TGeo1<F>;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 4];
+  __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 4 * G::kRowGroups];
   __shared__ int stage_tile[kMaxStages];
-  __shared__ int part_tile[2];
   const uint32_t bar_full = smem_addr(&bars[0]);
   const uint32_t bar_empty = smem_addr(&bars[kMaxStages]);
-  const uint32_t part_full = smem_addr(&bars[2 * kMaxStages]);    // [2]: consumers -> reducer
-  const uint32_t part_empty = smem_addr(&bars[2 * kMaxStages + 2]);   // [2]: reducer -> consumers
+  // per row group and buffer: the group's 4 warps wrote their row sums /
+  // the row sums were taken
+  const uint32_t comb_full = smem_addr(&bars[2 * kMaxStages]);
+  const uint32_t comb_empty = smem_addr(&bars[2 * kMaxStages + 2 * G::kRowGroups]);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t xsh = smem_addr(smem);
-  const uint32_t psum = xsh + tc_x_only(p.kpad, G::kSub);   // the two row-sum buffers
+  const uint32_t comb = xsh + tc_x_only(p.kpad, G::kSub);   // [2][kSlabSB][kRows] floats
   const uint32_t ring_a = xsh + p.x_bytes;
-  const int kseg = static_cast<int>(blockIdx.x) % p.ksplit;
-  const int cta = static_cast<int>(blockIdx.x) / p.ksplit;
-  const int cps = static_cast<int>(gridDim.x) / p.ksplit;
-  const int sl0 = kseg * p.slabs;
+  const int cta = static_cast<int>(blockIdx.x);
+  const int cps = static_cast<int>(gridDim.x);
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(bar_full + 8 * s, p.tma ? 1 : 32);
-      mbar_init(bar_empty + 8 * s, WC);
+      mbar_init(bar_empty + 8 * s, G::kWC);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(part_full + 8 * b, WC);
-      mbar_init(part_empty + 8 * b, 1);
+    for (int i = 0; i < 2 * G::kRowGroups; ++i) {
+      mbar_init(comb_full + 8 * i, G::kSlabSB);
+      mbar_init(comb_empty + 8 * i, 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  const bool producer = warp == WC, reducer = warp == WC + 1;
+  const bool producer = warp == G::kWC;
   asm volatile("griddepcontrol.launch_dependents;");
   Ring ring;
-  if (producer) produce_prefill<G>(p, smem, ring_a, bar_full, stage_tile, stages, cta, cps, sl0, ring);
+  if (producer) produce_prefill<G>(p, smem, ring_a, bar_full, stage_tile, stages, cta, cps, 0, ring);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  stage_x_tc<G::kSub>(p, xsh, kseg * p.kpad);
+  stage_x_tc<G::kSub>(p, xsh, 0);
   __syncthreads();
   if (producer) {
-    produce_rest<G>(p, smem, ring_a, bar_full, bar_empty, stage_tile, stages, cta, cps, kseg, sl0,
-                    ring);
-    return;
-  }
-  if (reducer) {
-    if (p.ksplit > 1) tc_reduce<1>(p, psum, part_full, part_empty, part_tile, kseg);
+    produce_rest<G>(p, smem, ring_a, bar_full, bar_empty, stage_tile, stages, cta, cps, 0, 0, ring);
     return;
   }
   const int g = lane >> 2, t = lane & 3;
-  // stage rows of this warp: ra + g and rb + g; in SwiGLU mode the gate and
-  // up rows of the tile's features 8 warp .. 8 warp + 7
-  const int half = p.tile_rows / 2;
-  const int ra = p.swiglu ? 8 * warp : 16 * warp;
-  const int rb = p.swiglu ? half + 8 * warp : 16 * warp + 8;
-  const int rfirst = p.swiglu ? 8 * warp : 16 * warp;   // this warp's first feature of the tile
+  const int rg = warp % G::kRowGroups;   // rows ra + g and rb + g of every stage
+  const int sc = warp / G::kRowGroups;   // super-block sc of every stage
+  const int ra = 16 * rg, rb = 16 * rg + 8;
   const ScaleSel ss = scale_sel(t);
+  const uint32_t xsum = xsh + 2u * static_cast<uint32_t>(p.kpad);
+  const uint32_t xscl = xsum + 4u * static_cast<uint32_t>(p.kpad / 32);
+  const uint32_t zero = xsh + tc_zero_off(p.kpad, 32);
+  const bool act_lo = g == 2 * t, act_hi = g == 2 * t + 1;   // column g of the B operand
   float2 acc[2];
   Tile tl{};
-  int tix = 0, unit = 0;
-  int xsl = 0, slot = 0;
+  int xsl = 0, slot = 0, ntile = 0;
   uint32_t parity = 0;
-  // hand unit `unit` (tile tix, or -1: no more) to the reducer through
-  // buffer unit & 1, once the reducer has drained that buffer's previous use
-  auto hand_over = [&](const float (&v)[2]) -> bool {
-    const int b = unit & 1;
-    if (unit >= 2 && !mbar_wait_warp(part_empty + 8 * b, static_cast<uint32_t>((unit >> 1) - 1) & 1u))
-      return false;
-    if (tix >= 0 && t == 0) {
-      const uint32_t buf = psum + 4u * static_cast<uint32_t>(b * p.tile_rows);
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        asm volatile("st.shared.f32 [%0], %1;" ::"r"(buf + 4u * ((h ? rb : ra) + g)), "f"(v[h])
-                     : "memory");
-    }
-    if (warp == 0 && lane == 0) part_tile[b] = tix;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(part_full + 8 * b);
-    ++unit;
-    return true;
-  };
   for (;;) {
-    const int sl = sl0 + xsl;
     if (!mbar_wait_warp(bar_full + 8 * slot, parity)) return;
     if (xsl == 0) {
-      tix = stage_tile[slot];
-      if (tix < 0) {
-        if (p.ksplit > 1) {
-          const float none[2] = {0.0f, 0.0f};
-          hand_over(none);
-        }
-        return;
-      }
+      const int tix = stage_tile[slot];
+      if (tix < 0) return;
       tl = tile_of(p, tix);
       acc[0] = acc[1] = make_float2(0.0f, 0.0f);
     }
     const uint32_t st = ring_a + slot * p.stage;
-    if (rfirst < tl.rcnt) tc_stage_q4<G>(p, tl, sl, xsl, st, ra, rb, xsh, ss, acc);
+    const int sbx = xsl * G::kSlabSB + sc;   // super-block of the row
+    if (sbx < p.nsb) {
+      const uint32_t xlo = act_lo ? xsh + 64u * (8 * sbx + 2 * t) : zero;
+      const uint32_t xhi = act_hi ? xsh + 64u * (8 * sbx + 2 * t + 1) : zero;
+      uint32_t qa[2];   // rows ra + g, rb + g: the chunk's qs bytes
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t rs = st + ((h ? rb : ra) + g) * p.slot;
+        qa[h] = (F == kG128) ? rs + 128 * sc + 32 * t : rs + G::kBB * sc + 16 + 32 * t;
+      }
+      float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      tc_sb_product(qa[0], qa[1], xlo, xhi, d);
+      float2 s1g, s2g, s1h, s2h;
+      tc_scales_q4<G>(p, tl, xsl, st, ra + g, sc, ss, t, s1g, s2g);
+      tc_scales_q4<G>(p, tl, xsl, st, rb + g, sc, ss, t, s1h, s2h);
+      const float2 sx = lds_f2(xsum + 4u * (8 * sbx + 2 * t));
+      const float2 cs = lds_f2(xscl + 4u * (8 * sbx + 2 * t));   // column scales
+      tc_epilogue(acc, d, __fmul2_rn(s1g, cs), s2g, __fmul2_rn(s1h, cs), s2h, sx);
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
     if (xsl == p.slabs - 1) {
-      // rows g, g+8: add the column pairs, then the four lanes of the row
-      float v[2];
+      // the tile's end: every warp leaves rows g, g+8 of its column in buffer
+      // b; one warp of the row group (rotating) adds the columns in order
+      // 0..3 and writes y.  In SwiGLU mode the up groups (2, 3) also take the
+      // gate sums of the same features from groups 0, 1 and write h.
+      const int b = ntile & 1;
+      const uint32_t k = static_cast<uint32_t>(ntile >> 1);
+      const uint32_t my_full = comb_full + 8u * (2 * rg + b);
+      const uint32_t my_empty = comb_empty + 8u * (2 * rg + b);
+      if (ntile >= 2 && !mbar_wait_warp(my_empty, (k - 1) & 1u)) return;
+      const uint32_t cb = comb + 4u * static_cast<uint32_t>(b * G::kSlabSB * G::kRows);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float a = acc[h].x + acc[h].y;
         a += __shfl_xor_sync(0xFFFFFFFFu, a, 1);
         a += __shfl_xor_sync(0xFFFFFFFFu, a, 2);
-        v[h] = a;
+        if (t == 0)
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(cb + 4u * (sc * G::kRows + (h ? rb : ra) + g)),
+                       "f"(a)
+                       : "memory");
       }
-      if (p.ksplit == 1) {
-        float* y = pick(p.g.y, tl.mi);
-        if (t == 0) {
-          if (p.swiglu) {
-            if (ra + g < tl.rcnt) swiglu_store(p, tl.row0 + ra + g, v[0], v[1]);
-          } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(my_full);
+      auto col_sum = [&](int row) {
+        float v = 0.0f;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int row = (h ? rb : ra) + g;
-              if (row < tl.rcnt) y[tl.row0 + row] = v[h];
-            }
-          }
+        for (int c = 0; c < G::kSlabSB; ++c) {
+          float u;
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(u) : "r"(cb + 4u * (c * G::kRows + row)));
+          v += u;
         }
-      } else if (!hand_over(v)) {
-        return;
+        return v;
+      };
+      const bool gate_group = p.swiglu && rg < G::kRowGroups / 2;
+      if (sc == (ntile & (G::kSlabSB - 1)) && !gate_group) {
+        if (!mbar_wait_warp(my_full, k & 1u)) return;
+        if (p.swiglu) {
+          // features f of this up group's rows: up row 32 + f, gate row f
+          const int gq = rg - G::kRowGroups / 2;
+          const uint32_t gate_full = comb_full + 8u * (2 * gq + b);
+          if (!mbar_wait_warp(gate_full, k & 1u)) return;
+          if (lane < 16) {
+            const int f = 16 * gq + lane;
+            if (f < tl.rcnt) swiglu_store(p, tl.row0 + f, col_sum(f), col_sum(G::kRows / 2 + f));
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(comb_empty + 8u * (2 * gq + b));
+        } else {
+          if (lane < 16) {
+            const int row = ra + lane;
+            if (row < tl.rcnt) pick(p.g.y, tl.mi)[tl.row0 + row] = col_sum(row);
+          }
+          __syncwarp();
+        }
+        if (lane == 0) mbar_arrive(my_empty);
       }
+      ++ntile;
     }
     if (++xsl == p.slabs) xsl = 0;
     if (++slot == stages) {
@@ -3040,7 +3111,7 @@ __device__ __forceinline__ void small_sb_q4(const SmallParams& p, uint32_t wreg,
   const int g = lane >> 2, t = lane & 3;
   const uint32_t xsum = xsh + 2u * static_cast<uint32_t>(p.K);
   const uint32_t xscl = xsum + 4u * static_cast<uint32_t>(p.K / 32);
-  const uint32_t zero = xscl + 4u * static_cast<uint32_t>(p.K / 32);
+  const uint32_t zero = xsh + tc_zero_off(p.K, 32);
   const bool act_lo = g == 2 * t, act_hi = g == 2 * t + 1;   // column g of the B operand
   const uint32_t xlo = act_lo ? xsh + 64u * (8 * sbx + 2 * t) : zero;
   const uint32_t xhi = act_hi ? xsh + 64u * (8 * sbx + 2 * t + 1) : zero;
@@ -3230,6 +3301,14 @@ bool launched(cudaError_t e) {
 
 constexpr size_t kStaticSmem = 256;   // the kernel's static shared memory (barriers, flag), rounded up
 
+// A nonzero tag per launch for the split-K partial sums (put_partial).
+uint32_t next_tag() {
+  static std::atomic<uint32_t> seq{0};
+  uint32_t t = 0;
+  while (t == 0) t = seq.fetch_add(1u, std::memory_order_relaxed) + 1u;
+  return t;
+}
+
 // Split-K scratch of the current device: a fixed region of kMaxTiles arrival
 // counters, then the partial sums.  The counter region never moves within a
 // buffer, so counters stay zero across launches of any shape (partial sums of
@@ -3332,7 +3411,7 @@ struct StaticScratch {
 };
 constexpr int kNoAllocMaxTiles = 1 << 14;
 constexpr size_t kNoAllocCounterBytes = size_t{kNoAllocMaxTiles} * sizeof(unsigned int);
-constexpr size_t kNoAllocScratchBytes = size_t{2} << 20;   // 2 MiB per device
+constexpr size_t kNoAllocScratchBytes = size_t{4} << 20;   // 4 MiB per device
 
 // cuTensorMapEncodeTiled, fetched from the driver once (nullptr if absent).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -3405,6 +3484,7 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   p.nt = n_tok;
   p.part = nullptr;
   p.arrivals = nullptr;
+  p.tag = next_tag();
   const Plan pl = make_plan<F, NT, RT, WC, XM>(K, ksplit, tma);
   if (pl.per_sm == 0) return false;
   p.tma = tma ? 1 : 0;
@@ -3475,13 +3555,13 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   }
   if (ksplit > 1) {
     const size_t part_bytes =
-        static_cast<size_t>(ksplit) * p.tiles * p.tile_rows * NT * sizeof(float);
+        static_cast<size_t>(ksplit) * p.tiles * p.tile_rows * NT * sizeof(uint64_t);
     if (src == ScratchSrc::kDevice) {
       if (p.tiles > kMaxTiles) return false;
       uint8_t* base = static_cast<uint8_t*>(scratch_get(kCounterBytes + part_bytes, s));
       if (base == nullptr) return false;
       p.arrivals = reinterpret_cast<unsigned int*>(base);
-      p.part = reinterpret_cast<float*>(base + kCounterBytes);
+      p.part = base + kCounterBytes;
     } else {
       if (p.tiles > kNoAllocMaxTiles ||
           kNoAllocCounterBytes + part_bytes > kNoAllocScratchBytes) {
@@ -3496,7 +3576,7 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
         return false;
       }
       p.arrivals = reinterpret_cast<unsigned int*>(st->base);
-      p.part = reinterpret_cast<float*>(st->base + kNoAllocCounterBytes);
+      p.part = st->base + kNoAllocCounterBytes;
     }
   }
   cudaLaunchConfig_t cfg = {};
@@ -3611,6 +3691,7 @@ bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   p.nt = n_tok;
   p.part = nullptr;
   p.arrivals = nullptr;
+  p.tag = 0;
   p.tma = tma ? 1 : 0;
   p.static_tiles = 0;   // the verify kernel keeps its fixed tile order
   p.slot = full.slot;
@@ -3693,7 +3774,7 @@ bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
                             : nullptr;
         if (base == nullptr) continue;   // no scratch (e.g. during capture): fewer segments
         p.arrivals = reinterpret_cast<unsigned int*>(base);
-        p.part = reinterpret_cast<float*>(base + kCounterBytes);
+        p.part = base + kCounterBytes;
       } else {
         if (p.tiles > kNoAllocMaxTiles ||
             kNoAllocCounterBytes + part_bytes > kNoAllocScratchBytes) {
@@ -3706,7 +3787,7 @@ bool launch_mma(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
           return false;
         }
         p.arrivals = reinterpret_cast<unsigned int*>(st->base);
-        p.part = reinterpret_cast<float*>(st->base + kNoAllocCounterBytes);
+        p.part = st->base + kNoAllocCounterBytes;
       }
     }
     p.tx = 0;
@@ -3757,32 +3838,22 @@ bool launch_verify(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cuda
                : launch_mma<F, 2, 8>(g, x, K, n_tok, s, src, st);
 }
 
-// The single-token tensor-core kernel: tiles of 16 WC rows (two CTAs per SM
-// up to eight consumer warps, else one), K split into the fewest segments
-// that give every CTA about kTcUnits (tile, segment) units to claim (finer
-// units shorten the tail; each segment's x is staged once per CTA), keeping
-// at least kTcMinStages stages per unit (each unit ends with one split-K
-// hand-over).  Rows whose stride is off the 16-byte grid (no tensor copies)
-// stay on gemv_stream: one-super-block stages would take one bulk copy per
-// row and super-block.
-constexpr int kTcUnits = 6;
-constexpr int kTcMinStages = 4;
-
-// h != nullptr: SwiGLU mode (g = {gate, up} of one shape; tiles of
-// kRows / 2 features; h = bf16(silu(gate) * up) written beside y).
-template <int F, int WC>
+// The single-token tensor-core kernel: one CTA per SM, 64-row tiles over all
+// of K (no split-K), x of the whole row staged once per CTA.  Rows whose
+// stride is off the 16-byte grid (no tensor copies), or rows too long for x
+// and two stages to fit in shared memory, stay on gemv_stream.
+// h != nullptr: SwiGLU mode (g = {gate, up} of one shape; tiles of 32
+// features; h = bf16(silu(gate) * up) written beside y).
+template <int F>
 bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
-                ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr,
                 uint16_t* h = nullptr) {
-  using G = TGeo<F, WC>;
+  using G = TGeo1<F>;
   const bool swiglu = h != nullptr;
   if (swiglu && (g.count != 2 || g.N[0] != g.N[1])) return false;
   const DevInfo* dip = dev_info();
   if (dip == nullptr) return false;
   const DevInfo& di = *dip;
-  const bool tma = tma_possible<G>(K);
-  if (!tma) return false;
-  const int per_sm = WC <= 8 ? 2 : 1;
+  if (!tma_possible<G>(K)) return false;
   Params p;
   p.g = g;
   p.x = x;
@@ -3791,9 +3862,12 @@ bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
   p.nt = 1;
   p.part = nullptr;
   p.arrivals = nullptr;
-  p.tma = tma ? 1 : 0;
-  const int slabs_row = (p.nsb + G::kSlabSB - 1) / G::kSlabSB;
-  const StageShape ss = stage_shape<G>(tma);
+  p.tag = 0;
+  p.tma = 1;
+  p.ksplit = 1;
+  p.slabs = (p.nsb + G::kSlabSB - 1) / G::kSlabSB;
+  p.kpad = p.slabs * G::kSlabK;
+  const StageShape ss = stage_shape<G>(true);
   p.slot = ss.slot;
   p.pslot = ss.pslot;
   p.pbase = ss.pbase;
@@ -3809,80 +3883,47 @@ bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
       p.tiles += (g.N[i] + G::kRows - 1) / G::kRows;
     p.tile_end[i] = p.tiles;
   }
-  size_t budget = di.smem_sm / per_sm > di.smem_reserved + kStaticSmem
-                      ? di.smem_sm / per_sm - di.smem_reserved - kStaticSmem
-                      : 0;
-  if (budget > di.smem_optin - kStaticSmem) budget = di.smem_optin - kStaticSmem;
-  int ksplit = 0;
-  for (int ks = 1; ks <= kMaxSegs && ks <= slabs_row; ++ks) {
-    if (slabs_row % ks != 0) continue;
-    if (ks > 1 && slabs_row / ks < kTcMinStages) break;
-    if (tc_x_bytes(slabs_row / ks * G::kSlabK, G::kSub, G::kRows) + 2 * ss.bytes > budget) continue;
-    ksplit = ks;
-    if (static_cast<int64_t>(p.tiles) * ks >= static_cast<int64_t>(kTcUnits) * per_sm * di.sms)
-      break;
-  }
-  if (ksplit == 0) return false;
-  for (;; ksplit = 1) {
-    p.ksplit = ksplit;
-    p.slabs = slabs_row / ksplit;
-    p.kpad = p.slabs * G::kSlabK;
-    p.x_bytes = tc_x_bytes(p.kpad, G::kSub, G::kRows);
-    if (p.x_bytes + 2 * ss.bytes > budget) return false;
-    if (ksplit == 1) break;
-    const size_t part_bytes = static_cast<size_t>(ksplit) * p.tiles * p.tile_rows * sizeof(float);
-    if (src == ScratchSrc::kDevice) {
-      if (p.tiles > kMaxTiles) continue;
-      uint8_t* base = static_cast<uint8_t*>(scratch_get(kCounterBytes + part_bytes, s));
-      if (base == nullptr) continue;   // no scratch (e.g. during capture): unsplit
-      p.arrivals = reinterpret_cast<unsigned int*>(base);
-      p.part = reinterpret_cast<float*>(base + kCounterBytes);
-    } else {
-      if (p.tiles > kNoAllocMaxTiles ||
-          kNoAllocCounterBytes + part_bytes > kNoAllocScratchBytes) {
-        st->too_large = true;   // beyond the fixed array: unsplit
-        continue;
-      }
-      if (cudaMemsetAsync(st->base, 0, static_cast<size_t>(p.tiles) * sizeof(unsigned int), s) !=
-          cudaSuccess) {
-        (void)cudaGetLastError();
-        return false;
-      }
-      p.arrivals = reinterpret_cast<unsigned int*>(st->base);
-      p.part = reinterpret_cast<float*>(st->base + kNoAllocCounterBytes);
+  // the kernel's static shared memory (its barriers) comes out of the same budget
+  static const size_t static_smem = [] {
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, gemv_tc1<F>) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return size_t{1024};
     }
-    break;
-  }
+    return fa.sharedSizeBytes;
+  }();
+  size_t budget = di.smem_sm > di.smem_reserved + static_smem
+                      ? di.smem_sm - di.smem_reserved - static_smem
+                      : 0;
+  if (budget > di.smem_optin - static_smem) budget = di.smem_optin - static_smem;
+  p.x_bytes = (tc_x_only(p.kpad, G::kSub) + G::kCombBytes + 127u) & ~127u;
+  if (p.x_bytes + 2 * static_cast<size_t>(ss.bytes) > budget) return false;
   int stages = static_cast<int>((budget - p.x_bytes) / ss.bytes);
   if (stages > kMaxStages) stages = kMaxStages;
-  int cps = per_sm * di.sms / p.ksplit;
-  if (cps > p.tiles) cps = p.tiles;
+  int cps = di.sms < p.tiles ? di.sms : p.tiles;
   if (cps < 1) cps = 1;
   p.static_tiles = (stages + p.slabs - 1) / p.slabs;
   const size_t smem = p.x_bytes + static_cast<size_t>(stages) * ss.bytes;
   static size_t configured[kMaxDevices] = {};   // per device: dynamic smem above 48 KB is opt-in
-  if (!raise_smem_limit(gemv_tc1<F, WC>, smem, configured)) return false;
-  p.tx = 0;
-  if (tma) {
-    const uint32_t box_rows = swiglu ? G::kRows / 2 : G::kRows;
-    for (int i = 0; i < g.count; ++i) {
-      const int64_t n = g.N[i];
-      bool ok;
-      if constexpr (F == kG128) {
-        ok = encode_plane(&p.tm[i][0], g.W[i], 128 * static_cast<uint64_t>(p.nsb), n, ss.slot,
-                          box_rows) &&
-             encode_plane(&p.tm[i][1], g.W[i] + n * p.nsb * 128, 8 * static_cast<uint64_t>(p.nsb), n,
-                          ss.pslot, box_rows);
-      } else {
-        ok = encode_plane(&p.tm[i][0], g.W[i], static_cast<uint64_t>(p.nsb) * G::kBB, n, ss.slot,
-                          box_rows);
-      }
-      if (!ok) return false;
+  if (!raise_smem_limit(gemv_tc1<F>, smem, configured)) return false;
+  const uint32_t box_rows = swiglu ? G::kRows / 2 : G::kRows;
+  for (int i = 0; i < g.count; ++i) {
+    const int64_t n = g.N[i];
+    bool ok;
+    if constexpr (F == kG128) {
+      ok = encode_plane(&p.tm[i][0], g.W[i], 128 * static_cast<uint64_t>(p.nsb), n, ss.slot,
+                        box_rows) &&
+           encode_plane(&p.tm[i][1], g.W[i] + n * p.nsb * 128, 8 * static_cast<uint64_t>(p.nsb), n,
+                        ss.pslot, box_rows);
+    } else {
+      ok = encode_plane(&p.tm[i][0], g.W[i], static_cast<uint64_t>(p.nsb) * G::kBB, n, ss.slot,
+                        box_rows);
     }
-    p.tx = static_cast<uint32_t>(G::kRows) * (ss.slot + ss.pslot);
+    if (!ok) return false;
   }
+  p.tx = static_cast<uint32_t>(G::kRows) * (ss.slot + ss.pslot);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(cps * p.ksplit));
+  cfg.gridDim = dim3(static_cast<unsigned>(cps));
   cfg.blockDim = dim3(G::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -3891,7 +3932,7 @@ bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return launched(cudaLaunchKernelEx(&cfg, gemv_tc1<F, WC>, p, stages));
+  return launched(cudaLaunchKernelEx(&cfg, gemv_tc1<F>, p, stages));
 }
 
 // The multi-token tensor-core kernel (n_tok 5..16, NB = 1 or 2 blocks of
@@ -3914,6 +3955,7 @@ bool launch_tcv(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   p.nt = n_tok;
   p.part = nullptr;
   p.arrivals = nullptr;
+  p.tag = 0;
   p.tma = 1;
   const int slabs_row = (p.nsb + G::kSlabSB - 1) / G::kSlabSB;
   const StageShape ss = stage_shape<G>(true);
@@ -3957,7 +3999,7 @@ bool launch_tcv(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
       uint8_t* base = static_cast<uint8_t*>(scratch_get(kCounterBytes + part_bytes, s));
       if (base == nullptr) continue;   // no scratch (e.g. during capture): unsplit
       p.arrivals = reinterpret_cast<unsigned int*>(base);
-      p.part = reinterpret_cast<float*>(base + kCounterBytes);
+      p.part = base + kCounterBytes;
     } else {
       if (p.tiles > kNoAllocMaxTiles ||
           kNoAllocCounterBytes + part_bytes > kNoAllocScratchBytes) {
@@ -3970,7 +4012,7 @@ bool launch_tcv(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
         return false;
       }
       p.arrivals = reinterpret_cast<unsigned int*>(st->base);
-      p.part = reinterpret_cast<float*>(st->base + kNoAllocCounterBytes);
+      p.part = st->base + kNoAllocCounterBytes;
     }
     break;
   }
@@ -4107,7 +4149,9 @@ bool tc1_eligible(int fmt, const GemvGroup& g, int K, int n_tok) {
 template <int F>
 bool launch_tc1_fmt(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
                     ScratchSrc src = ScratchSrc::kDevice, StaticScratch* st = nullptr) {
-  return launch_tc1<F, 16>(g, x, K, s, src, st);   // 16 consumer warps, one CTA per SM
+  (void)src;   // no split-K: no scratch
+  (void)st;
+  return launch_tc1<F>(g, x, K, s);
 }
 
 }  // namespace
@@ -4296,8 +4340,7 @@ StreamResult launch_swiglu(int fmt, const GemvGroup& g, const uint16_t* x, int K
   // tensor-core kernel
   if (n_tok == 1 && tc1_eligible(fmt, g, K, n_tok)) {
     const bool ok =
-        fmt == kQ4K ? launch_tc1<kQ4K, 16>(g, x, K, s, ScratchSrc::kDevice, nullptr, h)
-                    : launch_tc1<kG128, 16>(g, x, K, s, ScratchSrc::kDevice, nullptr, h);
+        fmt == kQ4K ? launch_tc1<kQ4K>(g, x, K, s, h) : launch_tc1<kG128>(g, x, K, s, h);
     if (ok) return StreamResult::kLaunched;
   }
   // otherwise: the grouped GEMV, then the activation as its own kernel
