@@ -2175,7 +2175,7 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC <= 4 ? 2 : 1)
 // mmas of a super-block, D[row][n] is the dot product of sub-block n alone,
 // the quantity one scale multiplies:
 //   y_row += s1[n] D[row][n] + s2[n] Sx[n]
-// A is exact (tc_sb_product: q or 16 q from (1024 + q) minus 1024 in fp16),
+// A is exact (tc_sb_product: q 2^-24 or 16 q 2^-24, fp16 subnormals),
 // so no offset term remains in D (a record of zero weights gives D = 0
 // whatever its scales); x is staged in fp16 with a power-of-two scale per
 // sub-block (stage_x_tc_raw) that the column scale undoes; s1 = d sc, s2 =
@@ -2275,9 +2275,10 @@ __host__ __device__ constexpr uint32_t tc_x_only(int kpad, int sub) {
 // (which lands in [2^14, 2^15)): then every value of the sub-block within a
 // factor 2^31 of its largest converts exactly (fp16 subnormals reach 2^-24),
 // and smaller ones round (contributing less than 2^-38 of the largest |x|
-// each).  The sub-block's column scale, stored beside Sx, undoes 2^-f: 2^f
-// for an even sub-block (low nibbles, A = q) and 2^(f-4) for an odd one
-// (high nibbles, A = 16 q).  bf16 subnormal x (below 2^-126) is not kept.
+// each).  The sub-block's column scale, stored beside Sx, undoes 2^-f and
+// the product's own power of two: 2^(f+24) for an even sub-block (low
+// nibbles, A = q 2^-24) and 2^(f+20) for an odd one (high nibbles, A =
+// 16 q 2^-24).  bf16 subnormal x (below 2^-126) is not kept.
 template <int S>
 __device__ void stage_x_tc_raw(const uint16_t* x, int K, int kpad, uint32_t xsh, int kbase) {
   static_assert(S == 32, "one sub-block is four lanes of eight positions");
@@ -2323,7 +2324,7 @@ __device__ void stage_x_tc_raw(const uint16_t* x, int K, int kpad, uint32_t xsh,
     sts128u(xsh + 16u * c, make_uint4(e[0], e[1], e[2], e[3]));
     if ((c & (S / 8 - 1)) == 0) {
       const int sb = c / (S / 8);
-      const float scale = __uint_as_float(static_cast<uint32_t>(127 + fs - 4 * (sb & 1)) << 23);
+      const float scale = __uint_as_float(static_cast<uint32_t>(127 + 24 + fs - 4 * (sb & 1)) << 23);
       asm volatile("st.shared.f32 [%0], %1;" ::"r"(xsum + 4u * sb), "f"(sum) : "memory");
       asm volatile("st.shared.f32 [%0], %1;" ::"r"(xscl + 4u * sb), "f"(scale) : "memory");
     }
@@ -2334,14 +2335,6 @@ __device__ void stage_x_tc_raw(const uint16_t* x, int K, int kpad, uint32_t xsh,
 template <int S>
 __device__ void stage_x_tc(const Params& p, uint32_t xsh, int kbase) {
   stage_x_tc_raw<S>(p.x, p.K, p.kpad, xsh, kbase);
-}
-
-constexpr uint32_t kF16Magic2 = 0x64006400u;   // fp16 (1024, 1024)
-
-__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
 }
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -2355,19 +2348,20 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
 // The single-token tensor-core product of one super-block for rows g and
 // g + 8 of a 16-row tile: lane t's qs chunk of each row starts at qa0 / qa1
 // (32 bytes), its B operands (the staged fp16 x of its column, or the zero
-// block) at xlo / xhi.  A is exact in fp16: one LOP3 makes (1024 + q) from
-// the low nibbles of bytes (0, 2) (mask 0x000F000F) and (1024 + 16 q) from
-// the high nibbles in place (mask 0x00F000F0: fp16's ten mantissa bits hold
-// bits 4..7), one fp16 subtraction of 1024 leaves q or 16 q; bytes (1, 3) go
-// through the same after one shift by 8.  The column scales of the staged x
-// absorb the factor 16 of the high nibbles.  d[0] / d[1]: the two mma
-// chains (bytes 0, 2 / bytes 1, 3); their sum per column is the dot product
-// of that column's sub-block.
+// block) at xlo / xhi.  A is exact in fp16 and needs one AND per two weights:
+// the low nibbles of bytes (0, 2) (mask 0x000F000F) read as fp16 are the
+// subnormals q 2^-24, the high nibbles in place (mask 0x00F000F0) are
+// 16 q 2^-24; bytes (1, 3) go through the same after one shift by 8.  The
+// tensor cores take fp16 subnormal operands as they are, and every product
+// and partial sum stays far inside fp32's normal range, so D is exactly
+// 2^-24 times the sum built from q itself; the column scales of the staged x
+// absorb 2^24 and the factor 16 of the high nibbles.  d[0] / d[1]: the two
+// mma chains (bytes 0, 2 / bytes 1, 3); their sum per column is the dot
+// product of that column's sub-block.
 __device__ __forceinline__ void tc_sb_product(uint32_t qa0, uint32_t qa1, uint32_t xlo,
                                               uint32_t xhi, float (&d)[2][4]) {
-  const uint32_t magic = kF16Magic2;
-  auto lo = [&](uint32_t w) { return f16x2_sub(lop_mask_or(w, 0x000F000Fu, magic), magic); };
-  auto hi = [&](uint32_t w) { return f16x2_sub(lop_mask_or(w, 0x00F000F0u, magic), magic); };
+  auto lo = [](uint32_t w) { return w & 0x000F000Fu; };
+  auto hi = [](uint32_t w) { return w & 0x00F000F0u; };
 #pragma unroll
   for (int hv = 0; hv < 2; ++hv) {   // words 4 hv .. 4 hv + 3 of the chunk
     const uint4 w0 = lds128(qa0 + 16 * hv), w8 = lds128(qa1 + 16 * hv);
@@ -2386,12 +2380,17 @@ __device__ __forceinline__ void tc_sb_product(uint32_t qa0, uint32_t qa1, uint32
   }
 }
 
-// y += s1 D + s2 Sx for rows g (h = 0) and g+8 (h = 1), columns (2t, 2t+1)
-__device__ __forceinline__ void tc_epilogue(float2 (&acc)[2], const float (&d)[2][4], float2 s1g,
-                                            float2 s2g, float2 s1h, float2 s2h, float2 sx) {
-  acc[0] = __ffma2_rn(s1g, make_float2(d[0][0] + d[1][0], d[0][1] + d[1][1]), acc[0]);
+// y += s1 (cs D) + s2 Sx for rows g (h = 0) and g+8 (h = 1), columns (2t,
+// 2t+1); cs, the columns' power-of-two scales, brings D to the units of x
+// before s1 multiplies it (no intermediate leaves fp32's range)
+__device__ __forceinline__ void tc_epilogue(float2 (&acc)[2], const float (&d)[2][4], float2 cs,
+                                            float2 s1g, float2 s2g, float2 s1h, float2 s2h,
+                                            float2 sx) {
+  const float2 dg = __fmul2_rn(cs, make_float2(d[0][0] + d[1][0], d[0][1] + d[1][1]));
+  const float2 dh = __fmul2_rn(cs, make_float2(d[0][2] + d[1][2], d[0][3] + d[1][3]));
+  acc[0] = __ffma2_rn(s1g, dg, acc[0]);
   acc[0] = __ffma2_rn(s2g, sx, acc[0]);
-  acc[1] = __ffma2_rn(s1h, make_float2(d[0][2] + d[1][2], d[0][3] + d[1][3]), acc[1]);
+  acc[1] = __ffma2_rn(s1h, dh, acc[1]);
   acc[1] = __ffma2_rn(s2h, sx, acc[1]);
 }
 
@@ -2598,7 +2597,7 @@ __global__ void __launch_bounds__(TGeo1<F>::kThreads, 1)
       tc_scales_q4<G>(p, tl, xsl, st, rb + g, sc, ss, t, s1h, s2h);
       const float2 sx = lds_f2(xsum + 4u * (8 * sbx + 2 * t));
       const float2 cs = lds_f2(xscl + 4u * (8 * sbx + 2 * t));   // column scales
-      tc_epilogue(acc, d, __fmul2_rn(s1g, cs), s2g, __fmul2_rn(s1h, cs), s2h, sx);
+      tc_epilogue(acc, d, cs, s1g, s2g, s1h, s2h, sx);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
@@ -3150,7 +3149,7 @@ __device__ __forceinline__ void small_sb_q4(const SmallParams& p, uint32_t wreg,
   }
   const float2 sx = lds_f2(xsum + 4u * (8 * sbx + 2 * t));
   const float2 cs = lds_f2(xscl + 4u * (8 * sbx + 2 * t));   // column scales
-  tc_epilogue(acc, d, __fmul2_rn(s1[0], cs), s2[0], __fmul2_rn(s1[1], cs), s2[1], sx);
+  tc_epilogue(acc, d, cs, s1[0], s2[0], s1[1], s2[1], sx);
 }
 
 template <int F>
