@@ -2697,13 +2697,17 @@ __host__ __device__ constexpr uint32_t tcv_xstride(int kpad) { return 2u * kpad 
 __host__ __device__ constexpr uint32_t tcv_row(int tok, int kpad) {
   return tok * tcv_xstride(kpad) + 8u * ((tok & 1) + 8 * ((tok >> 1) & 1));
 }
-// shared layout before the ring: x rows | Sx [kpad/32][8 NB] | WC scale
-// tables | two hand-over buffers of rows x 8 NB floats
+// shared layout before the ring: x rows | Sx [kpad/32][8 NB] | column
+// scales [kpad/32][8 NB] | WC scale tables | two hand-over buffers of rows x
+// 8 NB floats
 __host__ __device__ constexpr uint32_t tcv_sx(int kpad, int nb) {
   return tcv_xstride(kpad) * 8u * nb;
 }
-__host__ __device__ constexpr uint32_t tcv_tab(int kpad, int nb) {
+__host__ __device__ constexpr uint32_t tcv_cs(int kpad, int nb) {
   return tcv_sx(kpad, nb) + 4u * (kpad / 32) * 8u * nb;
+}
+__host__ __device__ constexpr uint32_t tcv_tab(int kpad, int nb) {
+  return tcv_cs(kpad, nb) + 4u * (kpad / 32) * 8u * nb;
 }
 __host__ __device__ constexpr uint32_t tcv_psum(int kpad, int nb, int wc) {
   return tcv_tab(kpad, nb) + wc * kTcvTabWarp;
@@ -2712,11 +2716,19 @@ __host__ __device__ constexpr uint32_t tcv_x_bytes(int kpad, int nb, int wc, int
   return (tcv_psum(kpad, nb, wc) + 2u * rows * 8u * nb * 4u + 127u) & ~127u;
 }
 
+// x of a K segment for the multi-token tensor-core product: per token, the
+// positions as fp16 (each group of four (a, b, c, d) stored (a, c, b, d)),
+// scaled per 32-position sub-block by a power of two 2^-f chosen from that
+// token's largest |x| in it, as in stage_x_tc_raw (so x converts exactly
+// within 2^31 of that largest); Sx, the fp32 sum of x per (sub-block, token);
+// and the (sub-block, token) column scale 2^(f+24) (low-nibble sub-blocks,
+// A = q 2^-24) or 2^(f+20) (high nibbles, A = 16 q 2^-24).
 template <int NB>
 __device__ void stage_x_tcv(const Params& p, uint32_t xsh, int kbase) {
   constexpr int NTP = 8 * NB;
   const int per_tok = p.kpad / 8;   // 16-byte chunks per token (a multiple of 32)
   const uint32_t sxa = xsh + tcv_sx(p.kpad, NB);
+  const uint32_t csa = xsh + tcv_cs(p.kpad, NB);
   const int lane = threadIdx.x & 31;
   for (int base = static_cast<int>(threadIdx.x) & ~31; base < NTP * per_tok;
        base += static_cast<int>(blockDim.x)) {
@@ -2725,24 +2737,44 @@ __device__ void stage_x_tcv(const Params& p, uint32_t xsh, int kbase) {
     const int k = kbase + 8 * c;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (tok < p.nt && k < p.K) v = ldg_nc_v4(p.x + static_cast<int64_t>(tok) * p.K + k);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[2 * j] = __uint_as_float(w[j] << 16);
+      f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+    float sum = 0.0f, amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      sum += f[j];
+      amax = fmaxf(amax, fabsf(f[j]));
+    }
+#pragma unroll
+    for (int m = 1; m < 4; m <<= 1) {
+      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, m);
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
+    }
+    int fs = amax > 0.0f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 14 : 0;
+    fs = fs < -100 ? -100 : (fs > 100 ? 100 : fs);
+    const float down = __uint_as_float(static_cast<uint32_t>(127 - fs) << 23);   // 2^-fs, exact
+    uint32_t e[4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {   // (p0, p2), (p1, p3) of each group of four
+      const __half2 a = __floats2half2_rn(f[4 * j] * down, f[4 * j + 2] * down);
+      const __half2 b = __floats2half2_rn(f[4 * j + 1] * down, f[4 * j + 3] * down);
+      e[2 * j] = *reinterpret_cast<const uint32_t*>(&a);
+      e[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&b);
+    }
     // rows start on 8-byte boundaries: two 8-byte stores
     const uint32_t a = xsh + tcv_row(tok, p.kpad) + 16u * c;
-    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(prmt(v.x, v.y, 0x5410u)),
-                 "r"(prmt(v.x, v.y, 0x7632u))
-                 : "memory");
-    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a + 8u), "r"(prmt(v.z, v.w, 0x5410u)),
-                 "r"(prmt(v.z, v.w, 0x7632u))
-                 : "memory");
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float sum = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      sum += __uint_as_float(w[j] << 16) + __uint_as_float(w[j] & 0xFFFF0000u);
-    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(e[0]), "r"(e[1]) : "memory");
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a + 8u), "r"(e[2]), "r"(e[3]) : "memory");
     if ((c & 3) == 0) {
-      asm volatile("st.shared.f32 [%0], %1;" ::"r"(sxa + 4u * ((c >> 2) * NTP + tok)), "f"(sum)
-                   : "memory");
+      const int j = c >> 2;   // sub-block of the segment (the segment starts on an even one)
+      const float scale = __uint_as_float(static_cast<uint32_t>(127 + 24 + fs - 4 * (j & 1)) << 23);
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(sxa + 4u * (j * NTP + tok)), "f"(sum) : "memory");
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(csa + 4u * (j * NTP + tok)), "f"(scale) : "memory");
     }
   }
 }
@@ -2797,8 +2829,8 @@ __device__ __forceinline__ void tcv_stage_q4(const Params& p, const Tile& tl, in
   constexpr int NTP = 8 * NB;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const uint32_t magic = 0x43004300u, mask = 0x000F000Fu;
   const uint32_t sxa = xsh + tcv_sx(p.kpad, NB);
+  const uint32_t csa = xsh + tcv_cs(p.kpad, NB);
   const int nrt = tl.rcnt - rbase > 16 ? 2 : 1;   // live row tiles of this warp
 #pragma unroll
   for (int s = 0; s < G::kSlabSB; ++s) {
@@ -2827,10 +2859,12 @@ __device__ __forceinline__ void tcv_stage_q4(const Params& p, const Tile& tl, in
           const uint32_t W[2] = {wv.x, wv.y};
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
-            l02[rt][h][m] = bf16x2_sub(lop_mask_or(W[m], mask, magic), magic);
-            l13[rt][h][m] = bf16x2_sub(lop_mask_or(W[m] >> 8, mask, magic), magic);
-            h02[rt][h][m] = bf16x2_sub(lop_mask_or(W[m] >> 4, mask, magic), magic);
-            h13[rt][h][m] = bf16x2_sub(lop_mask_or(W[m] >> 12, mask, magic), magic);
+            // fp16 subnormals: q 2^-24 (low nibbles), 16 q 2^-24 (high, in place)
+            const uint32_t w8 = W[m] >> 8;
+            l02[rt][h][m] = W[m] & 0x000F000Fu;
+            l13[rt][h][m] = w8 & 0x000F000Fu;
+            h02[rt][h][m] = W[m] & 0x00F000F0u;
+            h13[rt][h][m] = w8 & 0x00F000F0u;
           }
         }
       const int jlo = 8 * sbx + 2 * c;   // sub-block of the segment (low nibbles)
@@ -2844,25 +2878,27 @@ __device__ __forceinline__ void tcv_stage_q4(const Params& p, const Tile& tl, in
           const uint2 bh = lds64(xr + 64 + 8 * m);
 #pragma unroll
           for (int rt = 0; rt < kTcvRT; ++rt) {
-            mma_bf16(dl[rt], l02[rt][0][m], l02[rt][1][m], l13[rt][0][m], l13[rt][1][m], bl.x, bl.y);
-            mma_bf16(dh[rt], h02[rt][0][m], h02[rt][1][m], h13[rt][0][m], h13[rt][1][m], bh.x, bh.y);
+            mma_f16(dl[rt], l02[rt][0][m], l02[rt][1][m], l13[rt][0][m], l13[rt][1][m], bl.x, bl.y);
+            mma_f16(dh[rt], h02[rt][0][m], h02[rt][1][m], h13[rt][0][m], h13[rt][1][m], bh.x, bh.y);
           }
         }
         const float2 sxl = lds_f2(sxa + 4u * (jlo * NTP + 8 * nb + 2 * t));
         const float2 sxh = lds_f2(sxa + 4u * ((jlo + 1) * NTP + 8 * nb + 2 * t));
+        const float2 csl = lds_f2(csa + 4u * (jlo * NTP + 8 * nb + 2 * t));   // column scales
+        const float2 csh = lds_f2(csa + 4u * ((jlo + 1) * NTP + 8 * nb + 2 * t));
 #pragma unroll
         for (int rt = 0; rt < kTcvRT; ++rt) {
           const uint32_t te = tab + (rt * 8 + g) * kTcvTabPitch + 32u * c;
           const float4 el = lds_f4(te), eh = lds_f4(te + 16);   // (s1, s2) of rows g, g + 8
           float2& a0 = acc[nb][rt][0];
           float2& a1 = acc[nb][rt][1];
-          a0 = __ffma2_rn(make_float2(el.x, el.x), make_float2(dl[rt][0], dl[rt][1]), a0);
+          a0 = __ffma2_rn(make_float2(el.x, el.x), __fmul2_rn(csl, make_float2(dl[rt][0], dl[rt][1])), a0);
           a0 = __ffma2_rn(make_float2(el.y, el.y), sxl, a0);
-          a0 = __ffma2_rn(make_float2(eh.x, eh.x), make_float2(dh[rt][0], dh[rt][1]), a0);
+          a0 = __ffma2_rn(make_float2(eh.x, eh.x), __fmul2_rn(csh, make_float2(dh[rt][0], dh[rt][1])), a0);
           a0 = __ffma2_rn(make_float2(eh.y, eh.y), sxh, a0);
-          a1 = __ffma2_rn(make_float2(el.z, el.z), make_float2(dl[rt][2], dl[rt][3]), a1);
+          a1 = __ffma2_rn(make_float2(el.z, el.z), __fmul2_rn(csl, make_float2(dl[rt][2], dl[rt][3])), a1);
           a1 = __ffma2_rn(make_float2(el.w, el.w), sxl, a1);
-          a1 = __ffma2_rn(make_float2(eh.z, eh.z), make_float2(dh[rt][2], dh[rt][3]), a1);
+          a1 = __ffma2_rn(make_float2(eh.z, eh.z), __fmul2_rn(csh, make_float2(dh[rt][2], dh[rt][3])), a1);
           a1 = __ffma2_rn(make_float2(eh.w, eh.w), sxh, a1);
         }
       }
