@@ -2724,11 +2724,12 @@ __host__ __device__ constexpr uint32_t tcv_x_bytes(int kpad, int nb, int wc, int
 // and the (sub-block, token) column scale 2^(f+24) (low-nibble sub-blocks,
 // A = q 2^-24) or 2^(f+20) (high nibbles, A = 16 q 2^-24).
 template <int NB>
-__device__ void stage_x_tcv(const Params& p, uint32_t xsh, int kbase) {
+__device__ void stage_x_tcv_raw(const uint16_t* x, int K, int nt, int kpad, uint32_t xsh,
+                                int kbase) {
   constexpr int NTP = 8 * NB;
-  const int per_tok = p.kpad / 8;   // 16-byte chunks per token (a multiple of 32)
-  const uint32_t sxa = xsh + tcv_sx(p.kpad, NB);
-  const uint32_t csa = xsh + tcv_cs(p.kpad, NB);
+  const int per_tok = kpad / 8;   // 16-byte chunks per token (a multiple of 32)
+  const uint32_t sxa = xsh + tcv_sx(kpad, NB);
+  const uint32_t csa = xsh + tcv_cs(kpad, NB);
   const int lane = threadIdx.x & 31;
   for (int base = static_cast<int>(threadIdx.x) & ~31; base < NTP * per_tok;
        base += static_cast<int>(blockDim.x)) {
@@ -2736,7 +2737,7 @@ __device__ void stage_x_tcv(const Params& p, uint32_t xsh, int kbase) {
     const int tok = q / per_tok, c = q % per_tok;
     const int k = kbase + 8 * c;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (tok < p.nt && k < p.K) v = ldg_nc_v4(p.x + static_cast<int64_t>(tok) * p.K + k);
+    if (tok < nt && k < K) v = ldg_nc_v4(x + static_cast<int64_t>(tok) * K + k);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float f[8];
 #pragma unroll
@@ -2767,7 +2768,7 @@ __device__ void stage_x_tcv(const Params& p, uint32_t xsh, int kbase) {
       e[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&b);
     }
     // rows start on 8-byte boundaries: two 8-byte stores
-    const uint32_t a = xsh + tcv_row(tok, p.kpad) + 16u * c;
+    const uint32_t a = xsh + tcv_row(tok, kpad) + 16u * c;
     asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(e[0]), "r"(e[1]) : "memory");
     asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a + 8u), "r"(e[2]), "r"(e[3]) : "memory");
     if ((c & 3) == 0) {
@@ -2777,6 +2778,10 @@ __device__ void stage_x_tcv(const Params& p, uint32_t xsh, int kbase) {
       asm volatile("st.shared.f32 [%0], %1;" ::"r"(csa + 4u * (j * NTP + tok)), "f"(scale) : "memory");
     }
   }
+}
+template <int NB>
+__device__ void stage_x_tcv(const Params& p, uint32_t xsh, int kbase) {
+  stage_x_tcv_raw<NB>(p.x, p.K, p.nt, p.kpad, xsh, kbase);
 }
 
 __device__ __forceinline__ void sts_f2(uint32_t a, float x, float y) {
@@ -3076,6 +3081,10 @@ struct SmallParams {
   uint32_t ppitch;            // Q4_G128: shared bytes per row of the slice's params (+ halo)
   uint32_t warp_bytes;        // shared bytes per warp: 16 rows x (pitch + ppitch), 128-aligned
   uint32_t x_bytes;           // staged x, Sx, zero block and the slice sums, 128-aligned
+  // gemv_small_mt: tokens, and the offsets of the warps' scale tables and of
+  // the slice sums
+  int nt;
+  uint32_t tab_off, red_off;
 };
 
 __device__ __forceinline__ Tile small_tile(const SmallParams& p, int t) {
@@ -3259,6 +3268,181 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32, 1) gemv_small(const __gri
       a += e;
     }
     pick(p.g.y, ti.mi)[ti.row0 + r] = a;
+  }
+}
+
+// ------------------------------------------- small launches, 2..8 tokens
+//
+// gemv_small's structure -- one wave of CTAs, every warp's slice of 16 rows
+// bulk-copied before the dependency wait, slice sums added in shared memory
+// in slice order -- with gemv_tcv's product: the tokens are the n8 columns,
+// A is exact as fp16 subnormals, x is staged per token in fp16 with a
+// power-of-two scale per (token, sub-block) (stage_x_tcv_raw), and each
+// warp decodes its rows' (s1, s2) into a table once per super-block.  Like
+// gemv_small, it needs no global scratch: at verify widths the small
+// launches (attention projections) otherwise pay the split-K exchange.
+constexpr int kSmallMtMaxWarps = 16;   // registers for the multi-token product
+
+// This warp's (s1, s2) table for super-block s of its slice: entry (g, j), a
+// float4 at tab + g pitch + 16 j, holds (s1, s2) of row g and of row g + 8,
+// sub-block j.  Lane r < 16 decodes row r.
+template <int F>
+__device__ __forceinline__ void small_mt_table(const SmallParams& p, const Tile& tl, uint32_t wreg,
+                                               int s, int sb0, uint32_t tab) {
+  const int lane = threadIdx.x & 31;
+  if (lane >= 16) return;
+  const uint32_t te = tab + (lane & 7) * kTcvTabPitch + 8u * (lane >> 3);
+  if constexpr (F == kG128) {
+    const int64_t idx = (tl.row0 + lane) * static_cast<int64_t>(p.nsb) + sb0;
+    const uint32_t pa = wreg + 16u * p.pitch + lane * p.ppitch +
+                        static_cast<uint32_t>((idx * 8) & 15) + 8 * s;
+    const uint2 pr = lds64(pa);
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp) {
+      const float a = dd.x * static_cast<float>((pr.y >> (8 * grp)) & 0xFF);
+      const float b = -(dd.y * static_cast<float>((pr.y >> (16 + 8 * grp)) & 0xFF));
+#pragma unroll
+      for (int j = 4 * grp; j < 4 * grp + 4; ++j) sts_f2(te + 16 * j, a, b);
+    }
+  } else {
+    const uint4 hdr = lds128(wreg + lane * p.pitch + block_bytes(F) * s);
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t scp, mnp;
+      scale_pair6(scale_sel(c), hdr.y, hdr.z, hdr.w, scp, mnp);
+      sts_f2(te + 32 * c, dd.x * static_cast<float>(scp & 0xFF),
+             -(dd.y * static_cast<float>(mnp & 0xFF)));
+      sts_f2(te + 32 * c + 16, dd.x * static_cast<float>(scp >> 8),
+             -(dd.y * static_cast<float>(mnp >> 8)));
+    }
+  }
+}
+
+// Super-block s of this warp's slice (row s of the row's sb0 + s) for rows
+// g, g + 8 and tokens 2t, 2t + 1: gemv_tcv's product for one 16-row tile.
+template <int F>
+__device__ __forceinline__ void small_mt_sb(const SmallParams& p, uint32_t wreg, int s, int sbx,
+                                            uint32_t xsh, uint32_t tab, float2 (&acc)[2]) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t sxa = xsh + tcv_sx(p.K, 1);
+  const uint32_t csa = xsh + tcv_cs(p.K, 1);
+  uint32_t qa[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t rs = wreg + (g + 8 * h) * p.pitch;
+    qa[h] = (F == kG128) ? rs + 128 * s + 8 * t : rs + block_bytes(F) * s + 16 + 8 * t;
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t l02[2][2], l13[2][2], h02[2][2], h13[2][2];   // [row h][word m]
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint2 wv = lds64(qa[h] + 32 * c);
+      const uint32_t W[2] = {wv.x, wv.y};
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const uint32_t w8 = W[m] >> 8;
+        l02[h][m] = W[m] & 0x000F000Fu;
+        l13[h][m] = w8 & 0x000F000Fu;
+        h02[h][m] = W[m] & 0x00F000F0u;
+        h13[h][m] = w8 & 0x00F000F0u;
+      }
+    }
+    const int jlo = 8 * sbx + 2 * c;   // sub-block of the row (low nibbles)
+    const uint32_t xr = xsh + tcv_row(g, p.K) + 2u * (256 * sbx + 64 * c + 8 * t);
+    float dl[4] = {0.f, 0.f, 0.f, 0.f}, dh[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const uint2 bl = lds64(xr + 8 * m);
+      const uint2 bh = lds64(xr + 64 + 8 * m);
+      mma_f16(dl, l02[0][m], l02[1][m], l13[0][m], l13[1][m], bl.x, bl.y);
+      mma_f16(dh, h02[0][m], h02[1][m], h13[0][m], h13[1][m], bh.x, bh.y);
+    }
+    const float2 sxl = lds_f2(sxa + 4u * (jlo * 8 + 2 * t));
+    const float2 sxh = lds_f2(sxa + 4u * ((jlo + 1) * 8 + 2 * t));
+    const float2 csl = lds_f2(csa + 4u * (jlo * 8 + 2 * t));   // column scales
+    const float2 csh = lds_f2(csa + 4u * ((jlo + 1) * 8 + 2 * t));
+    const uint32_t te = tab + g * kTcvTabPitch + 32u * c;
+    const float4 el = lds_f4(te), eh = lds_f4(te + 16);   // (s1, s2) of rows g, g + 8
+    acc[0] = __ffma2_rn(make_float2(el.x, el.x), __fmul2_rn(csl, make_float2(dl[0], dl[1])), acc[0]);
+    acc[0] = __ffma2_rn(make_float2(el.y, el.y), sxl, acc[0]);
+    acc[0] = __ffma2_rn(make_float2(eh.x, eh.x), __fmul2_rn(csh, make_float2(dh[0], dh[1])), acc[0]);
+    acc[0] = __ffma2_rn(make_float2(eh.y, eh.y), sxh, acc[0]);
+    acc[1] = __ffma2_rn(make_float2(el.z, el.z), __fmul2_rn(csl, make_float2(dl[2], dl[3])), acc[1]);
+    acc[1] = __ffma2_rn(make_float2(el.w, el.w), sxl, acc[1]);
+    acc[1] = __ffma2_rn(make_float2(eh.z, eh.z), __fmul2_rn(csh, make_float2(dh[2], dh[3])), acc[1]);
+    acc[1] = __ffma2_rn(make_float2(eh.w, eh.w), sxh, acc[1]);
+  }
+}
+
+template <int F>
+__global__ void __launch_bounds__(kSmallMtMaxWarps * 32, 1)
+    gemv_small_mt(const __grid_constant__ SmallParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kSmallMtMaxWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = static_cast<int>(gridDim.x);
+  const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * p.tiles / C);
+  const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * p.tiles / C);
+  const int lt = warp / p.ks, j = warp % p.ks;
+  const bool active = t0 + lt < t1;           // warp-uniform
+  const int sb0 = j * p.sbs;
+  const int nsl = min(p.sbs, p.nsb - sb0);    // >= 1 (no empty slices)
+  const uint32_t xsh = smem_addr(smem);
+  const uint32_t tab = xsh + p.tab_off + static_cast<uint32_t>(warp) * (8u * kTcvTabPitch);
+  const uint32_t red = xsh + p.red_off;       // slice sums [max_tiles][ks][16][8]
+  const uint32_t wreg = xsh + p.x_bytes + static_cast<uint32_t>(warp) * p.warp_bytes;
+  const uint32_t bar = smem_addr(&bars[warp]);
+  Tile tl{};
+  if (active) tl = small_tile(p, t0 + lt);
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (active) {
+    const uint32_t tx = small_issue<F>(p, tl, sb0, nsl, wreg, bar, smem);
+    if (lane == 0) mbar_arrive_tx(bar, tx);
+  }
+  // x may be produced by the previous kernel
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  stage_x_tcv_raw<1>(p.x, p.K, p.nt, p.K, xsh, 0);
+  __syncthreads();
+  const int g = lane >> 2, t = lane & 3;
+  float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+  if (active && mbar_wait_warp(bar, 0u)) {
+    for (int s = 0; s < nsl; ++s) {
+      small_mt_table<F>(p, tl, wreg, s, sb0, tab);
+      __syncwarp();
+      small_mt_sb<F>(p, wreg, s, sb0 + s, xsh, tab, acc);
+      __syncwarp();   // the table is rebuilt for the next super-block
+    }
+  }
+  if (active) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      sts_f2(red + 4u * (((lt * p.ks + j) * 16 + g + 8 * h) * 8 + 2 * t), acc[h].x, acc[h].y);
+  }
+  __syncthreads();
+  // (row, token) i of the CTA's tiles: its slice sums in slice order
+  const int nval = (t1 - t0) * 16 * 8;
+  for (int i = static_cast<int>(threadIdx.x); i < nval; i += static_cast<int>(blockDim.x)) {
+    const int tt = i >> 7, r = (i >> 3) & 15, k = i & 7;
+    const Tile ti = small_tile(p, t0 + tt);
+    if (r >= ti.rcnt || k >= p.nt) continue;
+    float a = 0.0f;
+    for (int jj = 0; jj < p.ks; ++jj) {
+      float e;
+      asm volatile("ld.shared.f32 %0, [%1];"
+                   : "=f"(e)
+                   : "r"(red + 4u * (((tt * p.ks + jj) * 16 + r) * 8 + k)));
+      a += e;
+    }
+    pick(p.g.y, ti.mi)[static_cast<int64_t>(k) * pick(p.g.N, ti.mi) + ti.row0 + r] = a;
   }
 }
 
@@ -4140,6 +4324,67 @@ bool launch_small(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s) 
   return launched(cudaLaunchKernelEx(&cfg, gemv_small<F>, p));
 }
 
+// The small-launch kernel at 2..8 tokens: the same one wave of CTAs and
+// slices as launch_small (at most 16 warps per CTA), x of every token staged
+// once per CTA.
+template <int F>
+bool launch_small_mt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStream_t s) {
+  const DevInfo* dip = dev_info();
+  if (dip == nullptr) return false;
+  const DevInfo& di = *dip;
+  SmallParams p;
+  p.g = g;
+  p.x = x;
+  p.K = K;
+  p.nsb = K / 256;
+  p.nt = n_tok;
+  p.tiles = 0;
+  for (int i = 0; i < kMaxGroup; ++i) {
+    if (i < g.count) p.tiles += (g.N[i] + 15) / 16;
+    p.tile_end[i] = p.tiles;
+  }
+  const int C = p.tiles < di.sms ? p.tiles : di.sms;
+  if (C < 1) return false;
+  p.max_tiles = (p.tiles + C - 1) / C;
+  if (p.max_tiles > kSmallMaxTiles || p.max_tiles > kSmallMtMaxWarps) return false;
+  int ks = kSmallMtMaxWarps / p.max_tiles;
+  if (ks > p.nsb) ks = p.nsb;
+  p.sbs = (p.nsb + ks - 1) / ks;
+  p.ks = (p.nsb + p.sbs - 1) / p.sbs;   // every slice has at least one super-block
+  auto odd16 = [](uint32_t b) { b = (b + 15u) / 16u * 16u; return (b / 16u) % 2u ? b : b + 16u; };
+  p.pitch = odd16(static_cast<uint32_t>(p.sbs) * (F == kG128 ? 128u : block_bytes(F)));
+  p.ppitch = F == kG128 ? (static_cast<uint32_t>(p.sbs) * 8u + 16u + 15u) / 16u * 16u : 0u;
+  p.warp_bytes = (16u * (p.pitch + p.ppitch) + 127u) & ~127u;
+  const int warps = p.max_tiles * p.ks;
+  p.tab_off = tcv_tab(K, 1);
+  p.red_off = p.tab_off + static_cast<uint32_t>(warps) * 8u * kTcvTabPitch;
+  p.x_bytes = (p.red_off + 4u * static_cast<uint32_t>(p.max_tiles * p.ks * 16 * 8) + 127u) & ~127u;
+  const size_t smem = p.x_bytes + static_cast<size_t>(warps) * p.warp_bytes;
+  if (smem + kStaticSmem > di.smem_optin) return false;
+  static size_t configured[kMaxDevices] = {};
+  if (!raise_smem_limit(gemv_small_mt<F>, smem, configured)) return false;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(C));
+  cfg.blockDim = dim3(static_cast<unsigned>(warps * 32));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return launched(cudaLaunchKernelEx(&cfg, gemv_small_mt<F>, p));
+}
+
+// 2..8-token launches that take it: Q4_K and Q4_G128 launches of fewer than
+// 32 M weights (the tiles must still fit one wave).
+bool small_mt_eligible(int fmt, const GemvGroup& g, int K, int n_tok) {
+  if (n_tok < 2 || n_tok > 8 || (fmt != kQ4K && fmt != kG128)) return false;
+  int64_t rows = 0;
+  for (int i = 0; i < g.count; ++i) rows += g.N[i];
+  return rows * K < (int64_t{1} << 25);
+}
+
 // Single-token launches that take the small-launch kernel: Q4_K and Q4_G128
 // launches of fewer than 32 M weights (the single-token tensor-core kernel
 // takes the larger ones), as long as they fit one wave (launch_small).
@@ -4260,6 +4505,12 @@ StreamResult launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K
     if (tcv_eligible(fmt, g, K, n_tok)) {
       const bool ok = fmt == kQ4K ? launch_tcv_fmt<kQ4K>(g, x, K, n_tok, s, src, st)
                                   : launch_tcv_fmt<kG128>(g, x, K, n_tok, s, src, st);
+      if (ok) return StreamResult::kLaunched;
+    }
+    if (small_mt_eligible(fmt, g, K, n_tok)) {
+      // needs no scratch
+      const bool ok = fmt == kQ4K ? launch_small_mt<kQ4K>(g, x, K, n_tok, s)
+                                  : launch_small_mt<kG128>(g, x, K, n_tok, s);
       if (ok) return StreamResult::kLaunched;
     }
     bool ok = false;
