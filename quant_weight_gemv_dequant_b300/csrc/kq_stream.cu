@@ -3281,7 +3281,7 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32, 1) gemv_small(const __gri
 // warp decodes its rows' (s1, s2) into a table once per super-block.  Like
 // gemv_small, it needs no global scratch: at verify widths the small
 // launches (attention projections) otherwise pay the split-K exchange.
-constexpr int kSmallMtMaxWarps = 16;   // registers for the multi-token product
+constexpr int kSmallMtMaxWarps = 20;   // registers for the multi-token product
 
 // This warp's (s1, s2) table for super-block s of its slice: entry (g, j), a
 // float4 at tab + g pitch + 16 j, holds (s1, s2) of row g and of row g + 8,
@@ -4347,20 +4347,26 @@ bool launch_small_mt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cu
   if (C < 1) return false;
   p.max_tiles = (p.tiles + C - 1) / C;
   if (p.max_tiles > kSmallMaxTiles || p.max_tiles > kSmallMtMaxWarps) return false;
-  int ks = kSmallMtMaxWarps / p.max_tiles;
-  if (ks > p.nsb) ks = p.nsb;
-  p.sbs = (p.nsb + ks - 1) / ks;
-  p.ks = (p.nsb + p.sbs - 1) / p.sbs;   // every slice has at least one super-block
+  // the most warps (the shortest slices) whose layout fits shared memory
   auto odd16 = [](uint32_t b) { b = (b + 15u) / 16u * 16u; return (b / 16u) % 2u ? b : b + 16u; };
-  p.pitch = odd16(static_cast<uint32_t>(p.sbs) * (F == kG128 ? 128u : block_bytes(F)));
-  p.ppitch = F == kG128 ? (static_cast<uint32_t>(p.sbs) * 8u + 16u + 15u) / 16u * 16u : 0u;
-  p.warp_bytes = (16u * (p.pitch + p.ppitch) + 127u) & ~127u;
-  const int warps = p.max_tiles * p.ks;
-  p.tab_off = tcv_tab(K, 1);
-  p.red_off = p.tab_off + static_cast<uint32_t>(warps) * 8u * kTcvTabPitch;
-  p.x_bytes = (p.red_off + 4u * static_cast<uint32_t>(p.max_tiles * p.ks * 16 * 8) + 127u) & ~127u;
-  const size_t smem = p.x_bytes + static_cast<size_t>(warps) * p.warp_bytes;
-  if (smem + kStaticSmem > di.smem_optin) return false;
+  size_t smem = 0;
+  int warps = 0;
+  for (int want = kSmallMtMaxWarps / p.max_tiles; want >= 1; --want) {
+    const int ks = want < p.nsb ? want : p.nsb;
+    p.sbs = (p.nsb + ks - 1) / ks;
+    p.ks = (p.nsb + p.sbs - 1) / p.sbs;   // every slice has at least one super-block
+    p.pitch = odd16(static_cast<uint32_t>(p.sbs) * (F == kG128 ? 128u : block_bytes(F)));
+    p.ppitch = F == kG128 ? (static_cast<uint32_t>(p.sbs) * 8u + 16u + 15u) / 16u * 16u : 0u;
+    p.warp_bytes = (16u * (p.pitch + p.ppitch) + 127u) & ~127u;
+    warps = p.max_tiles * p.ks;
+    p.tab_off = tcv_tab(K, 1);
+    p.red_off = p.tab_off + static_cast<uint32_t>(warps) * 8u * kTcvTabPitch;
+    p.x_bytes = (p.red_off + 4u * static_cast<uint32_t>(p.max_tiles * p.ks * 16 * 8) + 127u) & ~127u;
+    smem = p.x_bytes + static_cast<size_t>(warps) * p.warp_bytes;
+    if (smem + kStaticSmem <= di.smem_optin) break;
+    smem = 0;
+  }
+  if (smem == 0) return false;
   static size_t configured[kMaxDevices] = {};
   if (!raise_smem_limit(gemv_small_mt<F>, smem, configured)) return false;
   cudaLaunchConfig_t cfg = {};
