@@ -2185,12 +2185,13 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC <= 4 ? 2 : 1)
 // and Q6_K would need their fields assembled first, which costs more integer
 // work than their CUDA-core path; they stay on gemv_stream.)
 //
-// gemv_tc1 (TGeo1): one CTA per SM, 16 consumer warps and a producer warp.
-// A tile is 64 rows over ALL of K, so no partial sum ever leaves the CTA: a
-// stage is the tile's 64 rows x 4 super-blocks (one tensor copy per plane),
-// warp w takes rows 16 (w & 3) .. + 15 of the stage's super-block w >> 2,
-// and at the tile's end the four warps of a row group add their row sums in
-// shared memory, super-block column 0 to 3 (a fixed order).  Tiles are
+// gemv_tc1 (TGeo1): one CTA per SM, 4 SB consumer warps and a producer warp
+// (SB = 5 where K / 256 divides by 5, else 4).  A tile is 64 rows over ALL
+// of K, so no partial sum ever leaves the CTA: a stage is the tile's 64 rows
+// x SB super-blocks (one tensor copy per plane), warp w takes rows 16 (w % 4)
+// .. + 15 of the stage's super-block w / 4, and at the tile's end the SB
+// warps of a row group add their row sums in shared memory, super-block
+// column 0 to SB - 1 (a fixed order).  Tiles are
 // claimed at run time (as in gemv_stream); x is staged once per CTA.
 // (Splitting K across CTAs instead needs a device-scope exchange of partial
 // sums whose latency ends up on the launch's critical path.)
@@ -2198,14 +2199,14 @@ __global__ void __launch_bounds__((WC + 1) * 32, WC <= 4 ? 2 : 1)
 // TGeo: the stage geometry of the multi-token kernel gemv_tcv (one-super-block
 // stages of 16 kWC RTW rows, a producer and a split-K reducer warp).
 
-template <int F>
+template <int F, int SB>
 struct TGeo1 {
   static constexpr int kF = F;
-  static constexpr int kWC = 16;
-  static constexpr int kThreads = (kWC + 1) * 32;   // + producer
   static constexpr int kRowGroups = 4;              // 16-row mma tiles per tile
+  static constexpr int kSlabSB = SB;                // super-blocks per stage
+  static constexpr int kWC = kRowGroups * SB;       // consumer warps
+  static constexpr int kThreads = (kWC + 1) * 32;   // + producer
   static constexpr int kRows = 16 * kRowGroups;
-  static constexpr int kSlabSB = kWC / kRowGroups;  // super-blocks per stage
   static constexpr int kSlabK = 256 * kSlabSB;
   static constexpr int kBB = block_bytes(F);
   static constexpr int kSub = 32;   // weights per sub-block
@@ -2516,10 +2517,10 @@ __device__ __forceinline__ void tc_reduce(const Params& p, uint32_t psum, uint32
   }
 }
 
-template <int F>
-__global__ void __launch_bounds__(TGeo1<F>::kThreads, 1)
+template <int F, int SB>
+__global__ void __launch_bounds__(TGeo1<F, SB>::kThreads, 1)
     gemv_tc1(const __grid_constant__ Params p, int stages) {
-  using G = TGeo1<F>;
+  using G = TGeo1<F, SB>;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 4 * G::kRowGroups];
   __shared__ int stage_tile[kMaxStages];
@@ -2635,7 +2636,7 @@ __global__ void __launch_bounds__(TGeo1<F>::kThreads, 1)
         return v;
       };
       const bool gate_group = p.swiglu && rg < G::kRowGroups / 2;
-      if (sc == (ntile & (G::kSlabSB - 1)) && !gate_group) {
+      if (sc == (ntile % G::kSlabSB) && !gate_group) {
         if (!mbar_wait_warp(my_full, k & 1u)) return;
         if (p.swiglu) {
           // features f of this up group's rows: up row 32 + f, gate row f
@@ -4063,10 +4064,9 @@ bool launch_verify(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cuda
 // and two stages to fit in shared memory, stay on gemv_stream.
 // h != nullptr: SwiGLU mode (g = {gate, up} of one shape; tiles of 32
 // features; h = bf16(silu(gate) * up) written beside y).
-template <int F>
-bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
-                uint16_t* h = nullptr) {
-  using G = TGeo1<F>;
+template <int F, int SB>
+bool launch_tc1_sb(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s, uint16_t* h) {
+  using G = TGeo1<F, SB>;
   const bool swiglu = h != nullptr;
   if (swiglu && (g.count != 2 || g.N[0] != g.N[1])) return false;
   const DevInfo* dip = dev_info();
@@ -4105,7 +4105,7 @@ bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
   // the kernel's static shared memory (its barriers) comes out of the same budget
   static const size_t static_smem = [] {
     cudaFuncAttributes fa{};
-    if (cudaFuncGetAttributes(&fa, gemv_tc1<F>) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, gemv_tc1<F, SB>) != cudaSuccess) {
       (void)cudaGetLastError();
       return size_t{1024};
     }
@@ -4124,7 +4124,7 @@ bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
   p.static_tiles = (stages + p.slabs - 1) / p.slabs;
   const size_t smem = p.x_bytes + static_cast<size_t>(stages) * ss.bytes;
   static size_t configured[kMaxDevices] = {};   // per device: dynamic smem above 48 KB is opt-in
-  if (!raise_smem_limit(gemv_tc1<F>, smem, configured)) return false;
+  if (!raise_smem_limit(gemv_tc1<F, SB>, smem, configured)) return false;
   const uint32_t box_rows = swiglu ? G::kRows / 2 : G::kRows;
   for (int i = 0; i < g.count; ++i) {
     const int64_t n = g.N[i];
@@ -4151,7 +4151,15 @@ bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return launched(cudaLaunchKernelEx(&cfg, gemv_tc1<F>, p, stages));
+  return launched(cudaLaunchKernelEx(&cfg, gemv_tc1<F, SB>, p, stages));
+}
+// Five super-block columns (20 consumer warps: more warps to hide the
+// product's latencies) where K / 256 divides by 5, so that no stage is left
+// partly empty; else four (16 warps).
+template <int F>
+bool launch_tc1(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s,
+                uint16_t* h = nullptr) {
+  return (K / 256) % 5 == 0 ? launch_tc1_sb<F, 5>(g, x, K, s, h) : launch_tc1_sb<F, 4>(g, x, K, s, h);
 }
 
 // The multi-token tensor-core kernel (n_tok 5..16, NB = 1 or 2 blocks of
