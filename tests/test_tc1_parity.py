@@ -10,7 +10,9 @@ Every row is checked against the fp64 oracle (|y - y_ref| <= 1e-3 sum|w^ x| +
 1e-5).  The shapes cover: ragged last tiles; an odd super-block count; Q6_K
 and Q4_G128 rows whose stride is off the 16-byte grid (per-row bulk copies;
 the tensor-core kernel declines those and the streaming kernel serves them);
-long rows split into many K segments (split-K hand-over to the reducer warp);
+long rows split into many K segments (split-K at verify widths; the
+single-token kernel takes whole rows); K / 256 = 20 (its five-column
+stages) with a ragged last tile;
 rows on the 16-byte grid (2-D tensor copies); random block bytes (every scale
 and field value); a grouped launch whose tiles straddle the two matrices; and
 repeated launches (tiles are claimed at run time, the result must not vary).
@@ -27,8 +29,10 @@ FMTS = [0, 1, 2, 3]
 FMT_IDS = ["Q4_K", "Q5_K", "Q6_K", "G128"]
 
 # (N, K): ragged tiles + odd K/256 (per-row copies for Q6_K and G128);
-# long rows with few tiles (many K segments); rows on the 16-byte grid
-CASES = [(8300, 4352), (1100, 32768), (20000, 2048)]
+# long rows with few tiles (many K segments); rows on the 16-byte grid;
+# K / 256 = 20 (the single-token kernel's five-column stages) with a ragged
+# last 64-row tile
+CASES = [(8300, 4352), (1100, 32768), (20000, 2048), (6600, 5120)]
 
 
 @pytest.fixture(scope="module")
@@ -179,3 +183,18 @@ def test_verify_width_grouped_launch(kq, oracle):
     kq.kq_device_status()
     for j, (yref, A) in enumerate(refs):
         _assert_parity(ys[j].cpu().numpy(), yref, A, f"matrix {j}")
+
+
+@pytest.mark.parametrize("fmt", [0, 3], ids=["Q4_K", "G128"])
+def test_single_token_five_columns_zero_weight_records(kq, oracle, fmt):
+    # the five-column stages (K / 256 = 20), a ragged last tile, and records
+    # of zero weights with nonzero scales, which must give exactly zero
+    from test_exact_edges import PERIOD, ZERO_TYPES, degenerate_matrix
+    N, K = 6600, 5120
+    W = degenerate_matrix(oracle, fmt, N, K, 4400 + fmt)
+    x = wl.activations_bf16(wl.derive_seed(4401, fmt), 1, K, heavy=True)
+    yref, A = oracle.gemv(fmt, W, N, K, x)
+    y = _gemv(kq, fmt, W, x, N, K)
+    _assert_parity(y, yref, A, f"fmt={fmt} five columns")
+    zero_rows = [r for r in range(N) if r % PERIOD in ZERO_TYPES]
+    assert np.all(yref[0, zero_rows] == 0.0) and np.all(y[0, zero_rows] == 0.0)
