@@ -181,14 +181,6 @@ __device__ __forceinline__ void lds_words_rec(uint32_t base, uint32_t sh, uint32
   for (int i = 0; i < N; ++i) w[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
 }
 
-// One LOP3 each.  Written as PTX with every operand in a register: with two
-// immediate operands the compiler splits (w & mask) | magic into two
-// instructions, which doubles the integer work per weight.
-__device__ __forceinline__ uint32_t lop_mask_or(uint32_t w, uint32_t mask, uint32_t magic) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(w), "r"(mask), "r"(magic));
-  return d;   // (w & mask) | magic
-}
 // (a - b) on two bf16 halves.  Used as bf16(c + q) - bf16(c) = bf16(q): both
 // operands and the difference are small integers, so the result is exact.
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
@@ -2670,21 +2662,22 @@ __global__ void __launch_bounds__(TGeo1<F, SB>::kThreads, 1)
 
 // ============================================= multi-token tensor-core kernel
 //
-// n_tok 5..16 on large Q4_K / Q4_G128 matrices (the speculative-verify
-// widths), on the skeleton of gemv_tc1 (one-super-block stages, tile
-// claiming, reducer warp; two 4-warp CTAs per SM up to eight tokens, one
-// 8-warp CTA beyond).  Columns of the n8 operand are tokens
-// (NB blocks of eight); a warp owns two 16-row mma tiles, so every B fragment
-// loaded from shared memory feeds two A fragments.  One mma covers 16
-// positions of one sub-block: lane t takes bytes 8t .. 8t+7 of a chunk, and
-// word m of them gives slots (2t, 2t+1) <- bytes (0, 2) and (2t+8, 2t+9) <-
-// bytes (1, 3): the low nibbles for the chunk's first sub-block, the high
-// nibbles (one more shift) for its second; A = bf16(q) exactly, as in
+// n_tok 2..16 on large Q4_K / Q4_G128 matrices (the speculative-verify
+// widths): one-super-block stages of 16 WC RTW rows, tile claiming, K split
+// into segments with a reducer warp (tc_reduce); two 4-warp CTAs per SM up
+// to eight tokens, one 8-warp CTA beyond.  Columns of the n8 operand are
+// tokens (NB blocks of eight); a warp owns two 16-row mma tiles, so every B
+// fragment loaded from shared memory feeds two A fragments.  One mma covers
+// 16 positions of one sub-block: lane t takes bytes 8t .. 8t+7 of a chunk,
+// and word m of them gives slots (2t, 2t+1) <- bytes (0, 2) and (2t+8, 2t+9)
+// <- bytes (1, 3): the low nibbles for the chunk's first sub-block, the high
+// nibbles (in place) for its second; A is exact as fp16 subnormals, as in
 // gemv_tc1.  Two mmas per sub-block, token block and row tile, then
-//   y[tok] += s1 D + s2 Sx[tok],  s1 = d sc, s2 = -dmin m
+//   y[tok] += s1 cs[tok] D + s2 Sx[tok],  s1 = d sc, s2 = -dmin m
 // per (row, sub-block), with s1, s2 from a per-warp table built once per
-// super-block (each lane decodes the four chunks of one row) and Sx staged
-// with x.  The staged x: token rows of kpad bf16 values, each group of four
+// super-block (each lane decodes the four chunks of one row), and Sx and the
+// column scale cs staged with x.  The staged x (stage_x_tcv_raw): token rows
+// of kpad fp16 values scaled per (token, sub-block), each group of four
 // positions (a, b, c, d) stored as (a, c, b, d) so that one 8-byte load gives
 // a lane both B registers of an mma; row tok starts at tok (2 kpad + 128) +
 // 8 ((tok & 1) + 8 ((tok >> 1) & 1)), which puts the 16 lanes of a half-warp
