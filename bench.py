@@ -664,18 +664,20 @@ def run_kq(args):
                        "share_of_step": dom[1]["share"]}
 
     # end to end through the public API with host buffers: per step, H2D of
-    # every activation input from pinned memory, the graph, D2H of the logits
+    # every activation input from pinned memory, the layers, D2H of the
+    # logits.  The step is captured with its input copies (DecodeStep.capture
+    # with host_x: layer by layer on a second stream, each layer waiting for
+    # its own inputs), so one replay copies every input of the step.
     e2e = None
     if not args.no_extra:
         y_host = torch.empty(step.y_head.shape, dtype=torch.float32).pin_memory()
         h2d = host_x.numel() * 2
         d2h = y_host.numel() * 4
+        ge = step.capture(stream, host_x=host_x)
 
         def e2e_step():
-            # one H2D copy of every activation input, the graph, the logits
             with torch.cuda.stream(stream):
-                step.x_all.copy_(host_x, non_blocking=True)
-                g.replay()
+                ge.replay()
                 y_host.copy_(step.y_head, non_blocking=True)
             stream.synchronize()
 

@@ -48,9 +48,12 @@ class DecodeStep:
             widths.append(lm_head[3])
         self.x_all = torch.zeros(n_tok * sum(widths), dtype=torch.bfloat16, device=device)
         views, off = [], 0
-        for w in widths:
+        self._xoff = [0]   # x_all elements before layer l (the LM head's input last)
+        for i, w in enumerate(widths):
             views.append(self.x_all[off:off + n_tok * w].view(n_tok, w))
             off += n_tok * w
+            if i % 4 == 3 or i == len(widths) - 1:
+                self._xoff.append(off)
         for li, L in enumerate(layers):
             xs = dict(zip(("x_attn", "x_o", "x_ffn", "x_down"), views[4 * li:4 * li + 4]))
             ys = {n: torch.empty((n_tok, L[n][2]), dtype=torch.float32, device=device)
@@ -89,10 +92,16 @@ class DecodeStep:
                     per_layer += 1
         return per_layer * len(self.layers) + (1 if self.lm_head is not None else 0)
 
-    def run(self, stream=None):
+    def run(self, stream=None, ready=None):
+        """Issue the step's launches on `stream`.  ready: {layer index (the LM
+        head's is the number of layers): event} -- that layer's first launch
+        waits for the event."""
         s = stream if stream is not None else torch.cuda.current_stream()
+        ready = ready or {}
         for li, (layer, io) in enumerate(self._structs):
             L, xs, ys = self.layers[li], self.x[li], self.y[li]
+            if li in ready:
+                s.wait_event(ready[li])
             if not self.fused_ffn and "attn_gate" not in L:
                 kq_layer_step(layer, io, self.n_tok, s)
                 continue
@@ -116,17 +125,53 @@ class DecodeStep:
                               xs["x_ffn"], gt[3], self.n_tok, s)
                 kq_gemv(dn[0], dn[1], xs["x_down"], ys["down"], dn[2], dn[3], self.n_tok, s)
         if self.lm_head is not None:
+            if len(self._structs) in ready:
+                s.wait_event(ready[len(self._structs)])
             f, W, N, K = self.lm_head
             kq_gemv(f, W, self.x_head, self.y_head, N, K, self.n_tok, s)
 
-    def capture(self, stream=None):
-        """Capture one step into a CUDA graph (replay with ``replay``)."""
+    def capture(self, stream=None, host_x=None):
+        """Capture one step into a CUDA graph (replay with ``replay``).
+
+        host_x: a pinned host tensor shaped like ``x_all``.  The graph then
+        also copies the step's inputs from it on a second stream, in three
+        pieces: layer 0's inputs, layers 1..16's, the rest (with the LM
+        head's).  Layer 0 waits for the first piece, layer 1 for the second,
+        layer 17 for the third, so the copies of later layers overlap the
+        earlier layers' work.  (A wait before every layer would cost more than
+        it hides: each one also ends the programmatic overlap of that
+        layer's first launch with its predecessor's tail.)"""
         s = stream if stream is not None else torch.cuda.Stream()
         self.run(s)                       # warm the launch path outside capture
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            self.run(s)
+        if host_x is None:
+            with torch.cuda.graph(g, stream=s):
+                self.run(s)
+        else:
+            if host_x.shape != self.x_all.shape or host_x.dtype != self.x_all.dtype:
+                raise ValueError("host_x must have the shape and dtype of x_all")
+            if not host_x.is_pinned():
+                raise ValueError("host_x must be pinned host memory")
+            cs = torch.cuda.Stream()
+            with torch.cuda.graph(g, stream=s):
+                fork = torch.cuda.Event()
+                fork.record(s)
+                cs.wait_event(fork)
+                nl = len(self._structs)
+                starts = sorted({0, min(1, nl), min(17, nl)})   # pieces begin at these layers
+                ready = {}
+                with torch.cuda.stream(cs):
+                    for i, li in enumerate(starts):
+                        end = starts[i + 1] if i + 1 < len(starts) else len(self._xoff) - 1
+                        a, b = self._xoff[li], self._xoff[end]
+                        if b > a:
+                            self.x_all[a:b].copy_(host_x[a:b], non_blocking=True)
+                        ev = torch.cuda.Event()
+                        ev.record(cs)
+                        ready[li] = ev
+                self.run(s, ready)
+                s.wait_event(ready[starts[-1]])   # join the copy stream
         self.graph = g
         return g
 

@@ -367,3 +367,55 @@ def test_degenerate_rows_and_tokens(kq, oracle, fmt):
         assert np.all(y[:, 0] == 0.0) and np.all(y[:, N - 1] == 0.0)   # zero rows give exact zeros
         if T > 1:
             assert np.all(y[1] == 0.0)                                  # so does a zero token
+
+
+def test_decode_step_graph_copies_host_inputs(kq, oracle, pools):
+    """DecodeStep.capture(host_x=...): the graph copies the step's inputs
+    from pinned host memory, layer by layer on a second stream, and each
+    layer waits for its own inputs.  Three layers and the LM head; the host
+    inputs change between replays, and each replay's outputs match the
+    oracle on that replay's inputs (a layer that ran before its copy landed
+    would use the previous inputs)."""
+    from quant_weight_gemv_dequant_b300.decode_step import DecodeStep, X_OF
+    nl = 3
+    pdev = {f: dev(p) for f, p in pools.items()}
+    layers = []
+    for l in range(nl):
+        L = {}
+        for i, m in enumerate(wl.DECODE_LAYER):
+            seed = wl.derive_seed(6, l, i)
+            L[m.name] = (m.fmt, wl.tile_matrix_device(pdev[m.fmt], m.fmt, seed, m.N, m.K), m.N, m.K)
+        layers.append(L)
+    h = wl.LM_HEAD
+    hs = wl.derive_seed(6, 999)
+    head = (h.fmt, wl.tile_matrix_device(pdev[h.fmt], h.fmt, hs, h.N, h.K), h.N, h.K)
+    step = DecodeStep(layers, head, 1)
+    host_x = torch.empty(step.x_all.shape, dtype=torch.bfloat16).pin_memory()
+    step.capture(host_x=host_x)
+    for r in range(2):
+        parts, xs = [], []
+        for l in range(nl):
+            d = {}
+            for j, key in enumerate(("x_attn", "x_o", "x_ffn", "x_down")):
+                d[key] = wl.activations_bf16(wl.derive_seed(6, r, l, j), 1, step.x[l][key].shape[1])
+                parts.append(d[key].reshape(-1))
+            xs.append(d)
+        xh = wl.activations_bf16(wl.derive_seed(6, r, 998), 1, h.K)
+        parts.append(xh.reshape(-1))
+        host_x.copy_(torch.from_numpy(np.concatenate(parts).view(np.int16)).view(torch.bfloat16))
+        for y in [step.y_head] + [t for ys in step.y for t in ys.values()]:
+            y.fill_(CANARY)
+        step.replay()
+        torch.cuda.synchronize()
+        for l in range(nl):
+            for i, m in enumerate(wl.DECODE_LAYER):
+                seed = wl.derive_seed(6, l, i)
+                rows = _sample_rows(m.N, 32, seed)
+                sub = wl.tiled_rows(pools[m.fmt], m.fmt, seed, m.N, m.K, rows)
+                yref, A = oracle.gemv(m.fmt, sub, len(rows), m.K, xs[l][X_OF[m.name]])
+                assert_parity(step.y[l][m.name].cpu().numpy()[:, rows], yref, A,
+                              f"replay {r} layer {l} {m.name}")
+        rows = _sample_rows(h.N, 64, hs)
+        sub = wl.tiled_rows(pools[h.fmt], h.fmt, hs, h.N, h.K, rows)
+        yref, A = oracle.gemv(h.fmt, sub, len(rows), h.K, xh)
+        assert_parity(step.y_head.cpu().numpy()[:, rows], yref, A, f"replay {r} lm_head")
