@@ -3079,6 +3079,10 @@ struct SmallParams {
   // the slice sums
   int nt;
   uint32_t tab_off, red_off;
+  // Q4_K: a warp's slice comes in one tensor copy (16 rows x pitch bytes)
+  // through the matrix's 2-D map, where the maps could be made
+  int tma;
+  CUtensorMap tm[kMaxGroup];
 };
 
 __device__ __forceinline__ Tile small_tile(const SmallParams& p, int t) {
@@ -3096,16 +3100,27 @@ __device__ __forceinline__ Tile small_tile(const SmallParams& p, int t) {
   return r;
 }
 
-// Issue the bulk copies of this warp's slice: lane r < 16 copies row r's
-// segment; returns the bytes the copies deliver (summed over the warp).
-// Q4_G128 param segments start on 8-byte boundaries: each is copied from
-// the 16-byte boundary at or below it (the consumer skips the offset), and
-// bytes past the plane's last 16-byte boundary are loaded with plain loads.
+// Issue the copies of this warp's slice; returns the bytes they deliver.
+// Tensor copy (Q4_K): lane 0 copies the 16 rows x pitch bytes from the
+// slice's first record (x in 8-byte elements; the box runs 16 bytes past a
+// slice whose records leave the pitch an even multiple of 16 bytes); rows
+// past the matrix and bytes past a row are zero-filled and counted.
+// Otherwise lane r < 16 copies row r's segment (the bytes are summed over
+// the warp).  Q4_G128 param segments start on 8-byte boundaries: each is
+// copied from the 16-byte boundary at or below it (the consumer skips the
+// offset), and bytes past the plane's last 16-byte boundary are loaded with
+// plain loads.
 template <int F>
 __device__ __forceinline__ uint32_t small_issue(const SmallParams& p, const Tile& tl, int sb0,
                                                 int nsl, uint32_t wreg, uint32_t bar,
                                                 uint8_t* smem) {
   const int lane = threadIdx.x & 31;
+  if constexpr (F == kQ4K) {
+    if (p.tma) {
+      if (lane == 0) tma_load_2d(wreg, &p.tm[tl.mi], sb0 * (block_bytes(F) / 8), tl.row0, bar);
+      return 16u * p.pitch;
+    }
+  }
   uint32_t tx = 0;
   if (lane < tl.rcnt) {
     const uint8_t* W = pick(p.g.W, tl.mi);
@@ -4273,6 +4288,19 @@ bool launch_tcv(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   return launched(cudaLaunchKernelEx(&cfg, gemv_tcv<F, WC, NB>, p, stages));
 }
 
+// The slices' tensor maps (Q4_K): a box of 16 rows x pitch bytes, which
+// must not be wider than a row.  Leaves p.tma = 0 (row copies) otherwise.
+template <int F>
+void small_maps(SmallParams& p, const GemvGroup& g) {
+  p.tma = 0;
+  if (F != kQ4K) return;
+  const uint64_t row = static_cast<uint64_t>(p.nsb) * block_bytes(F);
+  if (p.pitch > row) return;
+  for (int i = 0; i < g.count; ++i)
+    if (!encode_plane(&p.tm[i], g.W[i], row, static_cast<uint64_t>(g.N[i]), p.pitch, 16)) return;
+  p.tma = 1;
+}
+
 // The small-launch kernel: one wave, each CTA owning whole 16-row tiles
 // (at most kSmallMaxTiles), each warp one (tile, K slice); the slices are
 // as fine as kSmallMaxWarps warps per CTA allow.  Declines launches whose tiles do not
@@ -4310,6 +4338,7 @@ bool launch_small(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s) 
   const int warps = p.max_tiles * p.ks;
   const size_t smem = p.x_bytes + static_cast<size_t>(warps) * p.warp_bytes;
   if (smem + kStaticSmem > di.smem_optin) return false;
+  small_maps<F>(p, g);
   static size_t configured[kMaxDevices] = {};
   if (!raise_smem_limit(gemv_small<F>, smem, configured)) return false;
   cudaLaunchConfig_t cfg = {};
@@ -4368,6 +4397,7 @@ bool launch_small_mt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cu
     smem = 0;
   }
   if (smem == 0) return false;
+  small_maps<F>(p, g);
   static size_t configured[kMaxDevices] = {};
   if (!raise_smem_limit(gemv_small_mt<F>, smem, configured)) return false;
   cudaLaunchConfig_t cfg = {};
