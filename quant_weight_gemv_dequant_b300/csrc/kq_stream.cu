@@ -930,6 +930,20 @@ __device__ __forceinline__ ScaleSel scale_sel(int c) {
   r.shm = r.sh + (r.hi ? 4u : 0u);
   return r;
 }
+// (float(byte 0), float(byte 1)) of v, exact: each byte goes into the
+// mantissa of 2^23 with a byte permute and 2^23 is subtracted (no integer
+// to float conversion, which runs at a fraction of the FMA rate)
+__device__ __forceinline__ float2 bytes01_f2(uint32_t v) {
+  const float a = __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7440u));
+  const float b = __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7441u));
+  return __fadd2_rn(make_float2(a, b), make_float2(-8388608.0f, -8388608.0f));
+}
+
+// float(byte i) of v, exact, the same way
+__device__ __forceinline__ float byte_f(uint32_t v, int i) {
+  return __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7440u | static_cast<uint32_t>(i))) - 8388608.0f;
+}
+
 // (sc, m) byte pairs (sub-block 2c in byte 0, 2c+1 in byte 1), 6 bits each
 __device__ __forceinline__ void scale_pair6(const ScaleSel& q, uint32_t s0, uint32_t s1,
                                             uint32_t s2, uint32_t& sc, uint32_t& mn) {
@@ -1051,8 +1065,8 @@ __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl
       const uint2 pr = lds64(pa);
       const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
       const int g = c >> 1;
-      const float sc = static_cast<float>((pr.y >> (8 * g)) & 0xFF);
-      const float mn = static_cast<float>((pr.y >> (16 + 8 * g)) & 0xFF);
+      const float sc = byte_f(pr.y, g);
+      const float mn = byte_f(pr.y, 2 + g);
       dsc = make_float2(dd.x * sc, dd.x * sc);
       ndm = make_float2(-dd.y * mn, -dd.y * mn);
     } else {
@@ -1060,8 +1074,8 @@ __device__ __forceinline__ void stage_q4(const Params& p, const Tile& tl, int sl
       const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
       uint32_t scp, mnp;
       scale_pair6(ss, hdr.y, hdr.z, hdr.w, scp, mnp);
-      dsc = make_float2(dd.x * static_cast<float>(scp & 0xFF), dd.x * static_cast<float>(scp >> 8));
-      ndm = make_float2(-dd.y * static_cast<float>(mnp & 0xFF), -dd.y * static_cast<float>(mnp >> 8));
+      dsc = __fmul2_rn(make_float2(dd.x, dd.x), bytes01_f2(scp));
+      ndm = __fmul2_rn(make_float2(-dd.y, -dd.y), bytes01_f2(mnp));
     }
 #pragma unroll
     for (int k = 0; k < NT; ++k) {
@@ -1353,8 +1367,8 @@ __device__ __forceinline__ void stage_q4_q8(const Params& p, const Tile& tl, int
       const uint2 pr = lds64(st + p.pbase + row * p.pslot + po + 8 * sbl);
       const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
       const int g = c >> 1;
-      const float sc = static_cast<float>((pr.y >> (8 * g)) & 0xFF);
-      const float mn = static_cast<float>((pr.y >> (16 + 8 * g)) & 0xFF);
+      const float sc = byte_f(pr.y, g);
+      const float mn = byte_f(pr.y, 2 + g);
       dsc = make_float2(dd.x * sc, dd.x * sc);
       ndm = make_float2(-dd.y * mn, -dd.y * mn);
     } else {
@@ -1362,8 +1376,8 @@ __device__ __forceinline__ void stage_q4_q8(const Params& p, const Tile& tl, int
       const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
       uint32_t scp, mnp;
       scale_pair6(ss, hdr.y, hdr.z, hdr.w, scp, mnp);
-      dsc = make_float2(dd.x * static_cast<float>(scp & 0xFF), dd.x * static_cast<float>(scp >> 8));
-      ndm = make_float2(-dd.y * static_cast<float>(mnp & 0xFF), -dd.y * static_cast<float>(mnp >> 8));
+      dsc = __fmul2_rn(make_float2(dd.x, dd.x), bytes01_f2(scp));
+      ndm = __fmul2_rn(make_float2(-dd.y, -dd.y), bytes01_f2(mnp));
     }
 #pragma unroll
     for (int k = 0; k < NT; ++k) {
@@ -1788,8 +1802,8 @@ __device__ __forceinline__ void build_scale_table(const Params& p, const Tile& t
     const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
-      const float s1 = dd.x * static_cast<float>((pr.y >> (8 * g)) & 0xFF);
-      const float s2 = -(dd.y * static_cast<float>((pr.y >> (16 + 8 * g)) & 0xFF));
+      const float s1 = dd.x * byte_f(pr.y, g);
+      const float s2 = -(dd.y * byte_f(pr.y, 2 + g));
       const float4 e = make_float4(s1, s1, s2, s2);
 #pragma unroll
       for (int c = 2 * g; c < 2 * g + 2; ++c) {
@@ -1804,10 +1818,10 @@ __device__ __forceinline__ void build_scale_table(const Params& p, const Tile& t
     for (int c = 0; c < 4; ++c) {
       uint32_t scp, mnp;
       scale_pair6(scale_sel(c), hdr.y, hdr.z, hdr.w, scp, mnp);
-      const float s1l = dd.x * static_cast<float>(scp & 0xFF);
-      const float s1h = dd.x * static_cast<float>(scp >> 8);
-      const float s2l = -(dd.y * static_cast<float>(mnp & 0xFF));
-      const float s2h = -(dd.y * static_cast<float>(mnp >> 8));
+      const float s1l = dd.x * bytes01_f2(scp).x;
+      const float s1h = dd.x * bytes01_f2(scp).y;
+      const float s2l = -(dd.y * bytes01_f2(mnp).x);
+      const float s2h = -(dd.y * bytes01_f2(mnp).y);
       sts128(trow + ((s * 4 + c) * 2) * 16, make_float4(s1l, s1l, s2l, s2l));
       sts128(trow + ((s * 4 + c) * 2 + 1) * 16, make_float4(s1h, s1h, s2h, s2h));
     }
@@ -2400,8 +2414,8 @@ __device__ __forceinline__ void tc_scales_q4(const Params& p, const Tile& tl, in
     const uint2 pr = lds64(st + p.pbase + row * p.pslot + po + 8 * s);
     const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
     const int grp = t >> 1;
-    const float a = dd.x * static_cast<float>((pr.y >> (8 * grp)) & 0xFF);
-    const float b = -(dd.y * static_cast<float>((pr.y >> (16 + 8 * grp)) & 0xFF));
+    const float a = dd.x * byte_f(pr.y, grp);
+    const float b = -(dd.y * byte_f(pr.y, 2 + grp));
     s1 = make_float2(a, a);
     s2 = make_float2(b, b);
   } else {
@@ -2409,8 +2423,8 @@ __device__ __forceinline__ void tc_scales_q4(const Params& p, const Tile& tl, in
     const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
     uint32_t scp, mnp;
     scale_pair6(ss, hdr.y, hdr.z, hdr.w, scp, mnp);
-    s1 = make_float2(dd.x * static_cast<float>(scp & 0xFF), dd.x * static_cast<float>(scp >> 8));
-    s2 = make_float2(-(dd.y * static_cast<float>(mnp & 0xFF)), -(dd.y * static_cast<float>(mnp >> 8)));
+    s1 = __fmul2_rn(make_float2(dd.x, dd.x), bytes01_f2(scp));
+    s2 = __fmul2_rn(make_float2(-dd.y, -dd.y), bytes01_f2(mnp));
   }
 }
 
@@ -2799,8 +2813,8 @@ __device__ __forceinline__ void tcv_scale_table(const Params& p, const Tile& tl,
     const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
 #pragma unroll
     for (int grp = 0; grp < 2; ++grp) {
-      const float a = dd.x * static_cast<float>((pr.y >> (8 * grp)) & 0xFF);
-      const float b = -(dd.y * static_cast<float>((pr.y >> (16 + 8 * grp)) & 0xFF));
+      const float a = dd.x * byte_f(pr.y, grp);
+      const float b = -(dd.y * byte_f(pr.y, 2 + grp));
 #pragma unroll
       for (int j = 4 * grp; j < 4 * grp + 4; ++j) sts_f2(te + 16 * j, a, b);
     }
@@ -2811,10 +2825,10 @@ __device__ __forceinline__ void tcv_scale_table(const Params& p, const Tile& tl,
     for (int c = 0; c < 4; ++c) {
       uint32_t scp, mnp;
       scale_pair6(scale_sel(c), hdr.y, hdr.z, hdr.w, scp, mnp);
-      const float a0 = dd.x * static_cast<float>(scp & 0xFF);
-      const float a1 = dd.x * static_cast<float>(scp >> 8);
-      sts_f2(te + 32 * c, a0, -(dd.y * static_cast<float>(mnp & 0xFF)));
-      sts_f2(te + 32 * c + 16, a1, -(dd.y * static_cast<float>(mnp >> 8)));
+      const float a0 = dd.x * bytes01_f2(scp).x;
+      const float a1 = dd.x * bytes01_f2(scp).y;
+      sts_f2(te + 32 * c, a0, -(dd.y * bytes01_f2(mnp).x));
+      sts_f2(te + 32 * c + 16, a1, -(dd.y * bytes01_f2(mnp).y));
     }
   }
 }
@@ -3188,8 +3202,8 @@ __device__ __forceinline__ void small_sb_q4(const SmallParams& p, uint32_t wreg,
       const uint2 pr = lds64(pa);
       const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
       const int grp = t >> 1;
-      const float a = dd.x * static_cast<float>((pr.y >> (8 * grp)) & 0xFF);
-      const float b = -(dd.y * static_cast<float>((pr.y >> (16 + 8 * grp)) & 0xFF));
+      const float a = dd.x * byte_f(pr.y, grp);
+      const float b = -(dd.y * byte_f(pr.y, 2 + grp));
       s1[h] = make_float2(a, a);
       s2[h] = make_float2(b, b);
     } else {
@@ -3197,8 +3211,8 @@ __device__ __forceinline__ void small_sb_q4(const SmallParams& p, uint32_t wreg,
       const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
       uint32_t scp, mnp;
       scale_pair6(ss, hdr.y, hdr.z, hdr.w, scp, mnp);
-      s1[h] = make_float2(dd.x * static_cast<float>(scp & 0xFF), dd.x * static_cast<float>(scp >> 8));
-      s2[h] = make_float2(-(dd.y * static_cast<float>(mnp & 0xFF)), -(dd.y * static_cast<float>(mnp >> 8)));
+      s1[h] = __fmul2_rn(make_float2(dd.x, dd.x), bytes01_f2(scp));
+      s2[h] = __fmul2_rn(make_float2(-dd.y, -dd.y), bytes01_f2(mnp));
     }
   }
   const float2 sx = lds_f2(xsum + 4u * (8 * sbx + 2 * t));
@@ -3309,8 +3323,8 @@ __device__ __forceinline__ void small_mt_table(const SmallParams& p, const Tile&
     const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&pr.x));
 #pragma unroll
     for (int grp = 0; grp < 2; ++grp) {
-      const float a = dd.x * static_cast<float>((pr.y >> (8 * grp)) & 0xFF);
-      const float b = -(dd.y * static_cast<float>((pr.y >> (16 + 8 * grp)) & 0xFF));
+      const float a = dd.x * byte_f(pr.y, grp);
+      const float b = -(dd.y * byte_f(pr.y, 2 + grp));
 #pragma unroll
       for (int j = 4 * grp; j < 4 * grp + 4; ++j) sts_f2(te + 16 * j, a, b);
     }
@@ -3321,10 +3335,10 @@ __device__ __forceinline__ void small_mt_table(const SmallParams& p, const Tile&
     for (int c = 0; c < 4; ++c) {
       uint32_t scp, mnp;
       scale_pair6(scale_sel(c), hdr.y, hdr.z, hdr.w, scp, mnp);
-      sts_f2(te + 32 * c, dd.x * static_cast<float>(scp & 0xFF),
-             -(dd.y * static_cast<float>(mnp & 0xFF)));
-      sts_f2(te + 32 * c + 16, dd.x * static_cast<float>(scp >> 8),
-             -(dd.y * static_cast<float>(mnp >> 8)));
+      sts_f2(te + 32 * c, dd.x * bytes01_f2(scp).x,
+             -(dd.y * bytes01_f2(mnp).x));
+      sts_f2(te + 32 * c + 16, dd.x * bytes01_f2(scp).y,
+             -(dd.y * bytes01_f2(mnp).y));
     }
   }
 }
