@@ -1706,9 +1706,13 @@ struct MGeo {
   static constexpr int kQBytes = (F == kG128) ? 128 * kSlabSB : kBB * kSlabSB;
   static constexpr int kPBytes = (F == kG128) ? 8 * kSlabSB : 0;
   static constexpr int round16(int b) { return (b + 15) / 16 * 16; }
-  static constexpr int kSlotTma = round16(kQBytes + (kQBytes % 16 ? 15 : 0));
+  // row pitch an odd multiple of 16 bytes: the 8 rows a warp reads at once
+  // start in 8 different 16-byte bank groups (a tensor copy's box then reads
+  // up to 16 bytes of the next slab, or zeros past the row)
+  static constexpr int odd16(int b) { return (b / 16) % 2 ? b : b + 16; }
+  static constexpr int kSlotTma = odd16(round16(kQBytes + (kQBytes % 16 ? 15 : 0)));
   static constexpr int kPSlotTma = (F == kG128) ? round16(kPBytes + (kPBytes % 16 ? 15 : 0)) : 0;
-  static constexpr int kSlotBulk = round16(kQBytes + 16);
+  static constexpr int kSlotBulk = odd16(round16(kQBytes + 16));
   static constexpr int kPSlotBulk = (F == kG128) ? round16(kPBytes + 16) : 0;
   // per-warp scale table, one row of float4 per weight row (+1 float4 of
   // padding against bank conflicts):
