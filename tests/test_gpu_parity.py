@@ -92,13 +92,17 @@ def test_gemv_many_tiles_ragged_tail(kq, oracle, fmt):
 
 
 def test_gemv_long_rows(kq, oracle):
-    # the largest K on the path (down projection) and beyond
-    for fmt, K in ((2, 32768), (0, 65536)):
+    # the largest K on the path (down projection) and beyond; at K = 98304 a
+    # one-token small launch's warp slice (16 super-blocks) is wider than one
+    # tensor copy's box, so its rows are copied one by one
+    for fmt, K in ((2, 32768), (0, 65536), (0, 98304)):
         N = 5
         Wb = weights(oracle, fmt, N, K, wl.derive_seed(104, fmt))
         x = wl.activations_bf16(wl.derive_seed(105), 4, K, heavy=True)
         yref, A = oracle.gemv(fmt, Wb, N, K, x)
-        assert_parity(gpu_gemv(kq, fmt, Wb, x, N, K), yref, A, f"fmt={fmt} K={K}")
+        for T in (1, 4):
+            assert_parity(gpu_gemv(kq, fmt, Wb, x[:T], N, K), yref[:T], A[:T],
+                          f"fmt={fmt} K={K} n_tok={T}")
 
 
 @pytest.mark.parametrize("fmt", [0, 1, 2, 3], ids=["Q4_K", "Q5_K", "Q6_K", "G128"])
