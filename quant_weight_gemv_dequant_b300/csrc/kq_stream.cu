@@ -3064,15 +3064,16 @@ __global__ void __launch_bounds__((WC + 2) * 32, WC <= 4 ? 2 : 1)
 //   * one wave of CTAs (at most one per SM); CTA c owns the 16-row tiles
 //     [c T / C, (c+1) T / C) over all of K, so no partial sum leaves a CTA;
 //   * warp w owns slice (tile w / ks, K slice w % ks) of at most sbs
-//     super-blocks; before waiting for the previous kernel its lanes copy
-//     the slice's 16 row segments into the warp's part of shared memory with
-//     cp.async.bulk (one mbarrier per warp counts the bytes), so every weight
-//     byte of the launch is requested at once, while the previous kernel
-//     finishes;
+//     super-blocks; before waiting for the previous kernel it requests the
+//     slice into its part of shared memory (one mbarrier per warp counts the
+//     bytes), so every weight byte of the launch is requested at once, while
+//     the previous kernel finishes.  Q4_K: one 2-D tensor copy of the 16 rows
+//     (the number of copy instructions, not their size, is what costs here);
+//     Q4_G128, or a slice wider than a tensor box: one cp.async.bulk per row;
 //   * after griddepcontrol.wait the CTA stages x as gemv_tc1 does, and each
-//     warp runs gemv_tc1's tensor-core product (exact bf16 q, the eight n8
-//     columns carrying the eight sub-blocks of a super-block) on its slice as
-//     soon as its bytes have landed;
+//     warp runs gemv_tc1's tensor-core product (q exact as fp16 subnormals,
+//     the eight n8 columns carrying the eight sub-blocks of a super-block) on
+//     its slice as soon as its bytes have landed;
 //   * the ks slice sums of a row are added in slice order in shared memory
 //     (a fixed order: the result does not depend on timing) and written.
 // Row segments are copied at a pitch that is an odd multiple of 16 bytes, so
@@ -3301,8 +3302,8 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32, 1) gemv_small(const __gri
 // ------------------------------------------- small launches, 2..8 tokens
 //
 // gemv_small's structure -- one wave of CTAs, every warp's slice of 16 rows
-// bulk-copied before the dependency wait, slice sums added in shared memory
-// in slice order -- with gemv_tcv's product: the tokens are the n8 columns,
+// requested (one tensor copy, or row copies) before the dependency wait,
+// slice sums added in shared memory in slice order -- with gemv_tcv's product: the tokens are the n8 columns,
 // A is exact as fp16 subnormals, x is staged per token in fp16 with a
 // power-of-two scale per (token, sub-block) (stage_x_tcv_raw), and each
 // warp decodes its rows' (s1, s2) into a table once per super-block.  Like
