@@ -3303,7 +3303,8 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32, 1) gemv_small(const __gri
 //
 // gemv_small's structure -- one wave of CTAs, every warp's slice of 16 rows
 // requested (one tensor copy, or row copies) before the dependency wait,
-// slice sums added in shared memory in slice order -- with gemv_tcv's product: the tokens are the n8 columns,
+// slice sums added in shared memory in slice order -- with gemv_tcv's
+// product: the tokens are the n8 columns,
 // A is exact as fp16 subnormals, x is staged per token in fp16 with a
 // power-of-two scale per (token, sub-block) (stage_x_tcv_raw), and each
 // warp decodes its rows' (s1, s2) into a table once per super-block.  Like
