@@ -2739,55 +2739,81 @@ template <int NB>
 __device__ void stage_x_tcv_raw(const uint16_t* x, int K, int nt, int kpad, uint32_t xsh,
                                 int kbase) {
   constexpr int NTP = 8 * NB;
+  constexpr int kInFlight = 4;    // 16-byte chunks of x a thread loads before converting them
   const int per_tok = kpad / 8;   // 16-byte chunks per token (a multiple of 32)
+  const int total = NTP * per_tok;
+  const int stride = static_cast<int>(blockDim.x);
   const uint32_t sxa = xsh + tcv_sx(kpad, NB);
   const uint32_t csa = xsh + tcv_cs(kpad, NB);
   const int lane = threadIdx.x & 31;
-  for (int base = static_cast<int>(threadIdx.x) & ~31; base < NTP * per_tok;
-       base += static_cast<int>(blockDim.x)) {
-    const int q = base + lane;
-    const int tok = q / per_tok, c = q % per_tok;
-    const int k = kbase + 8 * c;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (tok < nt && k < K) v = ldg_nc_v4(x + static_cast<int64_t>(tok) * K + k);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float f[8];
+  // chunk q = token q / per_tok, positions 8 (q % per_tok) ..; a warp's 32
+  // chunks always belong to one token
+  for (int base = static_cast<int>(threadIdx.x) & ~31; base < total; base += kInFlight * stride) {
+    uint4 v[kInFlight];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      f[2 * j] = __uint_as_float(w[j] << 16);
-      f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-    }
-    float sum = 0.0f, amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      sum += f[j];
-      amax = fmaxf(amax, fabsf(f[j]));
+    for (int b = 0; b < kInFlight; ++b) {
+      const int q = base + b * stride + lane;
+      const int tok = q / per_tok, c = q % per_tok;
+      const int k = kbase + 8 * c;
+      v[b] = make_uint4(0, 0, 0, 0);
+      if (q < total && tok < nt && k < K) v[b] = ldg_nc_v4(x + static_cast<int64_t>(tok) * K + k);
     }
 #pragma unroll
-    for (int m = 1; m < 4; m <<= 1) {
-      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, m);
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
-    }
-    int fs = amax > 0.0f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 14 : 0;
-    fs = fs < -100 ? -100 : (fs > 100 ? 100 : fs);
-    const float down = __uint_as_float(static_cast<uint32_t>(127 - fs) << 23);   // 2^-fs, exact
-    uint32_t e[4];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {   // (p0, p2), (p1, p3) of each group of four
-      const __half2 a = __floats2half2_rn(f[4 * j] * down, f[4 * j + 2] * down);
-      const __half2 b = __floats2half2_rn(f[4 * j + 1] * down, f[4 * j + 3] * down);
-      e[2 * j] = *reinterpret_cast<const uint32_t*>(&a);
-      e[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&b);
-    }
-    // rows start on 8-byte boundaries: two 8-byte stores
-    const uint32_t a = xsh + tcv_row(tok, kpad) + 16u * c;
-    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(e[0]), "r"(e[1]) : "memory");
-    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a + 8u), "r"(e[2]), "r"(e[3]) : "memory");
-    if ((c & 3) == 0) {
+    for (int b = 0; b < kInFlight; ++b) {
+      if (base + b * stride >= total) break;   // warp-uniform
+      const int q = base + b * stride + lane;
+      const int tok = q / per_tok, c = q % per_tok;
+      const uint32_t a = xsh + tcv_row(tok, kpad) + 16u * c;
       const int j = c >> 2;   // sub-block of the segment (the segment starts on an even one)
-      const float scale = __uint_as_float(static_cast<uint32_t>(127 + 24 + fs - 4 * (j & 1)) << 23);
-      asm volatile("st.shared.f32 [%0], %1;" ::"r"(sxa + 4u * (j * NTP + tok)), "f"(sum) : "memory");
-      asm volatile("st.shared.f32 [%0], %1;" ::"r"(csa + 4u * (j * NTP + tok)), "f"(scale) : "memory");
+      if (tok >= nt) {
+        // a token the launch does not have: its row is zero (what the
+        // conversion below gives for zero x, without the work)
+        asm volatile("st.shared.v2.u32 [%0], {%1, %1};" ::"r"(a), "r"(0u) : "memory");
+        asm volatile("st.shared.v2.u32 [%0], {%1, %1};" ::"r"(a + 8u), "r"(0u) : "memory");
+        if ((c & 3) == 0) {
+          const float scale = __uint_as_float(static_cast<uint32_t>(127 + 24 - 4 * (j & 1)) << 23);
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(sxa + 4u * (j * NTP + tok)), "f"(0.0f) : "memory");
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(csa + 4u * (j * NTP + tok)), "f"(scale) : "memory");
+        }
+        continue;
+      }
+      const uint32_t w[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+      float f[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+      float sum = 0.0f, amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        sum += f[i];
+        amax = fmaxf(amax, fabsf(f[i]));
+      }
+#pragma unroll
+      for (int m = 1; m < 4; m <<= 1) {
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, m);
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
+      }
+      int fs = amax > 0.0f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 14 : 0;
+      fs = fs < -100 ? -100 : (fs > 100 ? 100 : fs);
+      const float down = __uint_as_float(static_cast<uint32_t>(127 - fs) << 23);   // 2^-fs, exact
+      uint32_t e[4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {   // (p0, p2), (p1, p3) of each group of four
+        const __half2 lo = __floats2half2_rn(f[4 * i] * down, f[4 * i + 2] * down);
+        const __half2 hi = __floats2half2_rn(f[4 * i + 1] * down, f[4 * i + 3] * down);
+        e[2 * i] = *reinterpret_cast<const uint32_t*>(&lo);
+        e[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+      }
+      // rows start on 8-byte boundaries: two 8-byte stores
+      asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(e[0]), "r"(e[1]) : "memory");
+      asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a + 8u), "r"(e[2]), "r"(e[3]) : "memory");
+      if ((c & 3) == 0) {
+        const float scale = __uint_as_float(static_cast<uint32_t>(127 + 24 + fs - 4 * (j & 1)) << 23);
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(sxa + 4u * (j * NTP + tok)), "f"(sum) : "memory");
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(csa + 4u * (j * NTP + tok)), "f"(scale) : "memory");
+      }
     }
   }
 }
