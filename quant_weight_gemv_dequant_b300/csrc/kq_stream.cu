@@ -2391,6 +2391,68 @@ __device__ __forceinline__ void tc_sb_product(uint32_t qa0, uint32_t qa1, uint32
   }
 }
 
+// rotate left by r (0..31)
+__device__ __forceinline__ uint32_t rotl32(uint32_t v, uint32_t r) {
+  return __funnelshift_l(v, v, r);
+}
+
+// Q5_K: the fifth bit of a weight sits in qh, byte l (position l of a
+// 32-position run) bit j for sub-block j, so the qh word with the same index
+// as a qs word holds the fifth bits of that word's four positions.  For the
+// low nibbles of sub-block j the bit goes beside the nibble, to bit 4 of each
+// 16-bit half (16 2^-24 as an fp16 subnormal), for the high nibbles of
+// sub-block j + 1 (kept in place, 16 q 2^-24) to bit 8 (256 2^-24): q stays
+// exact (at most 31 or 496 times 2^-24).  r = the rotation that brings bit j
+// of byte 0 to bit 4 (bytes 0, 2 of a word); the others follow from it.
+struct Q5Rot {
+  uint32_t lo02, lo13, hi02, hi13;
+};
+__device__ __forceinline__ Q5Rot q5_rot(int j) {   // j = the low-nibble sub-block (even)
+  Q5Rot r;
+  r.lo02 = static_cast<uint32_t>(4 - j) & 31u;    // bits j, 16 + j     -> 4, 20
+  r.lo13 = static_cast<uint32_t>(28 - j) & 31u;   // bits 8 + j, 24 + j -> 4, 20
+  r.hi02 = static_cast<uint32_t>(7 - j) & 31u;    // bits j + 1, 17 + j -> 8, 24
+  r.hi13 = static_cast<uint32_t>(31 - j) & 31u;   // bits 9 + j, 25 + j -> 8, 24
+  return r;
+}
+__device__ __forceinline__ uint32_t or_bits(uint32_t a, uint32_t q, uint32_t m) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xF8;" : "=r"(d) : "r"(a), "r"(q), "r"(m));
+  return d;   // a | (q & m)
+}
+
+// tc_sb_product for Q5_K: qh0 / qh1, the rows' 32 qh bytes; rot from q5_rot(2t).
+__device__ __forceinline__ void tc_sb_product_q5(uint32_t qa0, uint32_t qa1, uint32_t qh0,
+                                                 uint32_t qh1, uint32_t xlo, uint32_t xhi,
+                                                 const Q5Rot& rot, float (&d)[2][4]) {
+  const uint32_t M4 = 0x00100010u, M8 = 0x01000100u;
+#pragma unroll
+  for (int hv = 0; hv < 2; ++hv) {
+    const uint4 w0 = lds128(qa0 + 16 * hv), w8 = lds128(qa1 + 16 * hv);
+    const uint4 h0 = lds128(qh0 + 16 * hv), h8 = lds128(qh1 + 16 * hv);
+    const uint4 bl0 = lds128(xlo + 32 * hv), bl1 = lds128(xlo + 32 * hv + 16);
+    const uint4 bh0 = lds128(xhi + 32 * hv), bh1 = lds128(xhi + 32 * hv + 16);
+    const uint32_t W[2][4] = {{w0.x, w0.y, w0.z, w0.w}, {w8.x, w8.y, w8.z, w8.w}};
+    const uint32_t H[2][4] = {{h0.x, h0.y, h0.z, h0.w}, {h8.x, h8.y, h8.z, h8.w}};
+    const uint32_t BL[8] = {bl0.x, bl0.y, bl0.z, bl0.w, bl1.x, bl1.y, bl1.z, bl1.w};
+    const uint32_t BH[8] = {bh0.x, bh0.y, bh0.z, bh0.w, bh1.x, bh1.y, bh1.z, bh1.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      uint32_t l02[2], l13[2], h02[2], h13[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint32_t w = W[r][m], w8v = w >> 8, q = H[r][m];
+        l02[r] = or_bits(w & 0x000F000Fu, rotl32(q, rot.lo02), M4);
+        l13[r] = or_bits(w8v & 0x000F000Fu, rotl32(q, rot.lo13), M4);
+        h02[r] = or_bits(w & 0x00F000F0u, rotl32(q, rot.hi02), M8);
+        h13[r] = or_bits(w8v & 0x00F000F0u, rotl32(q, rot.hi13), M8);
+      }
+      mma_f16(d[0], l02[0], l02[1], h02[0], h02[1], BL[2 * m], BH[2 * m]);
+      mma_f16(d[1], l13[0], l13[1], h13[0], h13[1], BL[2 * m + 1], BH[2 * m + 1]);
+    }
+  }
+}
+
 // y += s1 (cs D) + s2 Sx for rows g (h = 0) and g+8 (h = 1), columns (2t,
 // 2t+1); cs, the columns' power-of-two scales, brings D to the units of x
 // before s1 multiplies it (no intermediate leaves fp32's range)
@@ -3106,6 +3168,9 @@ __global__ void __launch_bounds__((WC + 2) * 32, WC <= 4 ? 2 : 1)
 // the eight rows a warp reads at once fall in different bank groups.
 
 constexpr int kSmallMaxWarps = 24;   // 768 threads: registers for the product without spills
+// Q5_K's product holds the qh words too: 20 warps (102 registers a thread)
+template <int F>
+constexpr int small_max_warps() { return F == kQ5K ? 20 : kSmallMaxWarps; }
 
 struct SmallParams {
   GemvGroup g;
@@ -3124,7 +3189,7 @@ struct SmallParams {
   // the slice sums
   int nt;
   uint32_t tab_off, red_off;
-  // Q4_K: a warp's slice comes in one tensor copy (16 rows x pitch bytes)
+  // Q4_K, Q5_K: a warp's slice comes in one tensor copy (16 rows x pitch bytes)
   // through the matrix's 2-D map, where the maps could be made
   int tma;
   CUtensorMap tm[kMaxGroup];
@@ -3146,7 +3211,7 @@ __device__ __forceinline__ Tile small_tile(const SmallParams& p, int t) {
 }
 
 // Issue the copies of this warp's slice; returns the bytes they deliver.
-// Tensor copy (Q4_K): lane 0 copies the 16 rows x pitch bytes from the
+// Tensor copy (Q4_K, Q5_K): lane 0 copies the 16 rows x pitch bytes from the
 // slice's first record (x in 8-byte elements; the box runs 16 bytes past a
 // slice whose records leave the pitch an even multiple of 16 bytes); rows
 // past the matrix and bytes past a row are zero-filled and counted.
@@ -3160,7 +3225,7 @@ __device__ __forceinline__ uint32_t small_issue(const SmallParams& p, const Tile
                                                 int nsl, uint32_t wreg, uint32_t bar,
                                                 uint8_t* smem) {
   const int lane = threadIdx.x & 31;
-  if constexpr (F == kQ4K) {
+  if constexpr (F == kQ4K || F == kQ5K) {
     if (p.tma) {
       if (lane == 0) tma_load_2d(wreg, &p.tm[tl.mi], sb0 * (block_bytes(F) / 8), tl.row0, bar);
       return 16u * p.pitch;
@@ -3213,14 +3278,21 @@ __device__ __forceinline__ void small_sb_q4(const SmallParams& p, uint32_t wreg,
   const bool act_lo = g == 2 * t, act_hi = g == 2 * t + 1;   // column g of the B operand
   const uint32_t xlo = act_lo ? xsh + 64u * (8 * sbx + 2 * t) : zero;
   const uint32_t xhi = act_hi ? xsh + 64u * (8 * sbx + 2 * t + 1) : zero;
+  // chunk t of the qs bytes (Q5_K: after the 32 qh bytes) of rows g, g + 8
+  constexpr uint32_t kQs = (F == kG128) ? 0u : (F == kQ5K ? 48u : 16u);
   uint32_t qa[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const uint32_t rs = wreg + (g + 8 * h) * p.pitch;
-    qa[h] = (F == kG128) ? rs + 128 * s + 32 * t : rs + block_bytes(F) * s + 16 + 32 * t;
+    qa[h] = (F == kG128) ? rs + 128 * s + 32 * t : rs + block_bytes(F) * s + kQs + 32 * t;
   }
   float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  tc_sb_product(qa[0], qa[1], xlo, xhi, d);
+  if constexpr (F == kQ5K) {
+    const uint32_t qh0 = wreg + g * p.pitch + block_bytes(F) * s + 16;
+    tc_sb_product_q5(qa[0], qa[1], qh0, qh0 + 8 * p.pitch, xlo, xhi, q5_rot(2 * t), d);
+  } else {
+    tc_sb_product(qa[0], qa[1], xlo, xhi, d);
+  }
   // (s1, s2) of sub-blocks (2t, 2t+1) of rows g and g + 8
   float2 s1[2], s2[2];
 #pragma unroll
@@ -3252,7 +3324,8 @@ __device__ __forceinline__ void small_sb_q4(const SmallParams& p, uint32_t wreg,
 }
 
 template <int F>
-__global__ void __launch_bounds__(kSmallMaxWarps * 32, 1) gemv_small(const __grid_constant__ SmallParams p) {
+__global__ void __launch_bounds__(small_max_warps<F>() * 32, 1)
+    gemv_small(const __grid_constant__ SmallParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kSmallMaxWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -3384,11 +3457,20 @@ __device__ __forceinline__ void small_mt_sb(const SmallParams& p, uint32_t wreg,
   const int g = lane >> 2, t = lane & 3;
   const uint32_t sxa = xsh + tcv_sx(p.K, 1);
   const uint32_t csa = xsh + tcv_cs(p.K, 1);
+  // bytes 8t .. 8t + 7 of each 32-byte qs chunk (Q5_K: after the 32 qh
+  // bytes) of rows g, g + 8; Q5_K: the qh words of the same positions
+  constexpr uint32_t kQs = (F == kG128) ? 0u : (F == kQ5K ? 48u : 16u);
   uint32_t qa[2];
+  uint32_t qh[2][2] = {{0u, 0u}, {0u, 0u}};
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const uint32_t rs = wreg + (g + 8 * h) * p.pitch;
-    qa[h] = (F == kG128) ? rs + 128 * s + 8 * t : rs + block_bytes(F) * s + 16 + 8 * t;
+    qa[h] = (F == kG128) ? rs + 128 * s + 8 * t : rs + block_bytes(F) * s + kQs + 8 * t;
+    if constexpr (F == kQ5K) {
+      const uint2 hv = lds64(rs + block_bytes(F) * s + 16 + 8 * t);
+      qh[h][0] = hv.x;
+      qh[h][1] = hv.y;
+    }
   }
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -3404,6 +3486,14 @@ __device__ __forceinline__ void small_mt_sb(const SmallParams& p, uint32_t wreg,
         l13[h][m] = w8 & 0x000F000Fu;
         h02[h][m] = W[m] & 0x00F000F0u;
         h13[h][m] = w8 & 0x00F000F0u;
+        if constexpr (F == kQ5K) {   // the fifth bits of sub-blocks 2c, 2c + 1
+          const Q5Rot rot = q5_rot(2 * c);
+          const uint32_t q = qh[h][m];
+          l02[h][m] = or_bits(l02[h][m], rotl32(q, rot.lo02), 0x00100010u);
+          l13[h][m] = or_bits(l13[h][m], rotl32(q, rot.lo13), 0x00100010u);
+          h02[h][m] = or_bits(h02[h][m], rotl32(q, rot.hi02), 0x01000100u);
+          h13[h][m] = or_bits(h13[h][m], rotl32(q, rot.hi13), 0x01000100u);
+        }
       }
     }
     const int jlo = 8 * sbx + 2 * c;   // sub-block of the row (low nibbles)
@@ -4334,12 +4424,12 @@ bool launch_tcv(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   return launched(cudaLaunchKernelEx(&cfg, gemv_tcv<F, WC, NB>, p, stages));
 }
 
-// The slices' tensor maps (Q4_K): a box of 16 rows x pitch bytes, which
+// The slices' tensor maps (Q4_K, Q5_K): a box of 16 rows x pitch bytes, which
 // must not be wider than a row.  Leaves p.tma = 0 (row copies) otherwise.
 template <int F>
 void small_maps(SmallParams& p, const GemvGroup& g) {
   p.tma = 0;
-  if (F != kQ4K) return;
+  if (F != kQ4K && F != kQ5K) return;
   const uint64_t row = static_cast<uint64_t>(p.nsb) * block_bytes(F);
   if (p.pitch > row) return;
   for (int i = 0; i < g.count; ++i)
@@ -4349,7 +4439,7 @@ void small_maps(SmallParams& p, const GemvGroup& g) {
 
 // The small-launch kernel: one wave, each CTA owning whole 16-row tiles
 // (at most kSmallMaxTiles), each warp one (tile, K slice); the slices are
-// as fine as kSmallMaxWarps warps per CTA allow.  Declines launches whose tiles do not
+// as fine as small_max_warps<F>() warps per CTA allow.  Declines launches whose tiles do not
 // fit one CTA per SM in shared memory.
 constexpr int kSmallMaxTiles = 4;
 
@@ -4372,7 +4462,7 @@ bool launch_small(const GemvGroup& g, const uint16_t* x, int K, cudaStream_t s) 
   if (C < 1) return false;
   p.max_tiles = (p.tiles + C - 1) / C;
   if (p.max_tiles > kSmallMaxTiles) return false;
-  int ks = kSmallMaxWarps / p.max_tiles;
+  int ks = small_max_warps<F>() / p.max_tiles;
   if (ks > p.nsb) ks = p.nsb;
   p.sbs = (p.nsb + ks - 1) / ks;
   p.ks = (p.nsb + p.sbs - 1) / p.sbs;   // every slice has at least one super-block
@@ -4459,20 +4549,21 @@ bool launch_small_mt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cu
   return launched(cudaLaunchKernelEx(&cfg, gemv_small_mt<F>, p));
 }
 
-// 2..8-token launches that take it: Q4_K and Q4_G128 launches of fewer than
-// 32 M weights (the tiles must still fit one wave).
+// 2..8-token launches that take it: Q4_K, Q5_K and Q4_G128 launches of
+// fewer than 32 M weights (the tiles must still fit one wave).
 bool small_mt_eligible(int fmt, const GemvGroup& g, int K, int n_tok) {
-  if (n_tok < 2 || n_tok > 8 || (fmt != kQ4K && fmt != kG128)) return false;
+  if (n_tok < 2 || n_tok > 8 || (fmt != kQ4K && fmt != kQ5K && fmt != kG128)) return false;
   int64_t rows = 0;
   for (int i = 0; i < g.count; ++i) rows += g.N[i];
   return rows * K < (int64_t{1} << 25);
 }
 
-// Single-token launches that take the small-launch kernel: Q4_K and Q4_G128
-// launches of fewer than 32 M weights (the single-token tensor-core kernel
-// takes the larger ones), as long as they fit one wave (launch_small).
+// Single-token launches that take the small-launch kernel: Q4_K, Q5_K and
+// Q4_G128 launches of fewer than 32 M weights (the single-token tensor-core
+// kernel takes the larger Q4 ones), as long as they fit one wave
+// (launch_small).
 bool small_eligible(int fmt, const GemvGroup& g, int K, int n_tok) {
-  if (n_tok != 1 || (fmt != kQ4K && fmt != kG128)) return false;
+  if (n_tok != 1 || (fmt != kQ4K && fmt != kQ5K && fmt != kG128)) return false;
   int64_t rows = 0;
   for (int i = 0; i < g.count; ++i) rows += g.N[i];
   return rows * K < (int64_t{1} << 25);
@@ -4592,8 +4683,9 @@ StreamResult launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K
     }
     if (small_mt_eligible(fmt, g, K, n_tok)) {
       // needs no scratch
-      const bool ok = fmt == kQ4K ? launch_small_mt<kQ4K>(g, x, K, n_tok, s)
-                                  : launch_small_mt<kG128>(g, x, K, n_tok, s);
+      const bool ok = fmt == kQ4K   ? launch_small_mt<kQ4K>(g, x, K, n_tok, s)
+                      : fmt == kQ5K ? launch_small_mt<kQ5K>(g, x, K, n_tok, s)
+                                    : launch_small_mt<kG128>(g, x, K, n_tok, s);
       if (ok) return StreamResult::kLaunched;
     }
     bool ok = false;
@@ -4606,7 +4698,9 @@ StreamResult launch_stream(int fmt, const GemvGroup& g, const uint16_t* x, int K
     if (ok) return StreamResult::kLaunched;
   } else if (small_eligible(fmt, g, K, n_tok)) {
     // needs no scratch
-    const bool ok = fmt == kQ4K ? launch_small<kQ4K>(g, x, K, s) : launch_small<kG128>(g, x, K, s);
+    const bool ok = fmt == kQ4K   ? launch_small<kQ4K>(g, x, K, s)
+                    : fmt == kQ5K ? launch_small<kQ5K>(g, x, K, s)
+                                  : launch_small<kG128>(g, x, K, s);
     if (ok) return StreamResult::kLaunched;
   } else if (tc1_eligible(fmt, g, K, n_tok)) {
     const bool ok = fmt == kQ4K ? launch_tc1_fmt<kQ4K>(g, x, K, s, src, st)
