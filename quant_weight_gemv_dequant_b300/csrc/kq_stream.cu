@@ -4589,15 +4589,21 @@ bool launch_tcv_fmt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cud
 }
 
 // Single-token launches that take the tensor-core kernel: Q4_K and Q4_G128
-// matrices of at least 32 M weights (the MLP matrices of a decoder layer).
+// matrices of at least 32 M weights (the MLP matrices of a decoder layer)
+// with 64-row tiles for at least 60% of the SMs.  The kernel does not split
+// K, so a tall-skinny matrix leaves SMs idle: 5120 x 32768 Q4_K (80 tiles)
+// takes 34.7 us here against 31.6 us on gemv_stream, while 6656 rows (104
+// tiles) still run faster here (22.3 against 24.5 us at K = 19968).
 // Q5_K and Q6_K stay on gemv_stream: assembling their 5- and 6-bit fields
 // costs the A operand more integer instructions than the CUDA-core path
-// spends per weight, and the integer pipe is what bounds both kernels.
+// spends per weight (a Q5_K gate/up on this kernel: 57.3 against 58.7 us).
 bool tc1_eligible(int fmt, const GemvGroup& g, int K, int n_tok) {
   if (n_tok != 1 || (fmt != kQ4K && fmt != kG128)) return false;
   int64_t rows = 0;
   for (int i = 0; i < g.count; ++i) rows += g.N[i];
-  return rows * K >= (int64_t{1} << 25);
+  const DevInfo* di = dev_info();
+  const int64_t min_tiles = di != nullptr ? (3 * static_cast<int64_t>(di->sms) + 4) / 5 : 1;
+  return rows * K >= (int64_t{1} << 25) && (rows + 63) / 64 >= min_tiles;
 }
 
 template <int F>
