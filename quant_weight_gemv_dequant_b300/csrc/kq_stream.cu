@@ -3733,14 +3733,23 @@ constexpr int stream_max_per_sm() {
   return WC == 8 ? 2 : 3;
 }
 
+// Slabs of each of ksplit K segments of a row of slabs_row slabs: all equal
+// but the last, which may be shorter; 0 where that would leave the last
+// segment empty.
+inline int segment_slabs(int slabs_row, int ksplit) {
+  const int seg = (slabs_row + ksplit - 1) / ksplit;
+  return (ksplit - 1) * seg < slabs_row ? seg : 0;
+}
+
 template <int F, int NT, int RT, int WC, int XM>
 Plan make_plan(int K, int ksplit, bool tma) {
   using G = Geo<F, NT, RT, WC>;
   const size_t stage = stage_shape<G>(tma).bytes;
   Plan pl;
   const int slabs_row = (K / 256 + G::kSlabSB - 1) / G::kSlabSB;
-  if (slabs_row % ksplit != 0) return pl;
-  const int kpad = slabs_row / ksplit * G::kSlabK;
+  const int seg = segment_slabs(slabs_row, ksplit);
+  if (seg == 0) return pl;
+  const int kpad = seg * G::kSlabK;
   const size_t xb = XM == kXQ8 ? static_cast<size_t>(q8_x_bytes(NT, kpad, G::kPart))
                                : XLayout<F, NT, XM == kXBF16>::bytes(static_cast<size_t>(NT) * kpad) +
                                      static_cast<size_t>(NT) * (kpad / G::kPart) * 4;
@@ -3841,9 +3850,12 @@ bool launch_cfg(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStr
   p.K = K;
   p.nsb = K / 256;
   const int slabs_row = (p.nsb + G::kSlabSB - 1) / G::kSlabSB;
-  if (slabs_row % ksplit != 0) return false;
+  // the last segment may be shorter: its slabs past the row are copied as
+  // zeros (tensor copies) or not at all (row copies), and the consumers skip
+  // super-blocks past the row
+  p.slabs = segment_slabs(slabs_row, ksplit);
+  if (p.slabs == 0) return false;
   p.ksplit = ksplit;
-  p.slabs = slabs_row / ksplit;
   p.kpad = p.slabs * G::kSlabK;
   p.nt = n_tok;
   p.part = nullptr;
@@ -3962,7 +3974,9 @@ bool launch_rt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStre
   using G = Geo<F, NT, RT, WC>;
   // K segments: the fewest (a power of two dividing the slabs of a row, at
   // most 16) that reach the kernel's most CTAs per SM, else the fewest that
-  // reach the most CTAs per SM.
+  // reach the most CTAs per SM.  Where that leaves fewer than two (tile,
+  // segment) units per CTA (few rows, and a slab count with no such divisor,
+  // e.g. 31), more segments with a shorter last one.
   const int slabs_row = (K / 256 + G::kSlabSB - 1) / G::kSlabSB;
   const bool tma = tma_possible<G>(K);
   constexpr int kMaxPer = stream_max_per_sm<WC>();
@@ -4001,6 +4015,19 @@ bool launch_rt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStre
       }
     }
     if (best_ks == 0) return false;
+    const DevInfo* dip = dev_info();
+    int64_t tiles = 0;
+    for (int i = 0; i < g.count; ++i) tiles += (g.N[i] + G::kRows - 1) / G::kRows;
+    if (dip != nullptr) {
+      const int64_t slots = static_cast<int64_t>(best_sm) * dip->sms;
+      for (int ks = 2 * best_ks; ks <= 16 && tiles * best_ks < 2 * slots; ks *= 2) {
+        if (segment_slabs(slabs_row, ks) == 0) break;
+        const Plan pl = best_bf ? make_plan<F, NT, RT, WC, kXBF16>(K, ks, tma)
+                                : make_plan<F, NT, RT, WC, kXF32>(K, ks, tma);
+        if (pl.per_sm < best_sm) break;
+        best_ks = ks;
+      }
+    }
     for (int ks = best_ks;; ks = 1) {
       const bool ok = best_bf ? launch_cfg<F, NT, RT, WC, kXBF16>(g, x, K, n_tok, s, ks, tma, src, st)
                               : launch_cfg<F, NT, RT, WC, kXF32>(g, x, K, n_tok, s, ks, tma, src, st);

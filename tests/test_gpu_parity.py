@@ -94,13 +94,15 @@ def test_gemv_many_tiles_ragged_tail(kq, oracle, fmt):
 def test_gemv_long_rows(kq, oracle):
     # the largest K on the path (down projection) and beyond; at K = 98304 a
     # one-token small launch's warp slice (16 super-blocks) is wider than one
-    # tensor copy's box, so its rows are copied one by one
-    for fmt, K in ((2, 32768), (0, 65536), (0, 98304)):
+    # tensor copy's box, so its rows are copied one by one;
+    # K = 31744 (31 slabs of four super-blocks: no even split) takes K
+    # segments whose last one is shorter
+    for fmt, K in ((2, 32768), (0, 65536), (0, 98304), (2, 31744), (1, 31744)):
         N = 5
         Wb = weights(oracle, fmt, N, K, wl.derive_seed(104, fmt))
         x = wl.activations_bf16(wl.derive_seed(105), 4, K, heavy=True)
         yref, A = oracle.gemv(fmt, Wb, N, K, x)
-        for T in (1, 4):
+        for T in (1, 2, 4):
             assert_parity(gpu_gemv(kq, fmt, Wb, x[:T], N, K), yref[:T], A[:T],
                           f"fmt={fmt} K={K} n_tok={T}")
 
