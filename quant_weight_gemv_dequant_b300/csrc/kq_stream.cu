@@ -4018,14 +4018,23 @@ bool launch_rt(const GemvGroup& g, const uint16_t* x, int K, int n_tok, cudaStre
     const DevInfo* dip = dev_info();
     int64_t tiles = 0;
     for (int i = 0; i < g.count; ++i) tiles += (g.N[i] + G::kRows - 1) / G::kRows;
-    if (dip != nullptr) {
-      const int64_t slots = static_cast<int64_t>(best_sm) * dip->sms;
-      for (int ks = 2 * best_ks; ks <= 16 && tiles * best_ks < 2 * slots; ks *= 2) {
+    // two units per CTA of the plan?
+    auto enough = [&](int ks, int per_sm) {
+      return dip == nullptr || tiles * ks >= 2 * static_cast<int64_t>(per_sm) * dip->sms;
+    };
+    if (!enough(best_ks, best_sm)) {
+      // more segments (fp32 x: bf16 x with K split ran slower, e.g. 5120 x
+      // 31744 Q6_K 73.7 against 41.7 us), taken while they keep at least as
+      // many CTAs per SM
+      for (int ks = 2 * best_ks; ks <= 16; ks *= 2) {
         if (segment_slabs(slabs_row, ks) == 0) break;
-        const Plan pl = best_bf ? make_plan<F, NT, RT, WC, kXBF16>(K, ks, tma)
-                                : make_plan<F, NT, RT, WC, kXF32>(K, ks, tma);
-        if (pl.per_sm < best_sm) break;
-        best_ks = ks;
+        const Plan pl = make_plan<F, NT, RT, WC, kXF32>(K, ks, tma);
+        if (pl.per_sm > 0 && pl.per_sm >= best_sm) {
+          best_sm = pl.per_sm;
+          best_ks = ks;
+          best_bf = false;
+        }
+        if (best_sm == kMaxPer && enough(best_ks, best_sm)) break;
       }
     }
     for (int ks = best_ks;; ks = 1) {
