@@ -46,6 +46,27 @@ def test_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
     assert bench.profiled_traffic("k") is None
 
 
+def test_source_hash_covers_code_not_comments(tmp_path, monkeypatch):
+    csrc = tmp_path / "quant_weight_gemv_dequant_b300" / "csrc"
+    csrc.mkdir(parents=True)
+    code = "int f(int a) {\n  return a + 1;   // one more\n}\n/* block\n comment */\n"
+    (csrc / "k.cu").write_text(code)
+    (csrc / "notes.txt").write_text("not a kernel source")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    base = bench.kernel_source_sha()
+    # comments, blank lines and spacing do not count
+    (csrc / "k.cu").write_text("// header\n\nint f(int a) {\n    return a + 1;\n}\n")
+    assert bench.kernel_source_sha() == base
+    (csrc / "notes.txt").write_text("edited")
+    assert bench.kernel_source_sha() == base
+    # code does
+    (csrc / "k.cu").write_text("int f(int a) {\n  return a + 2;\n}\n")
+    assert bench.kernel_source_sha() != base
+    (csrc / "k.cu").write_text(code)
+    (csrc / "k2.cuh").write_text("#define X 1\n")
+    assert bench.kernel_source_sha() != base
+
+
 def test_committed_traffic_entry_is_well_formed():
     with open(os.path.join(ROOT, "profiles", "roofline_traffic.json")) as fh:
         d = json.load(fh)
